@@ -1,0 +1,300 @@
+/*
+ * oracle.c — plain, slow, fp64 CPU oracle for paged-KV attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg load this library.  It shares no code, header,
+ * table or helper with the CUDA library, and the CUDA library never calls it.
+ *
+ * What it computes (all in double precision, from inputs widened exactly from
+ * their stored fp32 / fp16 / bf16 encodings):
+ *
+ *   oracle_paged_decode — single-query attention of sequence s, head h over the
+ *     keys j in [start_s, ctx_s), each key gathered through the sequence's
+ *     block table:
+ *         x_j  = scale * (q . K_j + A[s,h,j])           (A absent -> 0)
+ *         out  = sum_j softmax(x)_j V_j
+ *     This is the formula of "PagedAttention: Support custom attention bias
+ *     for T5 model (1/2)", opening section: softmax((QK^T + A)/sqrt(d_k)) V,
+ *     with 1/sqrt(d_k) generalised to a caller-given scale that multiplies
+ *     the bias too.  A is the fully materialised bias padded to a row stride
+ *     (same page, first comment); a NULL A means no bias (same page, the
+ *     review answer on the optional pointer).  The block table is whichever
+ *     one the caller passes: decoder self-attention and encoder
+ *     cross-attention each have their own ("Add Encoder-decoder model support
+ *     and T5 Model support", the comments settling on two block tables).
+ *     start_s = max(0, ctx_s - W) for a window W > 0, else 0: the query is the
+ *     last token (position ctx_s - 1) and keeps the W most recent keys,
+ *     itself included ("[V1] Add sliding window support to Flex Attention
+ *     backend", causal sliding window).  ctx_s = 0 gives a zero row.
+ *
+ *   oracle_prefill — for every query row i of a packed variable-length batch
+ *     (cu_seqlens), softmax attention over the keys j of the same sequence
+ *     that the mask keeps, with r, c the positions inside the sequence:
+ *         window <= 0, causal = 0 : all j
+ *         window <= 0, causal = 1 : c <= r
+ *         window  > 0, causal = 0 : |r - c| < window   (bidirectional band)
+ *         window  > 0, causal = 1 : 0 <= r - c < window
+ *     ("[V1] Add sliding window support to Flex Attention backend":
+ *     bidirectional attention with a sliding window for encoder-only models.)
+ *
+ *   oracle_reshape_and_cache — the plain scatter of token rows into cache
+ *     blocks, cache[slot / bs, h, slot % bs, :] = key[t, h, :]; slot < 0 skips
+ *     the token.  Byte copies, so the result is exact.
+ *
+ * Cache layout (both oracle and library): [num_blocks, H, block_size, D].
+ *
+ * Work is spread over plain pthreads by (sequence, head) or (row, head); every
+ * output element is computed by exactly one thread in a fixed order, so the
+ * result does not depend on the thread count.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2 };
+
+/* ---- exact widening of the storage encodings ---------------------------- */
+
+static double half_bits_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int mant = h & 0x3ff;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)mant, -24);                 /* zero / subnormal */
+    else if (expo == 31)
+        v = mant ? NAN : INFINITY;
+    else
+        v = ldexp((double)(mant | 0x400), expo - 25);  /* (1.m) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+static double bf16_bits_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double load_elem(const void *base, size_t idx, int dtype)
+{
+    switch (dtype) {
+    case ORC_F32: return (double)((const float *)base)[idx];
+    case ORC_F16: return half_bits_to_double(((const uint16_t *)base)[idx]);
+    default:      return bf16_bits_to_double(((const uint16_t *)base)[idx]);
+    }
+}
+
+/* exported for the tests that pin the widening against numpy */
+double oracle_widen(const void *base, long long idx, int dtype)
+{
+    return load_elem(base, (size_t)idx, dtype);
+}
+
+/* ---- a tiny thread pool: run fn(i, ctx) for i in [0, n) ----------------- */
+
+typedef void (*item_fn)(long long i, void *ctx);
+
+struct pool_arg {
+    item_fn fn;
+    void *ctx;
+    long long n;
+    int tid, nthreads;
+};
+
+static void *pool_worker(void *p)
+{
+    struct pool_arg *a = (struct pool_arg *)p;
+    for (long long i = a->tid; i < a->n; i += a->nthreads)
+        a->fn(i, a->ctx);
+    return NULL;
+}
+
+static void run_items(item_fn fn, void *ctx, long long n, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if (n < nthreads) nthreads = (int)(n > 0 ? n : 1);
+    pthread_t th[256];
+    struct pool_arg args[256];
+    for (int t = 0; t < nthreads; ++t) {
+        args[t].fn = fn; args[t].ctx = ctx; args[t].n = n;
+        args[t].tid = t; args[t].nthreads = nthreads;
+    }
+    for (int t = 1; t < nthreads; ++t)
+        pthread_create(&th[t], NULL, pool_worker, &args[t]);
+    pool_worker(&args[0]);
+    for (int t = 1; t < nthreads; ++t)
+        pthread_join(th[t], NULL);
+}
+
+/* ---- softmax-weighted sum over an explicit list of logits --------------- */
+
+/* out[d] = sum_j exp(x_j - max x) V_j[d] / sum_j exp(x_j - max x).
+ * vrow(j) gives the element index of row j's first value.  n == 0 -> zeros. */
+static void softmax_combine(double *out, const double *x, const size_t *vrow, int n,
+                            const void *v, int dtype, int D)
+{
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (n == 0) return;
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) if (x[j] > m) m = x[j];
+    double l = 0.0;
+    for (int j = 0; j < n; ++j) {
+        double p = exp(x[j] - m);
+        l += p;
+        for (int d = 0; d < D; ++d) out[d] += p * load_elem(v, vrow[j] + d, dtype);
+    }
+    for (int d = 0; d < D; ++d) out[d] /= l;
+}
+
+/* ---- paged decode -------------------------------------------------------- */
+
+struct decode_ctx {
+    double *out;
+    const void *q, *k_cache, *v_cache;
+    const int32_t *block_tables, *context_lens;
+    const float *bias;
+    const int32_t *pairs;       /* optional list of (s, h) pairs */
+    int window;
+    double scale;
+    int block_size, num_seqs, num_heads, head_dim, max_blocks_per_seq, bias_row_stride, dtype;
+};
+
+static void decode_item(long long item, void *p)
+{
+    const struct decode_ctx *c = (const struct decode_ctx *)p;
+    const int H = c->num_heads, D = c->head_dim, bs = c->block_size;
+    int s, h;
+    if (c->pairs) { s = c->pairs[2 * item]; h = c->pairs[2 * item + 1]; }
+    else          { s = (int)(item / H); h = (int)(item % H); }
+    double *o = c->out + (size_t)item * D;
+    const int ctx = c->context_lens[s];
+    int start = 0;
+    if (c->window > 0 && ctx > c->window) start = ctx - c->window;
+    const int n = ctx > start ? ctx - start : 0;
+    double *x = (double *)malloc(sizeof(double) * (n > 0 ? n : 1));
+    size_t *vrow = (size_t *)malloc(sizeof(size_t) * (n > 0 ? n : 1));
+    const size_t qoff = ((size_t)s * H + h) * D;
+    for (int t = 0; t < n; ++t) {
+        const int j = start + t;
+        const int32_t blk = c->block_tables[(size_t)s * c->max_blocks_per_seq + j / bs];
+        const size_t row = (((size_t)blk * H + h) * bs + (j % bs)) * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += load_elem(c->q, qoff + d, c->dtype) * load_elem(c->k_cache, row + d, c->dtype);
+        double a = c->bias ? (double)c->bias[((size_t)s * H + h) * c->bias_row_stride + j] : 0.0;
+        x[t] = c->scale * (dot + a);
+        vrow[t] = row;
+    }
+    softmax_combine(o, x, vrow, n, c->v_cache, c->dtype, D);
+    free(x);
+    free(vrow);
+}
+
+/* out: double [num_items, D] where items are all (s, h) in s-major order when
+ * pairs == NULL, else the num_pairs listed (s, h) pairs in order. */
+void oracle_paged_decode(double *out, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, const int32_t *context_lens,
+                         const float *bias, int window, double scale, int block_size,
+                         int num_seqs, int num_heads, int head_dim, int max_blocks_per_seq,
+                         int bias_row_stride, int dtype, const int32_t *pairs, int num_pairs,
+                         int nthreads)
+{
+    struct decode_ctx c = {out, q, k_cache, v_cache, block_tables, context_lens, bias, pairs,
+                           window, scale, block_size, num_seqs, num_heads, head_dim,
+                           max_blocks_per_seq, bias_row_stride, dtype};
+    long long n = pairs ? num_pairs : (long long)num_seqs * num_heads;
+    run_items(decode_item, &c, n, nthreads);
+}
+
+/* ---- packed varlen prefill ---------------------------------------------- */
+
+struct prefill_ctx {
+    double *out;
+    const void *q, *k, *v;
+    const int32_t *cu_seqlens;
+    const int64_t *rows;        /* optional list of token rows */
+    int num_seqs, num_heads, head_dim, window, causal, dtype;
+    double scale;
+};
+
+static int mask_keeps(int r, int c, int window, int causal)
+{
+    if (causal && c > r) return 0;
+    if (window > 0) {
+        int d = r - c;
+        if (d < 0) d = -d;
+        if (d >= window) return 0;
+    }
+    return 1;
+}
+
+static void prefill_item(long long item, void *p)
+{
+    const struct prefill_ctx *c = (const struct prefill_ctx *)p;
+    const int H = c->num_heads, D = c->head_dim;
+    const long long row_i = item / H;
+    const int h = (int)(item % H);
+    const long long i = c->rows ? c->rows[row_i] : row_i;
+    int b = 0;
+    while (b + 1 <= c->num_seqs && c->cu_seqlens[b + 1] <= i) ++b;
+    const long long s0 = c->cu_seqlens[b];
+    const int L = c->cu_seqlens[b + 1] - c->cu_seqlens[b];
+    const int r = (int)(i - s0);
+    double *o = c->out + (size_t)item * D;
+    double *x = (double *)malloc(sizeof(double) * (L > 0 ? L : 1));
+    size_t *vrow = (size_t *)malloc(sizeof(size_t) * (L > 0 ? L : 1));
+    int n = 0;
+    const size_t qoff = ((size_t)i * H + h) * D;
+    for (int col = 0; col < L; ++col) {
+        if (!mask_keeps(r, col, c->window, c->causal)) continue;
+        const size_t row = ((size_t)(s0 + col) * H + h) * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += load_elem(c->q, qoff + d, c->dtype) * load_elem(c->k, row + d, c->dtype);
+        x[n] = c->scale * dot;
+        vrow[n] = row;
+        ++n;
+    }
+    softmax_combine(o, x, vrow, n, c->v, c->dtype, D);
+    free(x);
+    free(vrow);
+}
+
+/* out: double [num_rows, H, D] for the listed token rows (rows == NULL: all
+ * cu_seqlens[num_seqs] rows in order). */
+void oracle_prefill(double *out, const void *q, const void *k, const void *v,
+                    const int32_t *cu_seqlens, int num_seqs, int num_heads, int head_dim,
+                    int window, int causal, double scale, int dtype,
+                    const int64_t *rows, long long num_rows, int nthreads)
+{
+    struct prefill_ctx c = {out, q, k, v, cu_seqlens, rows, num_seqs, num_heads, head_dim,
+                            window, causal, dtype, scale};
+    long long nr = rows ? num_rows : (long long)cu_seqlens[num_seqs];
+    run_items(prefill_item, &c, nr * num_heads, nthreads);
+}
+
+/* ---- reshape_and_cache --------------------------------------------------- */
+
+void oracle_reshape_and_cache(void *k_cache, void *v_cache, const void *key, const void *value,
+                              const int64_t *slot_mapping, long long num_tokens, int num_heads,
+                              int head_dim, int block_size, int elt_bytes)
+{
+    const size_t rowb = (size_t)head_dim * elt_bytes;
+    for (long long t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        const int64_t blk = slot / block_size, off = slot % block_size;
+        for (int h = 0; h < num_heads; ++h) {
+            const size_t src = ((size_t)t * num_heads + h) * rowb;
+            const size_t dst = (((size_t)blk * num_heads + h) * block_size + off) * rowb;
+            memcpy((char *)k_cache + dst, (const char *)key + src, rowb);
+            memcpy((char *)v_cache + dst, (const char *)value + src, rowb);
+        }
+    }
+}
