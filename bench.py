@@ -1,0 +1,691 @@
+#!/usr/bin/env python
+"""bench.py — throughput of the paged-KV attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl pka|reference]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the hot path over one
+batch of seeded synthetic input, already resident in HBM:
+
+  t5-small-decode (default)  reshape_and_cache of each sequence's new token,
+        then biased paged decode: 64 seqs x 8 heads x 64, bf16, contexts
+        U[1,512], T5 bias [64,8,512] materialised from an [8,129] table.
+  tiny-decode        4 x 2 x 64 fp32, contexts U[1,64], Gaussian bias.
+  t5-large-decode    decoder self-attention (256 x 16 x 64 bf16, contexts
+        U[1,2048], T5 bias padded to 2048) + encoder cross-attention (own block
+        table, encoder length 512, no bias), each after its reshape_and_cache.
+  long-ctx-decode    512 x 16 x 128 fp16, contexts log-U[16,8192], causal
+        window 4096, bias [512,16,8192] N(0,0.25) NaN-padded.
+  encoder-prefill    32 packed sequences U[128,8192], 12 heads x 64 bf16,
+        three layers: full, window 64, window 64 (bidirectional).
+
+metric/unit: decode workloads report algorithmic KV+bias bytes per second
+(GB/s); the prefill workload reports TFLOP/s (4*D per kept (query, key) pair
+per head).  Inputs smaller than 3x L2 are rotated over enough copies that
+every step reads cold data.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload, in the same unit.
+N > 1 (torchrun): every rank runs its own replica (weak scaling; no
+collective on the data path); time = max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth import BF16, F16, F32, ELT_BYTES  # noqa: E402
+
+METRIC = "decode KV+bias GB/s (% of HBM peak) and seqs/sec, bias on/off; prefill TFLOPS"
+L2_BYTES = 129 * 1024 * 1024
+DECODE_WORKLOADS = {"tiny-decode": 1, "t5-small-decode": 2, "t5-large-decode": 3, "long-ctx-decode": 5}
+
+
+# ---------------------------------------------------------------------------
+# plumbing
+# ---------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+def kernel_source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "paged_kv_attention_23_gb300", "csrc", name)
+    return hashlib.sha1(open(path, "rb").read()).hexdigest()[:12]
+
+
+def recorded_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel source changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    h = kernel_source_hash(kernel_file)
+    for line in open(p):
+        f = line.split()
+        if len(f) >= 4 and not line.startswith("#") and f[0] == kernel_file and f[1] == workload and f[3] == h:
+            return float(f[2])
+    return None
+
+
+def gpu_id(local: int) -> str:
+    """nvidia-smi's id of this rank's GPU (index or UUID)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x.strip() for x in vis.split(",") if x.strip()]
+    return ids[local] if local < len(ids) else str(local)
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled every 200 ms."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0])); mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# decode workloads
+# ---------------------------------------------------------------------------
+def decode_alg_bytes(case, bias_on: bool) -> dict:
+    """Algorithmic bytes of one decode call: visible K and V rows, bias
+    entries of visible keys, q and out rows, block-table entries, context
+    lengths."""
+    n = case.visible().astype(np.int64)
+    H, D, elt = case.num_heads, case.head_dim, ELT_BYTES[case.dtype]
+    kv = int((2 * H * n * D * elt).sum())
+    bias = int((4 * H * n).sum()) if (bias_on and case.bias is not None) else 0
+    other = int(case.num_seqs * 2 * H * D * elt + (4 * ((n + case.block_size - 1) // case.block_size)).sum()
+                + 4 * case.num_seqs)
+    return {"kv": kv, "bias": bias, "other": other, "total": kv + bias + other}
+
+
+def _tdt(code):
+    import torch
+    return {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}[code]
+
+
+def _dev(arr, code, device):
+    import torch
+    a = np.ascontiguousarray(arr)
+    if code == BF16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+class DecodeSide:
+    """One decode call's device state (one attention type), with its new-token
+    inputs for reshape_and_cache."""
+
+    def __init__(self, case, pka, device):
+        import torch
+        self.case = case
+        H, D, bs = case.num_heads, case.head_dim, case.block_size
+        tdt = _tdt(case.dtype)
+        if case.device_kv is not None:
+            key, value = case.device_kv
+        else:
+            key, value = _dev(case.key, case.dtype, device), _dev(case.value, case.dtype, device)
+        self.kc = torch.zeros((case.num_blocks, H, bs, D), dtype=tdt, device=device)
+        self.vc = torch.zeros_like(self.kc)
+        pka.reshape_and_cache(key, value, self.kc, self.vc, torch.from_numpy(case.slot_mapping).to(device))
+        # the step's new token per sequence = its last context position
+        last = np.where(case.context_lens > 0, case.tok_offsets[1:] - 1, 0)
+        idx = torch.from_numpy(last.astype(np.int64)).to(device)
+        self.new_k = key[idx].contiguous()
+        self.new_v = value[idx].contiguous()
+        slots = (np.where(case.context_lens > 0, case.slot_mapping[last], -1) if case.num_tokens
+                 else np.full(case.num_seqs, -1))
+        self.slots = torch.from_numpy(slots.astype(np.int64)).to(device)
+        self.q = _dev(case.q, case.dtype, device)
+        self.bt = torch.from_numpy(np.ascontiguousarray(case.block_tables)).to(device)
+        self.cl = torch.from_numpy(case.context_lens).to(device)
+        self.bias = torch.from_numpy(case.bias).to(device) if case.bias is not None else None
+        self.out = torch.empty((case.num_seqs, H, D), dtype=tdt, device=device)
+        self.ws = torch.zeros(pka.paged_attn_decode_workspace_size(case.num_seqs, H, D, case.max_context_len,
+                                                                   case.window), dtype=torch.uint8, device=device)
+        del key, value
+
+    def clone(self):
+        import copy
+        c = copy.copy(self)
+        for n in ("kc", "vc", "new_k", "new_v", "slots", "q", "bt", "cl", "out"):
+            setattr(c, n, getattr(self, n).clone())
+        c.bias = self.bias.clone() if self.bias is not None else None
+        return c
+
+    def nbytes(self):
+        ts = [self.kc, self.vc, self.q, self.bt, self.new_k, self.new_v] + ([self.bias] if self.bias is not None else [])
+        return sum(t.numel() * t.element_size() for t in ts)
+
+    def reshape(self, pka):
+        pka.reshape_and_cache(self.new_k, self.new_v, self.kc, self.vc, self.slots)
+
+    def decode(self, pka, bias_on=True):
+        c = self.case
+        pka.paged_attn_decode(self.out, self.q, self.kc, self.vc, self.bt, self.cl,
+                              self.bias if bias_on else None, c.window, c.scale, max_context_len=c.max_context_len,
+                              workspace=self.ws)
+
+
+def build_decode_sides(workload, device, on_device_draw):
+    n = DECODE_WORKLOADS[workload]
+    dev = device if on_device_draw else None
+    cases = [synth.decode_workload(n, device=dev)]
+    if n == 3:
+        cases.append(synth.cross_workload(device=dev))
+    return cases
+
+
+def run_decode(args, rank, world, local, peaks):
+    import torch
+    import paged_kv_attention_23_gb300 as pka
+    pka.load()
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    big = args.workload in ("t5-large-decode", "long-ctx-decode")
+    cases = build_decode_sides(args.workload, device, big)
+    sides = [DecodeSide(c, pka, device) for c in cases]
+    bytes_on = [decode_alg_bytes(c, True) for c in cases]
+    bytes_off = [decode_alg_bytes(c, False) for c in cases]
+    step_bytes = sum(b["total"] for b in bytes_on)
+    per_copy = sum(s.nbytes() for s in sides)
+    copies = max(1, min(16, math.ceil(3 * L2_BYTES / per_copy)))
+    rot = [sides] + [[s.clone() for s in sides] for _ in range(copies - 1)]
+    torch.cuda.synchronize()
+
+    def step(i, bias_on=True, events=None):
+        for j, s in enumerate(rot[i % copies]):
+            s.reshape(pka)
+            if events is not None:
+                events[j][0][i].record()
+            s.decode(pka, bias_on and s.bias is not None)
+            if events is not None:
+                events[j][1][i].record()
+
+    clocks = ClockSampler(gpu_id(local))
+    clocks.start()
+    t_end = time.time() + args.clock_soak                       # clock soak (untimed)
+    i = 0
+    while time.time() < t_end:
+        step(i); i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    for w in range(args.warmup):
+        step(w)
+    K = args.steps
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(K)] for _ in range(2)] for _ in sides]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(); barrier(world)
+    t0.record()
+    for k in range(K):
+        step(k, True, ev)
+    t1.record()
+    torch.cuda.synchronize(); barrier(world)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    ms_step = total_ms / K
+    launch_ms = [statistics.mean(ev[j][0][k].elapsed_time(ev[j][1][k]) for k in range(K)) for j in range(len(sides))]
+
+    # bias off (same shapes), decode launches only
+    torch.cuda.synchronize()
+    off_ms = None
+    if any(s.bias is not None for s in sides):
+        ev2 = [[[torch.cuda.Event(enable_timing=True) for _ in range(K)] for _ in range(2)] for _ in sides]
+        for w in range(args.warmup):
+            step(w, False)
+        for k in range(K):
+            step(k, False, ev2)
+        torch.cuda.synchronize()
+        off_ms = sum(statistics.mean(ev2[j][0][k].elapsed_time(ev2[j][1][k]) for k in range(K))
+                     for j in range(len(sides)))
+
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    # dominant kernel: the decode launch carrying the most bytes
+    jd = int(np.argmax([b["total"] for b in bytes_on]))
+    achieved = bytes_on[jd]["total"] / (launch_ms[jd] * 1e-3) / 1e9
+    traffic = recorded_traffic("paged_decode.cu", args.workload)
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+            "kernel": "paged_decode_kernel", "alg_bytes_per_launch": bytes_on[jd]["total"],
+            "launch_ms": round(launch_ms[jd], 5), "peak_src": peaks["src"] + " hbm_gbs (copy)"}
+    e2e = decode_e2e(args, sides, pka, step_bytes, world) if not args.no_e2e else None
+    seqs = sum(c.num_seqs for c in cases[:1])
+    extra = {
+        "decode_ms_per_launch": [round(x, 5) for x in launch_ms],
+        "decode_GBps_per_launch": [round(b["total"] / (m * 1e-3) / 1e9, 1) for b, m in zip(bytes_on, launch_ms)],
+        "kv_GBps": round(sum(b["kv"] for b in bytes_on) / (sum(launch_ms) * 1e-3) / 1e9, 1),
+        "seqs_per_s": round(seqs / (sum(launch_ms) * 1e-3), 1),
+        "bias_off_decode_GBps": (round(sum(b["total"] for b in bytes_off) / (off_ms * 1e-3) / 1e9, 1)
+                                 if off_ms else None),
+        "bias_off_seqs_per_s": round(seqs / (off_ms * 1e-3), 1) if off_ms else None,
+        "alg_bytes_per_step": step_bytes,
+    }
+    cfg = {"workload": args.workload, "num_seqs": [c.num_seqs for c in cases], "num_heads": cases[0].num_heads,
+           "head_dim": cases[0].head_dim, "block_size": 16,
+           "window": [c.window for c in cases], "bias": [c.bias is not None for c in cases],
+           "l2": f"inputs rotated over {copies} copies ({per_copy * copies / 2**20:.0f} MiB > L2)"
+           if copies > 1 else f"inputs {per_copy / 2**20:.0f} MiB > L2", "parallelism": f"replicas x{world}"}
+    return {"value": value, "unit": "GB/s", "ms_per_step": ms_step, "dtype": synth.DTYPE_NAMES[cases[0].dtype],
+            "config": cfg, "roofline": roof, "e2e": e2e, "clocks": clk,
+            "gpu_launches": K * 2 * len(sides), "extra": extra, "cases": cases}
+
+
+def decode_e2e(args, sides, pka, step_bytes, world):
+    """The same step through the public API from pinned host buffers: copy the
+    step's inputs host->device, run it, read the output back."""
+    import torch
+    host_in = []
+    h2d = 0
+    for s in sides:
+        names = ["q", "new_k", "new_v", "slots", "bt", "cl"] + (["bias"] if s.bias is not None else [])
+        pairs = []
+        for n in names:
+            d = getattr(s, n)
+            h = torch.empty(d.shape, dtype=d.dtype, pin_memory=True)
+            h.copy_(d)
+            pairs.append((h, d))
+            h2d += d.numel() * d.element_size()
+        host_in.append(pairs)
+    outs = [torch.empty(s.out.shape, dtype=s.out.dtype, pin_memory=True) for s in sides]
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def step():
+        for s, pairs, o in zip(sides, host_in, outs):
+            for h, d in pairs:
+                d.copy_(h, non_blocking=True)
+            s.reshape(pka)
+            s.decode(pka, s.bias is not None)
+            o.copy_(s.out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(); barrier(world)
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize(); barrier(world)
+    ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
+    return {"value": round(step_bytes * world / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 5)}
+
+
+# ---------------------------------------------------------------------------
+# prefill workload
+# ---------------------------------------------------------------------------
+def prefill_flops(case) -> int:
+    return 4 * case.head_dim * case.num_heads * case.visible_pairs()
+
+
+def run_prefill(args, rank, world, local, peaks):
+    import torch
+    import paged_kv_attention_23_gb300 as pka
+    pka.load()
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    layers = [synth.prefill_workload(l, device=device) for l in range(3)]
+    flops = [prefill_flops(c) for c in layers]
+    cu = torch.from_numpy(layers[0].cu_seqlens).to(device)
+    outs = [torch.empty_like(c.device_qkv[0]) for c in layers]
+
+    def step(events=None, k=0):
+        for j, c in enumerate(layers):
+            q, kk, v = c.device_qkv
+            if events is not None:
+                events[j][0][k].record()
+            pka.swa_prefill(outs[j], q, kk, v, cu, c.max_seqlen, c.window, c.causal, c.scale)
+            if events is not None:
+                events[j][1][k].record()
+
+    clocks = ClockSampler(gpu_id(local))
+    clocks.start()
+    t_end = time.time() + args.clock_soak
+    while time.time() < t_end:
+        step(); torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step()
+    K = args.steps
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(K)] for _ in range(2)] for _ in layers]
+    t0 = torch.cuda.Event(enable_timing=True); t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(); barrier(world)
+    t0.record()
+    for k in range(K):
+        step(ev, k)
+    t1.record()
+    torch.cuda.synchronize(); barrier(world)
+    clk = clocks.stop()
+    ms_step = max_over_ranks(t0.elapsed_time(t1), world) / K
+    launch_ms = [statistics.mean(ev[j][0][k].elapsed_time(ev[j][1][k]) for k in range(K)) for j in range(3)]
+    value = sum(flops) * world / (ms_step * 1e-3) / 1e12
+    ach = flops[0] / (launch_ms[0] * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    qkv_bytes = [4 * c.num_tokens * c.num_heads * c.head_dim * 2 for c in layers]
+    roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(ach / peak, 4), "traffic": recorded_traffic("swa_prefill.cu", args.workload),
+            "kernel": "swa_prefill (full-attention layer)", "alg_flops_per_launch": flops[0],
+            "launch_ms": round(launch_ms[0], 4), "peak_src": peaks["src"] + " bf16_tflops (burst)"}
+    extra = {"layer_ms": [round(x, 4) for x in launch_ms],
+             "layer_TFLOPs": [round(f / (m * 1e-3) / 1e12, 2) for f, m in zip(flops, launch_ms)],
+             "window_layer_GBps": [round(b / (m * 1e-3) / 1e9, 1) for b, m in zip(qkv_bytes[1:], launch_ms[1:])],
+             "window_layer_hbm_frac": [round(b / (m * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+                                       for b, m in zip(qkv_bytes[1:], launch_ms[1:])],
+             "flops_per_step": sum(flops)}
+    e2e = prefill_e2e(args, layers, pka, cu, outs, sum(flops), world) if not args.no_e2e else None
+    cfg = {"workload": args.workload, "num_seqs": layers[0].num_seqs, "num_tokens": layers[0].num_tokens,
+           "num_heads": 12, "head_dim": 64, "windows": [c.window for c in layers], "causal": 0,
+           "l2": f"q/k/v {qkv_bytes[0] * 3 / 4 / 2**20:.0f} MiB per layer > L2", "parallelism": f"replicas x{world}"}
+    return {"value": value, "unit": "TFLOP/s", "ms_per_step": ms_step, "dtype": "bf16", "config": cfg,
+            "roofline": roof, "e2e": e2e, "clocks": clk, "gpu_launches": 3 * K, "extra": extra, "cases": layers}
+
+
+def prefill_e2e(args, layers, pka, cu, outs, flops, world):
+    import torch
+    hosts = []
+    h2d = cu.numel() * 4
+    for c in layers:
+        hs = []
+        for t in c.device_qkv:
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            hs.append(h)
+            h2d += t.numel() * t.element_size()
+        hosts.append(hs)
+    hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def step():
+        for c, hs, o, ho in zip(layers, hosts, outs, hout):
+            for h, d in zip(hs, c.device_qkv):
+                d.copy_(h, non_blocking=True)
+            q, k, v = c.device_qkv
+            pka.swa_prefill(o, q, k, v, cu, c.max_seqlen, c.window, c.causal, c.scale)
+            ho.copy_(o, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(); barrier(world)
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize(); barrier(world)
+    ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
+    return {"value": round(flops * world / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+def _host_sub_decode(case, seqs):
+    """Host arrays for a subset of sequences (token rows from the generator)."""
+    if case.device_kv is None and len(seqs) == case.num_seqs:
+        return case
+    ks, vs = [], []
+    for s in seqs:
+        a, b = int(case.tok_offsets[s]), int(case.tok_offsets[s + 1])
+        if case.device_kv is not None:
+            ks.append(_host_storage(case.device_kv[0][a:b], case.dtype))
+            vs.append(_host_storage(case.device_kv[1][a:b], case.dtype))
+        else:
+            ks.append(case.key[a:b]); vs.append(case.value[a:b])
+    ctx = case.context_lens[seqs]
+    pool, bt, slot, tok = synth._paged_layout(np.random.default_rng(0), ctx, case.block_size)
+    return synth.DecodeCase(case.name, case.dtype, len(seqs), case.num_heads, case.head_dim, case.block_size, pool,
+                            ctx.astype(np.int32), bt, slot, tok, case.q[seqs], np.concatenate(ks),
+                            np.concatenate(vs), case.bias[seqs] if case.bias is not None else None, case.window,
+                            case.scale)
+
+
+def _host_storage(t, code):
+    import torch
+    t = t.detach().contiguous().cpu()
+    return t.view(torch.int16).numpy().view(np.uint16) if code == BF16 else t.numpy()
+
+
+def oracle_decode_sample(cases, budget_s: float, seed: int = 0):
+    """Time the oracle on seeded random sequences of each case until about
+    budget_s seconds of CPU work; returns (bytes, seconds, threads, desc)."""
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(seed)
+    threads = oracle.default_threads()
+    total_b = 0
+    total_s = 0.0
+    nseq = 0
+    c0 = cases[0]
+    t_start = time.time()
+    while time.time() - t_start < budget_s:
+        for c in cases:
+            k = min(c.num_seqs, 8)
+            seqs = np.sort(rng.choice(c.num_seqs, size=k, replace=False))
+            sub = _host_sub_decode(c, seqs)
+            kc = np.zeros((sub.num_blocks, sub.num_heads, 16, sub.head_dim), dtype=sub.key.dtype)
+            vc = np.zeros_like(kc)
+            t = time.time()
+            oracle.reshape_and_cache(kc, vc, sub.key, sub.value, sub.slot_mapping, 16)
+            oracle.paged_decode(sub.q, kc, vc, sub.block_tables, sub.context_lens, sub.bias, sub.window, sub.scale,
+                                16, sub.dtype, nthreads=threads)
+            total_s += time.time() - t
+            total_b += decode_alg_bytes(sub, True)["total"]
+            nseq += k
+    desc = (f"{nseq} sequences drawn at random (all heads) from the {c0.name} batch, "
+            f"oracle scatter + fp64 paged decode, {total_s:.1f} s")
+    return total_b, total_s, threads, desc
+
+
+def oracle_prefill_sample(layers, budget_s: float, seed: int = 0):
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(seed)
+    threads = oracle.default_threads()
+    host = [[_host_storage(t, BF16) for t in c.device_qkv] if c.device_qkv is not None else [c.q, c.k, c.v]
+            for c in layers]
+    flops = 0
+    secs = 0.0
+    nrows = 0
+    t_start = time.time()
+    while time.time() - t_start < budget_s:
+        for c, (q, k, v) in zip(layers, host):
+            rows = np.sort(rng.choice(c.num_tokens, size=64, replace=False)).astype(np.int64)
+            t = time.time()
+            oracle.prefill(q, k, v, c.cu_seqlens, c.window, c.causal, c.scale, BF16, rows=rows, nthreads=threads)
+            secs += time.time() - t
+            flops += 4 * c.head_dim * c.num_heads * _kept_keys(c, rows)
+            nrows += len(rows)
+    desc = f"{nrows} query rows drawn at random over the 3 layers (all heads), fp64 oracle, {secs:.1f} s"
+    return flops, secs, threads, desc
+
+
+def _kept_keys(c, rows):
+    cu = c.cu_seqlens
+    tot = 0
+    for i in rows:
+        b = int(np.searchsorted(cu, i, side="right") - 1)
+        L = int(cu[b + 1] - cu[b]); r = int(i - cu[b])
+        if c.window > 0:
+            lo, hi = max(0, r - c.window + 1), min(L - 1, r + c.window - 1)
+        else:
+            lo, hi = 0, L - 1
+        if c.causal:
+            hi = min(hi, r)
+        tot += hi - lo + 1
+    return tot
+
+
+def cpu_baseline(res, args):
+    budget = args.cpu_seconds
+    if args.workload == "encoder-prefill":
+        f, s, th, desc = oracle_prefill_sample(res["cases"], budget)
+        return {"value": round(f / s / 1e12, 6), "unit": "TFLOP/s", "cores": th, "kind": "oracle", "sample": desc}
+    b, s, th, desc = oracle_decode_sample(res["cases"], budget)
+    return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": th, "kind": "oracle", "sample": desc}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the fp64 CPU oracle, timed on the host cores on a
+    bounded sample per step."""
+    if rank != 0:
+        return None
+    if args.workload == "encoder-prefill":
+        layers = [synth.prefill_workload(l) for l in range(3)]
+        per = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
+        oracle_prefill_sample(layers, 0.5)
+        f, s, th, desc = oracle_prefill_sample(layers, per * args.steps)
+        val, unit = f / s / 1e12, "TFLOP/s"
+        cfg = {"workload": args.workload}
+        dt = "f64"
+    else:
+        n = DECODE_WORKLOADS[args.workload]
+        cases = [synth.decode_workload(n)] + ([synth.cross_workload()] if n == 3 else [])
+        per = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
+        oracle_decode_sample(cases, 0.5)
+        b, s, th, desc = oracle_decode_sample(cases, per * args.steps)
+        val, unit = b / s / 1e9, "GB/s"
+        cfg = {"workload": args.workload}
+        dt = "f64"
+    line = {"metric": METRIC, "value": round(val, 6), "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(s * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic", "config": cfg,
+            "impl": "reference",
+            "cpu_baseline": {"value": round(val, 6), "unit": unit, "cores": th, "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(val, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return line
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
+    ap.add_argument("--workload", default="t5-small-decode",
+                    choices=sorted(DECODE_WORKLOADS) + ["encoder-prefill"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--clock-soak", type=float, default=1.5,
+                    help="seconds of untimed steps while nvidia-smi samples clocks before the warm-up")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    peaks = measured_peaks()
+    if args.workload == "encoder-prefill":
+        res = run_prefill(args, rank, world, local, peaks)
+    else:
+        res = run_decode(args, rank, world, local, peaks)
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(res, args)
+    line = {"metric": METRIC, "value": round(res["value"], 3), "unit": res["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": res["dtype"],
+            "data": "synthetic (seeded)", "config": res["config"], "roofline": res["roofline"],
+            "cpu_baseline": cpu, "e2e": res["e2e"], "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
+            "extra": res["extra"]}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,188 @@
+/*
+ * pka.h — C ABI of libpka.so: paged-KV attention kernels for GB300 (sm_103a).
+ *
+ * The operation is softmax((Q K^T + A) / sqrt(d_k)) V as written in
+ * "PagedAttention: Support custom attention bias for T5 model (1/2)" (opening
+ * section), with 1/sqrt(d_k) passed in as `scale`, which multiplies the bias
+ * as well.  K and V live in a paged cache and are reached through per-sequence
+ * block tables; decoder self-attention and encoder cross-attention each use
+ * their own table and are two calls ("Add Encoder-decoder model support and
+ * T5 Model support", the comments that settle on two block tables).  The
+ * optional sliding window follows "[V1] Add sliding window support to Flex
+ * Attention backend": causal for decode, bidirectional for encoder prefill.
+ *
+ * Conventions shared by every entry point
+ *  - Every pointer argument is a DEVICE pointer owned by the caller; the
+ *    library never allocates, frees or keeps a pointer after the call.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and runs asynchronously.  Outputs are valid once that work has
+ *    completed.
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns PKA_ERR_INVALID_ARG (or PKA_ERR_UNSUPPORTED for a legal
+ *    but unimplemented shape / dtype) and launches nothing.  A failed launch
+ *    returns PKA_ERR_CUDA.
+ *  - Data-dependent checks (a block id outside [0, num_blocks), a context
+ *    length outside [0, max_context_len]) happen on the device: the kernel
+ *    never reads or writes outside the buffers described by the size
+ *    arguments, ORs a PKA_DEVCHK_* bit into *status (when status != NULL) and
+ *    produces unspecified values for the affected rows.  The caller reads
+ *    *status after synchronising; the library never synchronises.
+ *  - Alignment: q, out, key, value, k, v, k_cache and v_cache must be 16-byte
+ *    aligned; attn_bias 4-byte aligned; integer arrays naturally aligned.
+ *  - Cache layout: [num_blocks, num_heads, block_size, head_dim], row-major;
+ *    one (block, head) is one contiguous block_size * head_dim run.
+ *  - Supported now: head_dim in {64, 128}; block_size 16; num_kv_heads ==
+ *    num_heads.  Decode: f32, f16, bf16 (q, caches and out share one dtype;
+ *    the bias is always f32).  Prefill: bf16, head_dim 64.
+ */
+#ifndef PKA_H
+#define PKA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKA_API __attribute__((visibility("default")))
+#else
+#define PKA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKA_OK = 0,
+    PKA_ERR_INVALID_ARG = 1,
+    PKA_ERR_UNSUPPORTED = 2,
+    PKA_ERR_CUDA = 3,
+    PKA_ERR_WORKSPACE = 4   /* workspace NULL, misaligned or smaller than required */
+} pka_status;
+
+typedef enum { PKA_F32 = 0, PKA_F16 = 1, PKA_BF16 = 2 } pka_dtype;
+
+/* Bits the kernels OR into the optional device status word. */
+#define PKA_DEVCHK_BLOCK_ID     0x1  /* a block-table entry outside [0, num_blocks) */
+#define PKA_DEVCHK_CONTEXT_LEN  0x2  /* a context length < 0, > max_context_len or
+                                        > max_blocks_per_seq * block_size */
+#define PKA_DEVCHK_SLOT         0x4  /* a slot >= num_blocks * block_size */
+#define PKA_DEVCHK_TIMEOUT      0x8  /* a pipeline wait gave up (a copy never landed) */
+#define PKA_DEVCHK_CU_SEQLENS   0x10 /* cu_seqlens not non-decreasing within [0, num_tokens] */
+
+/* Human-readable name of a status code (static string, never NULL). */
+PKA_API const char *pka_status_string(pka_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+PKA_API int pka_version(void);
+
+/*
+ * pka_reshape_and_cache — scatter new K/V token rows into the paged caches:
+ *   k_cache[slot / block_size, h, slot % block_size, :] = key[t, h, :]
+ *   v_cache[...same...]                                  = value[t, h, :]
+ * with slot = slot_mapping[t]; slot < 0 skips token t (padding).  This is the
+ * KV-caching step that "Add Encoder-decoder model support and T5 Model
+ * support" lists for cross-attention (its split-out "Cross-attention KV
+ * caching and memory-management" item), for the blocks that the block tables
+ * of either attention type point at.
+ *
+ *   key, value    [num_tokens, num_heads, head_dim] of dtype, contiguous
+ *   k_cache, v_cache [num_blocks, num_heads, block_size, head_dim] of dtype
+ *   slot_mapping  int64 [num_tokens]
+ *   status        int32 device word or NULL (PKA_DEVCHK_SLOT on a slot past
+ *                 the cache; that token is skipped)
+ * Exact: the cache receives the bytes of key/value unchanged.  Two tokens that
+ * map to the same slot leave one of them (unspecified which).
+ * num_tokens == 0 is a no-op.
+ */
+PKA_API pka_status pka_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
+                                 const int64_t *slot_mapping, int num_tokens, int num_heads,
+                                 int head_dim, int block_size, int num_blocks, pka_dtype dtype,
+                                 int32_t *status, void *stream);
+
+/*
+ * pka_paged_attn_decode — one query token per sequence against its paged
+ * K/V ("PagedAttention: Support custom attention bias for T5 model (1/2)":
+ * the paged kernel with the optional bias pointer).  For sequence s, head h:
+ *   ctx   = context_lens[s]  (keys 0 .. ctx-1; the query is token ctx-1)
+ *   start = sliding_window > 0 ? max(0, ctx - sliding_window) : 0
+ *   x_j   = scale * (q[s,h,:] . K_j + A[s,h,j])      for j in [start, ctx)
+ *   out[s,h,:] = sum_j softmax(x)_j V_j                (ctx == 0: zeros)
+ * with K_j = k_cache[block_tables[s, j / bs], h, j % bs, :] and V_j likewise.
+ * A is read only inside [start, ctx): padding (any value, NaN included) and
+ * block-table entries outside the window are never read — blocks before the
+ * window may be evicted ("[V1] Add sliding window support to Flex Attention
+ * backend": the direct build skips blocks outside the window when the page
+ * table evicts them).
+ *
+ *   out           [num_seqs, num_heads, head_dim] of dtype
+ *   q             [num_seqs, num_heads, head_dim] of dtype
+ *   k_cache, v_cache [num_blocks, num_heads, block_size, head_dim] of dtype
+ *   block_tables  int32 [num_seqs, max_blocks_per_seq]
+ *   context_lens  int32 [num_seqs], each in [0, max_context_len]
+ *   attn_bias     f32 [num_seqs, num_heads, bias_row_stride] or NULL (no bias,
+ *                 no extra work; the review answer that a null bias pointer is
+ *                 a no-op); bias_row_stride >= max_context_len (the bias is
+ *                 padded to the maximum sequence length).
+ *   sliding_window -1 (none) or >= 1
+ *   scale         multiplies q.k AND the bias (1/sqrt(head_dim) gives the
+ *                 formula as printed)
+ *   workspace     device scratch of at least
+ *                 pka_paged_attn_decode_workspace_size(...) bytes, 256-byte
+ *                 aligned, ZERO-FILLED before its first use.  Every call that
+ *                 completes leaves the whole workspace zero again, so it is
+ *                 reused without clearing by later calls of any shape (after a
+ *                 PKA_DEVCHK_TIMEOUT, zero it again).  Calls that share a
+ *                 workspace must not overlap in time (same stream, or ordered
+ *                 by events).
+ *   status        int32 device word or NULL (PKA_DEVCHK_* bits)
+ * Accumulation is f32 whatever the I/O dtype; f16 outputs stay finite for
+ * finite inputs (the f16 overflow report in "Add Encoder-decoder model support
+ * and T5 Model support").
+ */
+PKA_API size_t pka_paged_attn_decode_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                            int max_context_len, int sliding_window);
+
+PKA_API pka_status pka_paged_attn_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, const int32_t *context_lens,
+                                 const float *attn_bias, int sliding_window, float scale,
+                                 int block_size, int num_seqs, int num_heads, int head_dim,
+                                 int max_blocks_per_seq, int bias_row_stride, int num_blocks,
+                                 int max_context_len, pka_dtype dtype, void *workspace,
+                                 size_t workspace_bytes, int32_t *status, void *stream);
+
+/*
+ * pka_swa_prefill — attention for every token of a packed variable-length
+ * batch ("[V1] Add sliding window support to Flex Attention backend":
+ * bidirectional attention with a sliding window for encoder-only models; the
+ * alternating full / window layers).  For a token at position r of sequence
+ * b (rows cu_seqlens[b] .. cu_seqlens[b+1]-1), the keys are the positions c of
+ * the same sequence with
+ *   window <= 0 (-1), causal = 0 : every c
+ *   window <= 0 (-1), causal = 1 : c <= r
+ *   window  > 0,      causal = 0 : |r - c| < window
+ *   window  > 0,      causal = 1 : 0 <= r - c < window
+ *   out[i,h,:] = sum_c softmax(scale * q[i,h,:] . k[c,h,:])_c v[c,h,:]
+ * Only key tiles that intersect the mask are visited.
+ *
+ *   out, q, k, v  [num_tokens, num_heads, head_dim] bf16, contiguous
+ *   cu_seqlens    int32 [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0,
+ *                 cu_seqlens[num_seqs] = num_tokens
+ *   max_seqlen    upper bound on every sequence length (a longer sequence
+ *                 sets PKA_DEVCHK_CU_SEQLENS; its rows past max_seqlen are
+ *                 not written)
+ *   window        -1 (full) or >= 1
+ *   causal        0 or 1
+ *   status        int32 device word or NULL (PKA_DEVCHK_CU_SEQLENS,
+ *                 PKA_DEVCHK_TIMEOUT)
+ * Accumulation is f32; P is rounded to bf16 before the P.V product.
+ */
+PKA_API pka_status pka_swa_prefill(void *out, const void *q, const void *k, const void *v,
+                           const int32_t *cu_seqlens, int num_seqs, int num_tokens, int max_seqlen,
+                           int num_heads, int head_dim, int window, int causal, float scale,
+                           pka_dtype dtype, int32_t *status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKA_H */

@@ -1,0 +1,206 @@
+"""paged_kv_attention_23_gb300 — Python binding of libpka.so (sm_103a).
+
+A thin ctypes layer over the C ABI declared in ``include/pka.h``: it turns
+torch tensors into device pointers, sizes and dtype codes, passes the current
+CUDA stream, and raises on a non-OK status.  Every step of the computation
+runs in the library's CUDA kernels; there is no other code path, and calling
+any operation without the built library (or without a GPU) raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = ["PkaError", "load", "build", "lib_path", "reshape_and_cache", "paged_attn_decode",
+           "paged_attn_decode_workspace_size", "swa_prefill", "DecodeWorkspace", "DTYPE_CODE",
+           "DEVCHK_BLOCK_ID", "DEVCHK_CONTEXT_LEN", "DEVCHK_SLOT", "DEVCHK_TIMEOUT", "DEVCHK_CU_SEQLENS",
+           "EXPORTED_SYMBOLS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_PKG, "libpka.so")
+
+PKA_OK, PKA_ERR_INVALID_ARG, PKA_ERR_UNSUPPORTED, PKA_ERR_CUDA, PKA_ERR_WORKSPACE = range(5)
+DEVCHK_BLOCK_ID, DEVCHK_CONTEXT_LEN, DEVCHK_SLOT, DEVCHK_TIMEOUT, DEVCHK_CU_SEQLENS = 0x1, 0x2, 0x4, 0x8, 0x10
+
+EXPORTED_SYMBOLS = ("pka_status_string", "pka_version", "pka_reshape_and_cache",
+                    "pka_paged_attn_decode_workspace_size", "pka_paged_attn_decode", "pka_swa_prefill")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class PkaError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn}: {msg} ({code})")
+        self.code = code
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    from . import buildlib
+    return buildlib.build(force=force, verbose=verbose)
+
+
+def load():
+    """Load libpka.so (built in-tree by ``build()``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(lib_path):
+            raise RuntimeError(f"libpka.so not built at {lib_path}; run paged_kv_attention_23_gb300.build()")
+        lib = ctypes.CDLL(lib_path)
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.pka_status_string.argtypes = [I]
+        lib.pka_status_string.restype = ctypes.c_char_p
+        lib.pka_version.argtypes = []
+        lib.pka_version.restype = I
+        lib.pka_reshape_and_cache.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
+        lib.pka_reshape_and_cache.restype = I
+        lib.pka_paged_attn_decode_workspace_size.argtypes = [I, I, I, I, I]
+        lib.pka_paged_attn_decode_workspace_size.restype = ctypes.c_size_t
+        lib.pka_paged_attn_decode.argtypes = [P, P, P, P, P, P, P, I, F, I, I, I, I, I, I, I, I, I, P,
+                                              ctypes.c_size_t, P, P]
+        lib.pka_paged_attn_decode.restype = I
+        lib.pka_swa_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P]
+        lib.pka_swa_prefill.restype = I
+        _lib = lib
+        return lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    return {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[t.dtype]
+
+
+DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, code: int):
+    if code != PKA_OK:
+        raise PkaError(fn, code, load().pka_status_string(code).decode())
+
+
+def _need(t, name, dtype=None, ndim=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+# ---------------------------------------------------------------------------
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, status=None, stream=None):
+    """Scatter key/value [T, H, D] into the caches [num_blocks, H, bs, D]
+    at slot_mapping (int64 [T]; negative = skip)."""
+    torch = _torch()
+    for n, t in (("key", key), ("value", value), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, n, ndim=3 if n in ("key", "value") else 4)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    T, H, D = key.shape
+    nb, _, bs, _ = k_cache.shape
+    lib = load()
+    _check("pka_reshape_and_cache",
+           lib.pka_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+                                     T, H, D, bs, nb, _dtype_code(key), _ptr(status), _stream(stream)))
+
+
+def paged_attn_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len, sliding_window=-1) -> int:
+    return int(load().pka_paged_attn_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len,
+                                                           sliding_window))
+
+
+class DecodeWorkspace:
+    """A zero-filled device buffer for ``paged_attn_decode``, grown on demand.
+    The kernels leave its counter region zero after every call, so it is
+    reused without clearing; share one only between calls on one stream."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int):
+        torch = _torch()
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device or "cuda")
+        return self.buf
+
+
+_default_ws = {}
+
+
+def paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, attn_bias=None, sliding_window=-1,
+                      scale=None, max_context_len=None, workspace=None, status=None, stream=None):
+    """out[s,h,:] = softmax(scale * (q.K^T + A)) V over each sequence's paged
+    keys [max(0, ctx - W), ctx).  ``max_context_len`` defaults to the block
+    table's capacity (no device sync); ``workspace`` defaults to a cached
+    zero-filled buffer per device."""
+    torch = _torch()
+    _need(out, "out", ndim=3); _need(q, "q", ndim=3)
+    _need(k_cache, "k_cache", ndim=4); _need(v_cache, "v_cache", ndim=4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    if attn_bias is not None:
+        _need(attn_bias, "attn_bias", torch.float32, 3)
+    S, H, D = q.shape
+    nb, _, bs, _ = k_cache.shape
+    mbps = block_tables.shape[1]
+    stride = attn_bias.shape[2] if attn_bias is not None else 0
+    if max_context_len is None:
+        max_context_len = mbps * bs if attn_bias is None else min(mbps * bs, stride)
+    if scale is None:
+        scale = D ** -0.5
+    lib = load()
+    need = int(lib.pka_paged_attn_decode_workspace_size(S, H, D, int(max_context_len), int(sliding_window)))
+    if workspace is None:
+        dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
+        workspace = _default_ws.setdefault(dev, DecodeWorkspace(q.device)).get(need)
+    _check("pka_paged_attn_decode",
+           lib.pka_paged_attn_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                     _ptr(context_lens), _ptr(attn_bias), int(sliding_window), float(scale), bs, S,
+                                     H, D, mbps, stride, nb, int(max_context_len), _dtype_code(q), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
+    return out
+
+
+def swa_prefill(out, q, k, v, cu_seqlens, max_seqlen, window=-1, causal=0, scale=None, status=None, stream=None):
+    """Packed varlen prefill with full / causal / sliding-window (|i-j| < W)
+    masks; q/k/v/out [T, H, D] bf16, cu_seqlens int32 [B+1]."""
+    torch = _torch()
+    for n, t in (("out", out), ("q", q), ("k", k), ("v", v)):
+        _need(t, n, ndim=3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, H, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    lib = load()
+    _check("pka_swa_prefill",
+           lib.pka_swa_prefill(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T,
+                               int(max_seqlen), H, D, int(window), int(causal), float(scale), _dtype_code(q),
+                               _ptr(status), _stream(stream)))
+    return out

@@ -1,0 +1,531 @@
+// paged_decode.cu — single-query paged-KV attention with optional materialised
+// bias and optional causal sliding window, split-K over the visible blocks.
+//
+// Computes, per (sequence s, head h), the formula of "PagedAttention: Support
+// custom attention bias for T5 model (1/2)" (opening section):
+//   out = softmax(scale * (q K^T + A)) V
+// over the keys [start, ctx) with start = max(0, ctx - W) for a window W
+// ("[V1] Add sliding window support to Flex Attention backend"), K/V gathered
+// through the block table passed in (decoder self-attention and encoder
+// cross-attention each pass their own: "Add Encoder-decoder model support and
+// T5 Model support").  A NULL bias is a no-op: no bias bytes are touched.
+//
+// Design (memory-bound; everything below is about keeping HBM busy):
+//  * Work unit = (s, h, partition): `part_blocks` consecutive cache blocks of
+//    the visible range.  All units carry (almost) the same bytes, so a static
+//    round-robin over a compact unit list balances the GPU.  The list is the
+//    prefix sum over sequences of H * num_partitions(s), built by every CTA
+//    into shared memory at start (one read of context_lens).
+//  * Persistent grid (SMs x resident CTAs); every warp is an independent
+//    streaming pipeline over its units with NSTAGE shared-memory stages.
+//    Per stage: the K and V runs of one (block, head) — each a contiguous
+//    block_size * D run — arrive by two bulk copies on the TMA engine; the
+//    bias slice (16 floats, zero-filled outside [start, ctx)) and, at a
+//    unit's first block, the query row arrive by per-lane async copies.  One
+//    mbarrier per stage counts both (32 lane arrivals + the bulk bytes).
+//    Loads run up to NSTAGE blocks ahead of the math and across unit
+//    boundaries; block-table entries of the next unit are fetched one unit
+//    ahead.  Block-table entries and blocks outside the window are never read.
+//  * Math per block: 4 lanes per key compute q.k from 16-byte shared loads
+//    (chunk order rotated per key parity: no bank conflicts), online softmax
+//    in the log2 domain (ex2.approx), P.V with one 16-byte V load per lane per
+//    row group; f32 everywhere.
+//  * A unit that is its (s, h)'s only partition writes `out` directly.  Else
+//    it writes (m, l, acc) to the workspace and bumps a per-(s, h) counter with
+//    atomicInc(npart - 1), which wraps to zero: the last partition to arrive
+//    merges all partials, writes `out` and zeroes the slots it read.  A call
+//    therefore leaves the whole workspace zero, ready for the next call of any
+//    shape.
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "pka_device.cuh"
+#include "pka_launch.h"
+
+namespace pka {
+namespace {
+
+constexpr int BS = 16;                   // tokens per cache block (the only size built)
+constexpr int MAX_SEQS_PER_LAUNCH = 1024;
+
+template <typename T, int D> struct Tr {
+    static constexpr int ELT = sizeof(T);
+    static constexpr int ROW = D * ELT;              // bytes of one K or V row
+    static constexpr int NC = ROW / 16;              // 16-byte chunks per row: 8, 16, 32
+    static constexpr int EPC = 16 / ELT;             // elements per chunk
+    static constexpr int CHUNK = BS * ROW;           // bytes of one (block, head) run
+    static constexpr int QCH = NC / 2;               // chunks per lane in q.k (2 lanes per key)
+    static constexpr int QSWZ = QCH >= 8 ? 4 : 0;    // extra chunk rotation of the second half-row
+    static constexpr int RPI = 32 / NC;              // V rows per warp-wide 16-byte load
+    static constexpr int PV_IT = BS / RPI;           // P.V iterations per block
+    static constexpr int DPL = D / 32;               // dims per lane in the partition merge
+    // stage layout
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = CHUNK;
+    static constexpr int B_OFF = 2 * CHUNK;          // 16 floats of bias
+    static constexpr int Q_OFF = 2 * CHUNK + 64;     // one query row
+    static constexpr int STAGE = ((Q_OFF + ROW) + 127) / 128 * 128;
+    static_assert(NC % 8 == 0 && 32 % NC == 0, "row must be 8, 16 or 32 chunks");
+};
+
+struct Params {
+    void *out;
+    const unsigned char *q, *k_cache, *v_cache;
+    const int32_t *block_tables, *context_lens;
+    const float *bias;
+    int32_t *status;
+    unsigned *counters;
+    float2 *ws_ml;
+    float *ws_acc;
+    float scale_log2;
+    int window, seq_base, num_seqs, H, mbps, num_blocks, max_ctx, part_blocks, max_parts;
+    long long bias_stride;
+};
+
+struct Unit {
+    int s;       // sequence index within this launch
+    int h, p, npart, ctx, start, b0, nb;
+};
+
+// Unit u -> (s, h, p) by binary search in the per-sequence prefix sums.
+__device__ __forceinline__ Unit unit_of(int u, const int *cum, const int *ctxs, const Params &P)
+{
+    int lo = 0, hi = P.num_seqs;                      // cum[lo] <= u < cum[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cum[mid] <= u) lo = mid; else hi = mid;
+    }
+    Unit U;
+    U.s = lo;
+    U.npart = (cum[lo + 1] - cum[lo]) / P.H;
+    const int r = u - cum[lo];
+    U.h = r / U.npart;
+    U.p = r - U.h * U.npart;
+    U.ctx = ctxs[lo];
+    U.start = (P.window > 0 && U.ctx > P.window) ? U.ctx - P.window : 0;
+    if (U.ctx == 0) {
+        U.b0 = 0; U.nb = 0;
+    } else {
+        const int last = (U.ctx - 1) / BS;
+        U.b0 = U.start / BS + U.p * P.part_blocks;
+        U.nb = min(P.part_blocks, last + 1 - U.b0);
+    }
+    return U;
+}
+
+__device__ __forceinline__ int load_bt(const Unit &U, const Params &P, int lane)
+{
+    if (lane < U.nb)
+        return __ldg(P.block_tables + (size_t)(P.seq_base + U.s) * P.mbps + U.b0 + lane);
+    return 0;
+}
+
+// q.k for one key: this lane's half-row (QCH chunks of 16 bytes) against the
+// query half-row kept in registers; partial sums in two chains.
+template <typename T, int D> struct Dot {
+    using R = Tr<T, D>;
+    // query registers: packed 16-bit pairs, or f32
+    struct Q { uint32_t w[R::QCH][4]; };
+    __device__ __forceinline__ static void load_q(Q &q, const unsigned char *qrow, int first, int rot)
+    {
+#pragma unroll
+        for (int m = 0; m < R::QCH; ++m) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(qrow + (first + ((m + rot) & (R::QCH - 1))) * 16);
+            q.w[m][0] = v.x; q.w[m][1] = v.y; q.w[m][2] = v.z; q.w[m][3] = v.w;
+        }
+    }
+    __device__ __forceinline__ static float dot(const Q &q, const unsigned char *krow, int first, int rot)
+    {
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int m = 0; m < R::QCH; ++m) {
+            const uint4 k = *reinterpret_cast<const uint4 *>(krow + (first + ((m + rot) & (R::QCH - 1))) * 16);
+            if constexpr (sizeof(T) == 4) {
+                a0 = fmaf(__uint_as_float(q.w[m][0]), __uint_as_float(k.x), a0);
+                a1 = fmaf(__uint_as_float(q.w[m][1]), __uint_as_float(k.y), a1);
+                a2 = fmaf(__uint_as_float(q.w[m][2]), __uint_as_float(k.z), a2);
+                a3 = fmaf(__uint_as_float(q.w[m][3]), __uint_as_float(k.w), a3);
+            } else {
+                fma2_mixed<T>(q.w[m][0], k.x, a0, a1);
+                fma2_mixed<T>(q.w[m][1], k.y, a2, a3);
+                fma2_mixed<T>(q.w[m][2], k.z, a0, a1);
+                fma2_mixed<T>(q.w[m][3], k.w, a2, a3);
+            }
+        }
+        return (a0 + a1) + (a2 + a3);
+    }
+};
+
+template <typename T, int D, int NSTAGE, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P)
+{
+    using R = Tr<T, D>;
+    using DT = Dot<T, D>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    unsigned char *stages = smem + (size_t)warp * NSTAGE * R::STAGE;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)NW * NSTAGE * R::STAGE) + warp * NSTAGE;
+    int *cum = reinterpret_cast<int *>(smem + (size_t)NW * NSTAGE * R::STAGE + NW * NSTAGE * 8);
+    int *ctxs = cum + P.num_seqs + 1;
+
+    // ---- per-sequence partition counts -> prefix sums (whole CTA) ----------
+    for (int s = threadIdx.x; s < P.num_seqs; s += blockDim.x) {
+        int c = __ldg(P.context_lens + P.seq_base + s);
+        if (c < 0 || c > P.max_ctx || c > P.mbps * BS) {
+            flag_status(P.status, PKA_DEVCHK_CONTEXT_LEN);
+            c = c < 0 ? 0 : min(c, min(P.max_ctx, P.mbps * BS));
+        }
+        ctxs[s] = c;
+        int npart = 1;
+        if (c > 0) {
+            const int start = (P.window > 0 && c > P.window) ? c - P.window : 0;
+            const int nblk = (c - 1) / BS - start / BS + 1;
+            npart = min((nblk + P.part_blocks - 1) / P.part_blocks, P.max_parts);
+        }
+        cum[s + 1] = npart * P.H;
+    }
+    if (lane == 0)
+        for (int i = 0; i < NSTAGE; ++i) mbar_init(smem_u32(&bars[i]), 32);
+    fence_barrier_init();
+    __syncthreads();
+    if (warp == 0) {
+        // chunked inclusive scan of cum[1..S] by one warp
+        const int per = (P.num_seqs + 31) / 32;
+        const int a = min(lane * per, P.num_seqs), b = min(a + per, P.num_seqs);
+        int local = 0;
+        for (int i = a; i < b; ++i) local += cum[i + 1];
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        for (int i = a; i < b; ++i) { run += cum[i + 1]; cum[i + 1] = run; }
+        if (lane == 0) cum[0] = 0;
+    }
+    __syncthreads();
+
+    const int total_units = cum[P.num_seqs];
+    const int gw = blockIdx.x * NW + warp;
+    const int nwt = gridDim.x * NW;
+    if (gw >= total_units) return;                    // no CTA-wide sync after this point
+
+    const bool has_bias = P.bias != nullptr;
+
+    // ---- producer state (issue side) ---------------------------------------
+    int pk = 0;                                        // unit ordinal of the issue side
+    Unit pu = unit_of(gw, cum, ctxs, P);
+    int pbt = load_bt(pu, P, lane);
+    bool p_next_ok = gw + nwt < total_units;
+    Unit pn = pu;
+    int pnbt = 0;
+    if (p_next_ok) { pn = unit_of(gw + nwt, cum, ctxs, P); pnbt = load_bt(pn, P, lane); }
+    bool p_active = true;
+    int pib = 0;
+    auto p_advance_unit = [&]() {
+        ++pk;
+        if (!p_next_ok) { p_active = false; return; }
+        pu = pn; pbt = pnbt; pib = 0;
+        const int nu = gw + (pk + 1) * nwt;
+        p_next_ok = nu < total_units;
+        if (p_next_ok) { pn = unit_of(nu, cum, ctxs, P); pnbt = load_bt(pn, P, lane); }
+    };
+    while (p_active && pu.nb == 0) p_advance_unit();
+
+    // ---- consumer state ------------------------------------------------------
+    // q.k lanes: key = lane / 2, half = lane % 2; chunk order rotated per key
+    // so the 8 lanes of a quarter-warp always hit 8 different bank groups.
+    const int key = lane >> 1, half = lane & 1;
+    const int q_first = half * R::QCH;
+    const int q_rot = (key & 3) + half * R::QSWZ;
+    // P.V lanes: row = it * RPI + vr, 16-byte column vc
+    const int vr = lane / R::NC, vc = lane % R::NC;
+    typename DT::Q qreg;
+    float acc[R::EPC];
+    float m_run = -INFINITY, l_run = 0.f;
+    uint32_t issued = 0, consumed = 0;
+    const uint32_t st_base = smem_u32(stages);
+
+    auto top_up = [&]() {
+        while (p_active && issued - consumed < (uint32_t)NSTAGE) {
+            const int stage = issued % NSTAGE;
+            const uint32_t st = st_base + stage * R::STAGE;
+            const uint32_t bar = smem_u32(&bars[stage]);
+            int phys = __shfl_sync(kFull, pbt, pib);
+            if ((unsigned)phys >= (unsigned)P.num_blocks) {
+                if (lane == 0) flag_status(P.status, PKA_DEVCHK_BLOCK_ID);
+                phys = 0;
+            }
+            const int gs = P.seq_base + pu.s;
+            if (lane == 0) {
+                mbar_expect_tx(bar, 2 * R::CHUNK);
+                const size_t off = ((size_t)phys * P.H + pu.h) * (size_t)R::CHUNK;
+                bulk_g2s(st + R::K_OFF, P.k_cache + off, R::CHUNK, bar);
+                bulk_g2s(st + R::V_OFF, P.v_cache + off, R::CHUNK, bar);
+            }
+            if (has_bias && lane < BS) {
+                const int j = (pu.b0 + pib) * BS + lane;
+                const bool ok = j >= pu.start && j < pu.ctx;
+                const float *src = P.bias + ((size_t)gs * P.H + pu.h) * P.bias_stride + (ok ? j : 0);
+                cp_async_4(st + R::B_OFF + lane * 4, src, ok ? 4u : 0u);
+            }
+            if (pib == 0 && lane < R::NC)
+                cp_async_16(st + R::Q_OFF + lane * 16, P.q + ((size_t)gs * P.H + pu.h) * R::ROW + lane * 16);
+            cp_async_arrive_noinc(bar);
+            ++issued;
+            if (++pib >= pu.nb) {
+                p_advance_unit();
+                while (p_active && pu.nb == 0) p_advance_unit();
+            }
+        }
+    };
+
+    for (int ck = 0;; ++ck) {
+        const int u = gw + ck * nwt;
+        if (u >= total_units) break;
+        const Unit cu = unit_of(u, cum, ctxs, P);
+        m_run = -INFINITY;
+        l_run = 0.f;
+#pragma unroll
+        for (int e = 0; e < R::EPC; ++e) acc[e] = 0.f;
+
+        for (int cb = 0; cb < cu.nb; ++cb) {
+            top_up();
+            const int stage = consumed % NSTAGE;
+            const unsigned char *stp = stages + stage * R::STAGE;
+            if (!mbar_wait_bounded(smem_u32(&bars[stage]), (consumed / NSTAGE) & 1)) {
+                if (lane == 0) flag_status(P.status, PKA_DEVCHK_TIMEOUT);
+                return;
+            }
+            if (cb == 0) DT::load_q(qreg, stp + R::Q_OFF, q_first, q_rot);
+            // score of key `key` (both lanes of the pair end with the full sum)
+            float d = DT::dot(qreg, stp + R::K_OFF + key * R::ROW, q_first, q_rot);
+            d += __shfl_xor_sync(kFull, d, 1);
+            const int j = (cu.b0 + cb) * BS + key;
+            const float bv = has_bias ? reinterpret_cast<const float *>(stp + R::B_OFF)[key] : 0.f;
+            const float x = (j >= cu.start && j < cu.ctx) ? (d + bv) * P.scale_log2 : -INFINITY;
+            float mb = fmaxf(x, __shfl_xor_sync(kFull, x, 2));
+            mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 4));
+            mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 8));
+            mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 16));
+            const float m_new = fmaxf(m_run, mb);
+            const float corr = ex2(m_run - m_new);
+            const float p = ex2(x - m_new);
+            l_run = fmaf(l_run, corr, p);
+            m_run = m_new;
+#pragma unroll
+            for (int e = 0; e < R::EPC; ++e) acc[e] *= corr;
+#pragma unroll
+            for (int it = 0; it < R::PV_IT; ++it) {
+                const int row = it * R::RPI + vr;
+                const float pr = __shfl_sync(kFull, p, row * 2);
+                float vf[R::EPC];
+                Vec<T>::to_f32(*reinterpret_cast<const uint4 *>(stp + R::V_OFF + row * R::ROW + vc * 16), vf);
+#pragma unroll
+                for (int e = 0; e < R::EPC; ++e) acc[e] = fmaf(pr, vf[e], acc[e]);
+            }
+            __syncwarp();
+            ++consumed;
+        }
+        if (cu.nb == 0) top_up();          // keep the loads streaming past an empty unit
+
+        // ---- unit finished: write out or merge partials ------------------------
+        float l = l_run;                                // lanes 2k, 2k+1 hold key k's weights
+        l += __shfl_xor_sync(kFull, l, 2);
+        l += __shfl_xor_sync(kFull, l, 4);
+        l += __shfl_xor_sync(kFull, l, 8);
+        l += __shfl_xor_sync(kFull, l, 16);
+#pragma unroll
+        for (int x = R::NC; x < 32; x <<= 1)
+#pragma unroll
+            for (int e = 0; e < R::EPC; ++e) acc[e] += __shfl_xor_sync(kFull, acc[e], x);
+        const int gs = P.seq_base + cu.s;
+        const size_t sh = (size_t)gs * P.H + cu.h;
+        if (cu.npart == 1) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            if (lane < R::NC) {
+                float o[R::EPC];
+#pragma unroll
+                for (int e = 0; e < R::EPC; ++e) o[e] = acc[e] * inv;
+                reinterpret_cast<uint4 *>(static_cast<unsigned char *>(P.out) + sh * R::ROW)[lane] =
+                    Vec<T>::from_f32(o);
+            }
+            continue;
+        }
+        const size_t slot = sh * P.max_parts + cu.p;
+        if (lane < R::NC) {
+            float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + slot * D + lane * R::EPC);
+#pragma unroll
+            for (int e = 0; e < R::EPC; e += 4)
+                __stcg(dst + e / 4, make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]));
+        }
+        if (lane == 0) __stcg(P.ws_ml + slot, make_float2(m_run, l));
+        __syncwarp();
+        unsigned old = 0;
+        if (lane == 0) old = atom_inc_acq_rel(P.counters + sh, (unsigned)(cu.npart - 1));
+        old = __shfl_sync(kFull, old, 0);
+        if (old != (unsigned)(cu.npart - 1)) continue;
+
+        // last partition of (s, h): merge, write out, return the slots to zero
+        const size_t base = sh * P.max_parts;
+        float M = -INFINITY;
+        for (int i = lane; i < cu.npart; i += 32) M = fmaxf(M, __ldcg(P.ws_ml + base + i).x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        float L = 0.f;
+        for (int i = lane; i < cu.npart; i += 32) {
+            const float2 ml = __ldcg(P.ws_ml + base + i);
+            L += ml.y * ex2(ml.x - M);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
+        float o_acc[R::DPL];
+#pragma unroll
+        for (int e = 0; e < R::DPL; ++e) o_acc[e] = 0.f;
+        for (int i = 0; i < cu.npart; ++i) {
+            const float w = ex2(__ldcg(P.ws_ml + base + i).x - M);
+            float *src = P.ws_acc + (base + i) * D + lane * R::DPL;
+            if constexpr (R::DPL == 4) {
+                const float4 a4 = __ldcg(reinterpret_cast<const float4 *>(src));
+                o_acc[0] = fmaf(w, a4.x, o_acc[0]); o_acc[1] = fmaf(w, a4.y, o_acc[1]);
+                o_acc[2] = fmaf(w, a4.z, o_acc[2]); o_acc[3] = fmaf(w, a4.w, o_acc[3]);
+                __stcg(reinterpret_cast<float4 *>(src), make_float4(0.f, 0.f, 0.f, 0.f));
+            } else {
+                const float2 a2 = __ldcg(reinterpret_cast<const float2 *>(src));
+                o_acc[0] = fmaf(w, a2.x, o_acc[0]); o_acc[1] = fmaf(w, a2.y, o_acc[1]);
+                __stcg(reinterpret_cast<float2 *>(src), make_float2(0.f, 0.f));
+            }
+        }
+        __syncwarp();
+        for (int i = lane; i < cu.npart; i += 32) __stcg(P.ws_ml + base + i, make_float2(0.f, 0.f));
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        T *dst = reinterpret_cast<T *>(static_cast<unsigned char *>(P.out) + sh * R::ROW) + lane * R::DPL;
+#pragma unroll
+        for (int e = 0; e < R::DPL; ++e) {
+            const float v = o_acc[e] * inv;
+            if constexpr (sizeof(T) == 4) dst[e] = v;
+            else if constexpr (std::is_same<T, __half>::value) dst[e] = __float2half_rn(v);
+            else dst[e] = __float2bfloat16_rn(v);
+        }
+    }
+}
+
+// ---- host side --------------------------------------------------------------------
+template <typename T, int D, int NSTAGE, int NW> struct Config {
+    using R = Tr<T, D>;
+    static size_t smem_bytes(int nseq)
+    {
+        return (size_t)NW * NSTAGE * R::STAGE + (size_t)NW * NSTAGE * 8 + (size_t)(2 * nseq + 1) * 4;
+    }
+    static cudaError_t launch(const Params &P, int sms, cudaStream_t stream)
+    {
+        auto kern = paged_decode_kernel<T, D, NSTAGE, NW>;
+        const size_t smem = smem_bytes(P.num_seqs);
+        const size_t smem_max = smem_bytes(MAX_SEQS_PER_LAUNCH);
+        static std::once_flag once;
+        static cudaError_t attr_err = cudaSuccess;
+        static int occ = 1;
+        std::call_once(once, [&] {
+            attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
+            if (attr_err == cudaSuccess)
+                attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NW * 32, smem_max);
+            if (occ < 1) occ = 1;
+        });
+        if (attr_err != cudaSuccess) return attr_err;
+        const long long units_upper = (long long)P.num_seqs * P.H * P.max_parts;
+        long long grid = std::min<long long>((long long)sms * occ, (units_upper + NW - 1) / NW);
+        if (grid < 1) grid = 1;
+        kern<<<(unsigned)grid, NW * 32, smem, stream>>>(P);
+        return cudaGetLastError();
+    }
+};
+
+template <typename T, int D>
+cudaError_t dispatch_cfg(const Params &P, int sms, cudaStream_t stream)
+{
+    // one CTA per SM, about 200 KB of stages: 16 warps x 3 stages for 4.3 KB
+    // stages (2-byte D=64), 12 x 2 for 8.5 KB, 6 x 2 for 17 KB (f32 D=128)
+    if constexpr (Tr<T, D>::STAGE <= 5000)
+        return Config<T, D, 3, 16>::launch(P, sms, stream);
+    else if constexpr (Tr<T, D>::STAGE <= 9000)
+        return Config<T, D, 2, 12>::launch(P, sms, stream);
+    else
+        return Config<T, D, 2, 6>::launch(P, sms, stream);
+}
+
+}  // namespace
+
+DecodePlan decode_plan(int max_context_len, int sliding_window, int block_size)
+{
+    long long maxvb = (max_context_len + block_size - 1) / block_size;
+    if (sliding_window > 0) maxvb = std::min<long long>(maxvb, (sliding_window + block_size - 2) / block_size + 1);
+    if (maxvb < 1) maxvb = 1;
+    int pb = 4;
+    while (pb < 32 && (maxvb + pb - 1) / pb > 16) pb *= 2;
+    DecodePlan plan;
+    plan.part_blocks = pb;
+    plan.max_parts = (int)std::max<long long>(1, (maxvb + pb - 1) / pb);
+    return plan;
+}
+
+static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, const DecodePlan &plan)
+{
+    const size_t sh = (size_t)num_seqs * num_heads;
+    const size_t slots = sh * plan.max_parts;
+    return round_up(sh * 4, 256) + round_up(slots * 8, 256) + round_up(slots * head_dim * 4, 256);
+}
+
+cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream)
+{
+    if (a.num_seqs == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t sh = (size_t)a.num_seqs * a.num_heads;
+    const size_t slots = sh * plan.max_parts;
+    unsigned char *ws = static_cast<unsigned char *>(a.workspace);
+    Params P;
+    P.out = a.out;
+    P.q = static_cast<const unsigned char *>(a.q);
+    P.k_cache = static_cast<const unsigned char *>(a.k_cache);
+    P.v_cache = static_cast<const unsigned char *>(a.v_cache);
+    P.block_tables = a.block_tables;
+    P.context_lens = a.context_lens;
+    P.bias = a.bias;
+    P.status = a.status;
+    P.counters = reinterpret_cast<unsigned *>(ws);
+    P.ws_ml = reinterpret_cast<float2 *>(ws + round_up(sh * 4, 256));
+    P.ws_acc = reinterpret_cast<float *>(ws + round_up(sh * 4, 256) + round_up(slots * 8, 256));
+    P.scale_log2 = a.scale * 1.4426950408889634f;
+    P.window = a.window;
+    P.H = a.num_heads;
+    P.mbps = a.max_blocks_per_seq;
+    P.num_blocks = a.num_blocks;
+    P.max_ctx = a.max_context_len;
+    P.part_blocks = plan.part_blocks;
+    P.max_parts = plan.max_parts;
+    P.bias_stride = a.bias_row_stride;
+    for (int base = 0; base < a.num_seqs; base += MAX_SEQS_PER_LAUNCH) {
+        P.seq_base = base;
+        P.num_seqs = std::min(MAX_SEQS_PER_LAUNCH, a.num_seqs - base);
+        cudaError_t e;
+        if (a.head_dim == 64) {
+            if (a.dtype == PKA_F32) e = dispatch_cfg<float, 64>(P, sms, stream);
+            else if (a.dtype == PKA_F16) e = dispatch_cfg<__half, 64>(P, sms, stream);
+            else e = dispatch_cfg<__nv_bfloat16, 64>(P, sms, stream);
+        } else {
+            if (a.dtype == PKA_F32) e = dispatch_cfg<float, 128>(P, sms, stream);
+            else if (a.dtype == PKA_F16) e = dispatch_cfg<__half, 128>(P, sms, stream);
+            else e = dispatch_cfg<__nv_bfloat16, 128>(P, sms, stream);
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace pka

@@ -1,0 +1,144 @@
+// pka_abi.cu — the extern "C" entry points of libpka.so: argument checks on
+// the host, then one launch on the caller's stream.  Nothing here allocates.
+#include <cmath>
+#include <cstdint>
+
+#include "pka_launch.h"
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool dtype_ok(pka_dtype d) { return d == PKA_F32 || d == PKA_F16 || d == PKA_BF16; }
+
+int elt_bytes(pka_dtype d) { return d == PKA_F32 ? 4 : 2; }
+
+pka_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *pka_status_string(pka_status s)
+{
+    switch (s) {
+    case PKA_OK: return "PKA_OK";
+    case PKA_ERR_INVALID_ARG: return "PKA_ERR_INVALID_ARG";
+    case PKA_ERR_UNSUPPORTED: return "PKA_ERR_UNSUPPORTED";
+    case PKA_ERR_CUDA: return "PKA_ERR_CUDA";
+    case PKA_ERR_WORKSPACE: return "PKA_ERR_WORKSPACE";
+    }
+    return "PKA_ERR_UNKNOWN";
+}
+
+int pka_version(void) { return 100; }
+
+pka_status pka_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
+                                 const int64_t *slot_mapping, int num_tokens, int num_heads,
+                                 int head_dim, int block_size, int num_blocks, pka_dtype dtype,
+                                 int32_t *status, void *stream)
+{
+    if (num_tokens < 0 || num_heads < 1 || num_blocks < 1 || !dtype_ok(dtype)) return PKA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PKA_ERR_UNSUPPORTED;
+    if (block_size != 16) return PKA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PKA_ERR_INVALID_ARG;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8) || !aligned(status, 4))
+        return PKA_ERR_INVALID_ARG;
+    return from_cuda(pka::launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                                                   num_heads, head_dim, block_size, num_blocks,
+                                                   elt_bytes(dtype), status,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+size_t pka_paged_attn_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                            int sliding_window)
+{
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+    const pka::DecodePlan plan = pka::decode_plan(max_context_len, sliding_window, 16);
+    return pka::decode_workspace_bytes(num_seqs, num_heads, head_dim, plan);
+}
+
+pka_status pka_paged_attn_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, const int32_t *context_lens,
+                                 const float *attn_bias, int sliding_window, float scale,
+                                 int block_size, int num_seqs, int num_heads, int head_dim,
+                                 int max_blocks_per_seq, int bias_row_stride, int num_blocks,
+                                 int max_context_len, pka_dtype dtype, void *workspace,
+                                 size_t workspace_bytes, int32_t *status, void *stream)
+{
+    if (num_seqs < 0 || num_heads < 1 || max_blocks_per_seq < 1 || num_blocks < 1 || max_context_len < 0 ||
+        !dtype_ok(dtype) || !std::isfinite(scale))
+        return PKA_ERR_INVALID_ARG;
+    if (sliding_window != -1 && sliding_window < 1) return PKA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PKA_ERR_UNSUPPORTED;
+    if (block_size != 16) return PKA_ERR_UNSUPPORTED;
+    if ((long long)max_context_len > (long long)max_blocks_per_seq * block_size) return PKA_ERR_INVALID_ARG;
+    if (attn_bias && (bias_row_stride < max_context_len || bias_row_stride < 1)) return PKA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKA_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(attn_bias, 4) ||
+        !aligned(status, 4))
+        return PKA_ERR_INVALID_ARG;
+    const pka::DecodePlan plan = pka::decode_plan(max_context_len, sliding_window, block_size);
+    const size_t need = pka::decode_workspace_bytes(num_seqs, num_heads, head_dim, plan);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PKA_ERR_WORKSPACE;
+    pka::DecodeArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.bias = attn_bias;
+    a.status = status;
+    a.scale = scale;
+    a.window = sliding_window;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.head_dim = head_dim;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.max_context_len = max_context_len;
+    a.bias_row_stride = attn_bias ? bias_row_stride : 0;
+    a.dtype = dtype;
+    a.workspace = workspace;
+    return from_cuda(pka::launch_paged_decode(a, plan, static_cast<cudaStream_t>(stream)));
+}
+
+pka_status pka_swa_prefill(void *out, const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                           int num_seqs, int num_tokens, int max_seqlen, int num_heads, int head_dim, int window,
+                           int causal, float scale, pka_dtype dtype, int32_t *status, void *stream)
+{
+    if (num_seqs < 0 || num_tokens < 0 || max_seqlen < 0 || num_heads < 1 || !std::isfinite(scale) ||
+        (causal != 0 && causal != 1) || !dtype_ok(dtype))
+        return PKA_ERR_INVALID_ARG;
+    if (window != -1 && window < 1) return PKA_ERR_INVALID_ARG;
+    if (dtype != PKA_BF16) return PKA_ERR_UNSUPPORTED;
+    if (head_dim != 64) return PKA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || num_tokens == 0) return PKA_OK;
+    if (!out || !q || !k || !v || !cu_seqlens) return PKA_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(cu_seqlens, 4) ||
+        !aligned(status, 4))
+        return PKA_ERR_INVALID_ARG;
+    pka::PrefillArgs a;
+    a.out = out;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.cu_seqlens = cu_seqlens;
+    a.status = status;
+    a.scale = scale;
+    a.num_seqs = num_seqs;
+    a.num_tokens = num_tokens;
+    a.max_seqlen = max_seqlen;
+    a.num_heads = num_heads;
+    a.head_dim = head_dim;
+    a.window = window;
+    a.causal = causal;
+    return from_cuda(pka::launch_swa_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// pka_launch.h — host-side launchers behind the C ABI (internal to libpka).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pka.h"
+
+namespace pka {
+
+// ---- reshape_and_cache ------------------------------------------------------
+cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
+                                     const int64_t *slot_mapping, int num_tokens, int num_heads,
+                                     int head_dim, int block_size, int num_blocks, int elt_bytes,
+                                     int32_t *status, cudaStream_t stream);
+
+// ---- paged decode -----------------------------------------------------------
+// How a decode call is split: each (sequence, head) range of visible key
+// blocks is cut into partitions of `part_blocks` cache blocks; at most
+// `max_parts` partitions per (sequence, head).
+struct DecodePlan {
+    int part_blocks;
+    int max_parts;
+};
+
+DecodePlan decode_plan(int max_context_len, int sliding_window, int block_size);
+
+// Workspace layout: [counters: int32 S*H | pad 256][m,l: float2 S*H*P | pad][acc: f32 S*H*P*D]
+size_t decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, const DecodePlan &plan);
+
+struct DecodeArgs {
+    void *out;
+    const void *q, *k_cache, *v_cache;
+    const int32_t *block_tables, *context_lens;
+    const float *bias;
+    int32_t *status;
+    float scale;
+    int window, num_seqs, num_heads, head_dim, max_blocks_per_seq, num_blocks, max_context_len;
+    long long bias_row_stride;
+    pka_dtype dtype;
+    void *workspace;
+};
+
+cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
+
+// ---- sliding-window prefill ----------------------------------------------------
+struct PrefillArgs {
+    void *out;
+    const void *q, *k, *v;
+    const int32_t *cu_seqlens;
+    int32_t *status;
+    float scale;
+    int num_seqs, num_tokens, max_seqlen, num_heads, head_dim, window, causal;
+};
+
+cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+}  // namespace pka

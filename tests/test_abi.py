@@ -1,0 +1,113 @@
+"""The C ABI library loads and exports every symbol include/pka.h declares;
+host-side argument checks answer without touching a GPU.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_attention_23_gb300 as pka
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pka.build()
+    return pka.load()
+
+
+def declared_symbols():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"PKA_API\s+[\w\s\*]+?\b(pka_\w+)\s*\(", src))
+    return names
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_symbols() == set(pka.EXPORTED_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.pka_status_string(0) == b"PKA_OK"
+    assert lib.pka_status_string(1) == b"PKA_ERR_INVALID_ARG"
+    assert lib.pka_status_string(99) == b"PKA_ERR_UNKNOWN"
+    assert lib.pka_version() >= 100
+
+
+def test_workspace_size_grows_with_work(lib):
+    f = lib.pka_paged_attn_decode_workspace_size
+    a = f(64, 8, 64, 512, -1)
+    assert a > 0
+    assert f(128, 8, 64, 512, -1) > a
+    assert f(64, 8, 128, 512, -1) > a
+    assert f(64, 8, 64, 512, 16) < a          # a window bounds the partitions
+    assert f(0, 8, 64, 512, -1) == 0
+
+
+NULL = None
+
+
+def _decode(lib, **kw):
+    a = dict(out=NULL, q=NULL, kc=NULL, vc=NULL, bt=NULL, cl=NULL, bias=NULL, window=-1, scale=0.125, bs=16,
+             S=0, H=2, D=64, mbps=4, stride=0, nb=8, maxctx=64, dt=0, ws=NULL, wsb=0, st=NULL, stream=NULL)
+    a.update(kw)
+    return lib.pka_paged_attn_decode(a["out"], a["q"], a["kc"], a["vc"], a["bt"], a["cl"], a["bias"], a["window"],
+                                     a["scale"], a["bs"], a["S"], a["H"], a["D"], a["mbps"], a["stride"], a["nb"],
+                                     a["maxctx"], a["dt"], a["ws"], a["wsb"], a["st"], a["stream"])
+
+
+def test_decode_argument_checks_need_no_gpu(lib):
+    assert _decode(lib) == pka.PKA_OK                               # zero sequences: nothing to do
+    assert _decode(lib, window=0) == pka.PKA_ERR_INVALID_ARG
+    assert _decode(lib, window=-2) == pka.PKA_ERR_INVALID_ARG
+    assert _decode(lib, D=96) == pka.PKA_ERR_UNSUPPORTED
+    assert _decode(lib, bs=32) == pka.PKA_ERR_UNSUPPORTED
+    assert _decode(lib, dt=7) == pka.PKA_ERR_INVALID_ARG
+    assert _decode(lib, maxctx=65) == pka.PKA_ERR_INVALID_ARG      # > mbps * bs
+    assert _decode(lib, scale=float("nan")) == pka.PKA_ERR_INVALID_ARG
+    fake = ctypes.c_void_p(4096)                                   # never dereferenced: checks fail first
+    assert _decode(lib, bias=fake, stride=10) == pka.PKA_ERR_INVALID_ARG   # stride < max_context_len
+    assert _decode(lib, S=1) == pka.PKA_ERR_INVALID_ARG            # NULL buffers
+    assert _decode(lib, S=1, out=fake, q=fake, kc=fake, vc=fake, bt=fake, cl=fake,
+                   ws=NULL) == pka.PKA_ERR_WORKSPACE
+    assert _decode(lib, S=1, out=ctypes.c_void_p(4100), q=fake, kc=fake, vc=fake, bt=fake,
+                   cl=fake) == pka.PKA_ERR_INVALID_ARG             # misaligned out
+
+
+def test_reshape_and_prefill_argument_checks_need_no_gpu(lib):
+    f = lib.pka_reshape_and_cache
+    assert f(NULL, NULL, NULL, NULL, NULL, 0, 2, 64, 16, 8, 2, NULL, NULL) == pka.PKA_OK
+    assert f(NULL, NULL, NULL, NULL, NULL, 3, 2, 64, 16, 8, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
+    assert f(NULL, NULL, NULL, NULL, NULL, 3, 2, 80, 16, 8, 2, NULL, NULL) == pka.PKA_ERR_UNSUPPORTED
+    p = lib.pka_swa_prefill
+    assert p(NULL, NULL, NULL, NULL, NULL, 0, 0, 0, 12, 64, -1, 0, 0.125, 2, NULL, NULL) == pka.PKA_OK
+    assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, 0, 0, 0.125, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
+    assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 2, 0.125, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
+    assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, 0.125, 0, NULL, NULL) == pka.PKA_ERR_UNSUPPORTED
+    assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, 0.125, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
+
+
+def test_product_path_refuses_to_run_without_the_library(monkeypatch, tmp_path):
+    """No silent fallback: with the library missing, load() raises."""
+    monkeypatch.setattr(pka, "_lib", None)
+    monkeypatch.setattr(pka, "lib_path", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        pka.load()
+
+
+def test_product_package_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "paged_kv_attention_23_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
+                assert "oracle.c" not in src and "liboracle" not in src, f

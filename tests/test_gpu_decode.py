@@ -1,0 +1,278 @@
+"""GPU parity of reshape_and_cache and paged_attn_decode against the fp64
+oracle, through the C ABI, on seeded synthetic inputs."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import TOL, GpuDecode, max_err, oracle_decode, to_dev, to_f64, to_host_storage, torch_dtype
+from synth import BF16, F16, F32
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(got, ref, dtype, what=""):
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = max_err(got, ref)
+    assert err <= TOL[dtype], f"{what}: max abs err {err:.3g} > {TOL[dtype]}"
+    return err
+
+
+# ---------------------------------------------------------------------------
+# reshape_and_cache: bit-exact against the oracle's scatter
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", [F32, F16, BF16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_reshape_and_cache_bitexact(cuda_lib, dtype, D):
+    import torch
+    case = synth.make_decode_case("rc", 21, dtype, 7, 3, D, context_lens=np.array([1, 15, 16, 17, 40, 0, 33]),
+                                  pool_blocks=20)
+    slots = case.slot_mapping.copy()
+    slots[[0, 5, 17]] = -1
+    H, bs = 3, 16
+    shape = (case.num_blocks, H, bs, D)
+    pat = np.full(int(np.prod(shape)) * case.key.itemsize, 0x5A, np.uint8)
+    host_k = pat.view(case.key.dtype).reshape(shape).copy()
+    host_v = host_k.copy()
+    oracle.reshape_and_cache(host_k, host_v, case.key, case.value, slots, bs)
+    kc = to_dev(pat.view(case.key.dtype).reshape(shape), dtype)
+    vc = kc.clone()
+    cuda_lib.reshape_and_cache(to_dev(case.key, dtype), to_dev(case.value, dtype), kc, vc,
+                               torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    assert to_host_storage(kc, dtype).tobytes() == host_k.tobytes()
+    assert to_host_storage(vc, dtype).tobytes() == host_v.tobytes()
+
+
+def test_reshape_and_cache_slot_past_cache_flags_status(cuda_lib):
+    import torch
+    case = synth.make_decode_case("rc", 22, BF16, 2, 2, 64, context_lens=np.array([5, 9]))
+    slots = case.slot_mapping.copy()
+    slots[3] = case.num_blocks * 16 + 5           # past the cache: skipped and flagged
+    kc = torch.zeros((case.num_blocks, 2, 16, 64), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cuda_lib.reshape_and_cache(to_dev(case.key, BF16), to_dev(case.value, BF16), kc, vc,
+                               torch.from_numpy(slots).cuda(), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & cuda_lib.DEVCHK_SLOT
+
+
+# ---------------------------------------------------------------------------
+# the named decode workloads
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("n", [1, 2, 3])
+@pytest.mark.parametrize("bias", [True, False])
+def test_decode_workload_parity(cuda_lib, n, bias):
+    case = synth.decode_workload(n)
+    g = GpuDecode(case, cuda_lib)
+    got = to_f64(g.run(bias=bias), case.dtype)
+    ref = oracle_decode(case, bias=bias)
+    _check(got, ref, case.dtype, f"workload {n} bias={bias}")
+    assert int(g.status.item()) == 0
+
+
+def test_cross_attention_decode_parity(cuda_lib):
+    """Cross-attention decode: its own block table and pool, encoder length
+    512, no bias, no window."""
+    case = synth.cross_workload()
+    g = GpuDecode(case, cuda_lib)
+    _check(to_f64(g.run(), case.dtype), oracle_decode(case), case.dtype, "cross")
+
+
+def test_long_context_window_decode_full_size_sampled(cuda_lib):
+    """fp16 / head_dim 128 / window 4096 / NaN-padded bias, at full size
+    (512 x 16, contexts log-uniform [16, 8192]); the oracle checks a seeded
+    sample of (sequence, head) pairs that includes the longest and shortest
+    sequences."""
+    import torch
+    case = synth.decode_workload(5, device="cuda")
+    g = GpuDecode(case, cuda_lib)
+    got = to_f64(g.run(), case.dtype)
+    assert np.isfinite(got).all()
+    assert int(g.status.item()) == 0
+    order = np.argsort(case.context_lens)
+    rng = np.random.default_rng(55)
+    seqs = sorted(set(order[:3].tolist() + order[-5:].tolist() + rng.choice(512, 16, replace=False).tolist()))
+    # a compact host case with just those sequences, from the generator's token rows
+    sub = _subcase(case, seqs)
+    pairs = np.array([[i, h] for i in range(len(seqs)) for h in range(case.num_heads)], dtype=np.int32)
+    ref = oracle_decode(sub, pairs=pairs).reshape(len(seqs), case.num_heads, case.head_dim)
+    _check(got[seqs], ref, case.dtype, "long-context sample")
+
+
+def _subcase(case, seqs):
+    """Host copy of a few sequences of a device-drawn case, laid out in a
+    fresh contiguous pool."""
+    key, value = case.device_kv
+    ctx = case.context_lens[seqs]
+    ks, vs = [], []
+    for s in seqs:
+        a, b = int(case.tok_offsets[s]), int(case.tok_offsets[s + 1])
+        ks.append(to_host_storage(key[a:b], case.dtype))
+        vs.append(to_host_storage(value[a:b], case.dtype))
+    pool, bt, slot, tok = synth._paged_layout(np.random.default_rng(0), ctx, case.block_size)
+    bias = case.bias[seqs] if case.bias is not None else None
+    return synth.DecodeCase("sub", case.dtype, len(seqs), case.num_heads, case.head_dim, case.block_size, pool,
+                            ctx.astype(np.int32), bt, slot, tok, case.q[seqs], np.concatenate(ks),
+                            np.concatenate(vs), bias, case.window, case.scale)
+
+
+# ---------------------------------------------------------------------------
+# edge cases: every dtype and head size, ragged contexts, windows
+# ---------------------------------------------------------------------------
+EDGE_CTX = (0, 1, 2, 15, 16, 17, 31, 32, 33, 64, 65, 300, 1000)
+
+
+@pytest.mark.parametrize("dtype", [F32, F16, BF16])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("window", [-1, 1, 7, 16, 17, 100, 5000])
+def test_decode_edge_cases(cuda_lib, dtype, D, window):
+    case = synth.make_decode_case("edge", 31 + D + window, dtype, len(EDGE_CTX), 3, D,
+                                  context_lens=np.array(EDGE_CTX), pool_blocks=120, bias="gauss",
+                                  bias_stride=1003, window=window, scale=0.17)
+    g = GpuDecode(case, cuda_lib)
+    for bias in (True, False):
+        got = to_f64(g.run(bias=bias), dtype)
+        _check(got, oracle_decode(case, bias=bias), dtype, f"edge bias={bias}")
+        np.testing.assert_array_equal(got[0], 0.0)               # ctx 0 -> zero row
+    assert int(g.status.item()) == 0
+
+
+def test_decode_many_sequences_multi_launch(cuda_lib):
+    """More sequences than one launch takes (the host splits them)."""
+    rng = np.random.default_rng(77)
+    ctx = rng.integers(0, 90, size=2600)
+    case = synth.make_decode_case("many", 77, BF16, 2600, 2, 64, context_lens=ctx, bias="gauss", bias_stride=90)
+    g = GpuDecode(case, cuda_lib)
+    _check(to_f64(g.run(), BF16), oracle_decode(case), BF16, "many")
+
+
+def test_decode_long_unwindowed_many_partitions(cuda_lib):
+    """Contexts long enough for the most partitions per (sequence, head)."""
+    ctx = np.array([8192, 8191, 7000, 4097, 33])
+    case = synth.make_decode_case("long", 78, F16, 5, 2, 128, context_lens=ctx, bias="gauss", bias_stride=8200)
+    g = GpuDecode(case, cuda_lib)
+    _check(to_f64(g.run(), F16), oracle_decode(case), F16, "long")
+
+
+# ---------------------------------------------------------------------------
+# poison, invariants, status
+# ---------------------------------------------------------------------------
+def test_decode_ignores_padding_and_evicted_blocks(cuda_lib):
+    """NaN bias outside [start, ctx), block-table entries before the window
+    set to -1 (evicted) and junk past the context leave the output as is."""
+    import torch
+    ctx = np.array([5, 40, 100, 257, 16])
+    case = synth.make_decode_case("poison", 90, BF16, 5, 4, 64, context_lens=ctx, bias="gauss", bias_stride=260,
+                                  window=20, max_blocks_per_seq=20)
+    g = GpuDecode(case, cuda_lib)
+    base = to_f64(g.run(), BF16).copy()
+    bias = case.bias.copy()
+    bt = case.block_tables.copy()
+    for s, c in enumerate(ctx):
+        start = max(0, c - 20)
+        bias[s, :, c:] = np.nan
+        bias[s, :, :start] = np.nan
+        bt[s, :start // 16] = -1
+        bt[s, (c + 15) // 16:] = 1 << 30
+    g.bias.copy_(torch.from_numpy(bias))
+    g.block_tables.copy_(torch.from_numpy(bt))
+    got = to_f64(g.run(), BF16)
+    np.testing.assert_array_equal(got, base)
+    assert int(g.status.item()) == 0
+
+
+def test_decode_block_permutation_is_bitwise_invariant(cuda_lib):
+    import torch
+    case = synth.decode_workload(2)
+    g = GpuDecode(case, cuda_lib)
+    base = to_host_storage(g.run(), BF16).copy()
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(case.num_blocks)).cuda()
+    kc2 = torch.empty_like(g.k_cache); vc2 = torch.empty_like(g.v_cache)
+    kc2[perm] = g.k_cache; vc2[perm] = g.v_cache
+    bt = g.block_tables.long()
+    g.block_tables = torch.where(bt >= 0, perm[bt.clamp(min=0)], bt).int().contiguous()
+    g.k_cache, g.v_cache = kc2, vc2
+    assert to_host_storage(g.run(), BF16).tobytes() == base.tobytes()
+
+
+def test_decode_repeat_calls_are_deterministic_and_leave_counters_clean(cuda_lib):
+    import torch
+    case = synth.decode_workload(3)
+    g = GpuDecode(case, cuda_lib)
+    need = cuda_lib.paged_attn_decode_workspace_size(case.num_seqs, case.num_heads, case.head_dim,
+                                                     case.max_context_len, case.window)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    a = to_host_storage(g.run(workspace=ws), BF16).copy()
+    b = to_host_storage(g.run(workspace=ws), BF16).copy()
+    assert a.tobytes() == b.tobytes()
+    assert int(ws.count_nonzero().item()) == 0          # the whole workspace is zero again
+
+
+def test_decode_workspace_shared_across_shapes(cuda_lib):
+    """One workspace, calls of different (num_seqs, num_heads, partitions) in
+    turn: every call must leave it clean for the next."""
+    import torch
+    cases = [synth.decode_workload(2), synth.decode_workload(3), synth.decode_workload(1),
+             synth.make_decode_case("wide", 94, F16, 1500, 4, 128, ctx_range=(1, 300))]
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    gs = [GpuDecode(c, cuda_lib) for c in cases]
+    for rep in range(2):
+        for c, g in zip(cases, gs):
+            got = to_f64(g.run(workspace=ws), c.dtype)
+            _check(got, oracle_decode(c), c.dtype, f"shared workspace {c.name} rep {rep}")
+            assert int(ws.count_nonzero().item()) == 0
+
+
+def test_decode_bad_block_id_sets_status(cuda_lib):
+    """A block id past the pool inside the visible range: the kernel reads a
+    valid block instead, finishes, and reports PKA_DEVCHK_BLOCK_ID."""
+    import torch
+    case = synth.make_decode_case("bad", 91, F32, 3, 2, 64, context_lens=np.array([20, 40, 3]))
+    g = GpuDecode(case, cuda_lib)
+    bt = case.block_tables.copy()
+    bt[1, 1] = case.num_blocks + 7
+    g.block_tables.copy_(torch.from_numpy(bt))
+    g.run()
+    torch.cuda.synchronize()
+    assert int(g.status.item()) & cuda_lib.DEVCHK_BLOCK_ID
+
+
+def test_decode_context_len_over_bound_sets_status(cuda_lib):
+    import torch
+    case = synth.make_decode_case("ctx", 92, F32, 3, 2, 64, context_lens=np.array([20, 40, 3]))
+    g = GpuDecode(case, cuda_lib)
+    g.context_lens[1] = 41                     # > max_context_len passed (40)
+    g.run()
+    torch.cuda.synchronize()
+    assert int(g.status.item()) & cuda_lib.DEVCHK_CONTEXT_LEN
+
+
+def test_f16_large_logits_stay_finite(cuda_lib):
+    """q.k far beyond the f16 range (the T5-large f16 overflow report): f32
+    scores keep the output finite and correct."""
+    case = synth.make_decode_case("big", 93, F16, 4, 2, 128, context_lens=np.array([3, 50, 200, 17]),
+                                  scale=1.0)
+    big_q = (synth.decode_to_f32(case.q, F16) * 40).astype(np.float16)
+    big_k = (synth.decode_to_f32(case.key, F16) * 40).astype(np.float16)
+    case.q, case.key = big_q, big_k
+    g = GpuDecode(case, cuda_lib)
+    got = to_f64(g.run(), F16)
+    _check(got, oracle_decode(case), F16, "f16 large logits")
+
+
+def test_api_rejects_bad_arguments(cuda_lib):
+    import torch
+    case = synth.decode_workload(1)
+    g = GpuDecode(case, cuda_lib)
+    with pytest.raises(cuda_lib.PkaError):
+        g.run(window=0)
+    with pytest.raises(cuda_lib.PkaError):
+        cuda_lib.paged_attn_decode(g.out, g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.bias,
+                                   max_context_len=65)          # bias stride 64 < 65
+    small = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(cuda_lib.PkaError):
+        g.run(workspace=small)
