@@ -151,6 +151,40 @@ PKA_API pka_status pka_paged_attn_decode(void *out, const void *q, const void *k
                                  size_t workspace_bytes, int32_t *status, void *stream);
 
 /*
+ * pka_paged_attn_decode_noalloc — pka_paged_attn_decode for callers that
+ * cannot allocate device memory.  The pages have no counterpart: this is an
+ * interface convenience, not part of the method.
+ *
+ * Some callers have no way to hand over a scratch workspace: code embedded in
+ * a host framework that owns all device memory through its own pool and
+ * forbids allocations outside it, or a latency-critical loop where a
+ * cudaMalloc could stall the device.  This entry point takes the same
+ * arguments as pka_paged_attn_decode minus the workspace, computes the same
+ * result with the same kernel, and allocates nothing: its scratch is one
+ * fixed device array of PKA_NOALLOC_SCRATCH_BYTES inside libpka, which every
+ * GPU that loads the library holds until the process exits.
+ *  - Returns PKA_ERR_WORKSPACE, with nothing enqueued, when the call needs more
+ *    scratch than that (compare pka_paged_attn_decode_workspace_size with
+ *    PKA_NOALLOC_SCRATCH_BYTES).  Other argument errors are as for
+ *    pka_paged_attn_decode.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents; each call clears, on its own stream, the part that must start at
+ *    zero.  Calls whose work overlaps on the GPU (different streams not ordered
+ *    by events) race on the array and produce wrong results.
+ *  - The array's device address is looked up on the first call made with a
+ *    device current; make that first call before any stream capture begins.
+ */
+#define PKA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+PKA_API pka_status pka_paged_attn_decode_noalloc(void *out, const void *q, const void *k_cache,
+                                                 const void *v_cache, const int32_t *block_tables,
+                                                 const int32_t *context_lens, const float *attn_bias,
+                                                 int sliding_window, float scale, int block_size, int num_seqs,
+                                                 int num_heads, int head_dim, int max_blocks_per_seq,
+                                                 int bias_row_stride, int num_blocks, int max_context_len,
+                                                 pka_dtype dtype, int32_t *status, void *stream);
+
+/*
  * pka_swa_prefill — attention for every token of a packed variable-length
  * batch ("[V1] Add sliding window support to Flex Attention backend":
  * bidirectional attention with a sliding window for encoder-only models; the

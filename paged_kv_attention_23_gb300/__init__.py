@@ -24,7 +24,8 @@ PKA_OK, PKA_ERR_INVALID_ARG, PKA_ERR_UNSUPPORTED, PKA_ERR_CUDA, PKA_ERR_WORKSPAC
 DEVCHK_BLOCK_ID, DEVCHK_CONTEXT_LEN, DEVCHK_SLOT, DEVCHK_TIMEOUT, DEVCHK_CU_SEQLENS = 0x1, 0x2, 0x4, 0x8, 0x10
 
 EXPORTED_SYMBOLS = ("pka_status_string", "pka_version", "pka_reshape_and_cache",
-                    "pka_paged_attn_decode_workspace_size", "pka_paged_attn_decode", "pka_swa_prefill")
+                    "pka_paged_attn_decode_workspace_size", "pka_paged_attn_decode",
+                    "pka_paged_attn_decode_noalloc", "pka_swa_prefill")
 
 _lib = None
 _lock = threading.Lock()
