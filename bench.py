@@ -200,6 +200,31 @@ def _dev(arr, code, device):
     return torch.from_numpy(a).to(device)
 
 
+def capture_graph(fn):
+    """Capture fn()'s launches (all on the current stream) into a CUDA graph."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    return g
+
+
+def per_launch_ms(run, nsides, K):
+    """Mean device duration of each side's timed launch over K steps: run(ev)
+    records ev[side][0][k] / ev[side][1][k] around the launch of step k."""
+    import torch
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(K)] for _ in range(2)] for _ in range(nsides)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e6) * (K + 10))          # ~1 ms per step at 2 GHz: the host queues ahead
+    run(ev)
+    torch.cuda.synchronize()
+    return [statistics.mean(ev[j][0][k].elapsed_time(ev[j][1][k]) for k in range(K)) for j in range(nsides)]
+
+
 class DecodeSide:
     """One decode call's device state (one attention type), with its new-token
     inputs for reshape_and_cache."""
@@ -255,12 +280,12 @@ class DecodeSide:
                               workspace=self.ws)
 
 
-def build_decode_sides(workload, device, on_device_draw):
+def build_decode_sides(workload, device, on_device_draw, num_seqs=None):
     n = DECODE_WORKLOADS[workload]
     dev = device if on_device_draw else None
-    cases = [synth.decode_workload(n, device=dev)]
+    cases = [synth.decode_workload(n, device=dev, num_seqs=num_seqs)]
     if n == 3:
-        cases.append(synth.cross_workload(device=dev))
+        cases.append(synth.cross_workload(device=dev, num_seqs=num_seqs))
     return cases
 
 
@@ -271,8 +296,12 @@ def run_decode(args, rank, world, local, peaks):
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
     big = args.workload in ("t5-large-decode", "long-ctx-decode")
-    cases = build_decode_sides(args.workload, device, big)
+    cases = build_decode_sides(args.workload, device, big, args.num_seqs)
     sides = [DecodeSide(c, pka, device) for c in cases]
+    if args.no_cpu_baseline:
+        for c in cases:               # the token arrays are only needed again by the CPU leg
+            c.device_kv = None
+        torch.cuda.empty_cache()
     bytes_on = [decode_alg_bytes(c, True) for c in cases]
     bytes_off = [decode_alg_bytes(c, False) for c in cases]
     step_bytes = sum(b["total"] for b in bytes_on)
@@ -301,32 +330,26 @@ def run_decode(args, rank, world, local, peaks):
     for w in range(args.warmup):
         step(w)
     K = args.steps
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(K)] for _ in range(2)] for _ in sides]
+    # the K timed steps are one CUDA graph (no host launch gaps); one untimed
+    # replay first uploads it
+    graph = capture_graph(lambda: [step(k) for k in range(K)])
+    graph.replay()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(); barrier(world)
     t0.record()
-    for k in range(K):
-        step(k, True, ev)
+    graph.replay()
     t1.record()
     torch.cuda.synchronize(); barrier(world)
     clk = clocks.stop()
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
     ms_step = total_ms / K
-    launch_ms = [statistics.mean(ev[j][0][k].elapsed_time(ev[j][1][k]) for k in range(K)) for j in range(len(sides))]
-
-    # bias off (same shapes), decode launches only
-    torch.cuda.synchronize()
+    # per-launch durations: the same K steps eagerly, queued behind a GPU-side
+    # sleep so the host is ahead and events see kernel time, not launch gaps
+    launch_ms = per_launch_ms(lambda ev: [step(k, True, ev) for k in range(K)], len(sides), K)
     off_ms = None
     if any(s.bias is not None for s in sides):
-        ev2 = [[[torch.cuda.Event(enable_timing=True) for _ in range(K)] for _ in range(2)] for _ in sides]
-        for w in range(args.warmup):
-            step(w, False)
-        for k in range(K):
-            step(k, False, ev2)
-        torch.cuda.synchronize()
-        off_ms = sum(statistics.mean(ev2[j][0][k].elapsed_time(ev2[j][1][k]) for k in range(K))
-                     for j in range(len(sides)))
+        off_ms = sum(per_launch_ms(lambda ev: [step(k, False, ev) for k in range(K)], len(sides), K))
 
     value = step_bytes * world / (ms_step * 1e-3) / 1e9
     # dominant kernel: the decode launch carrying the most bytes
@@ -436,17 +459,17 @@ def run_prefill(args, rank, world, local, peaks):
     for _ in range(args.warmup):
         step()
     K = args.steps
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(K)] for _ in range(2)] for _ in layers]
+    graph = capture_graph(lambda: [step() for _ in range(K)])
+    graph.replay()
     t0 = torch.cuda.Event(enable_timing=True); t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(); barrier(world)
     t0.record()
-    for k in range(K):
-        step(ev, k)
+    graph.replay()
     t1.record()
     torch.cuda.synchronize(); barrier(world)
     clk = clocks.stop()
     ms_step = max_over_ranks(t0.elapsed_time(t1), world) / K
-    launch_ms = [statistics.mean(ev[j][0][k].elapsed_time(ev[j][1][k]) for k in range(K)) for j in range(3)]
+    launch_ms = per_launch_ms(lambda ev: [step(ev, k) for k in range(K)], 3, K)
     value = sum(flops) * world / (ms_step * 1e-3) / 1e12
     ach = flops[0] / (launch_ms[0] * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
@@ -658,6 +681,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="profiling only: fewer sequences than the named decode workload")
     ap.add_argument("--clock-soak", type=float, default=1.5,
                     help="seconds of untimed steps while nvidia-smi samples clocks before the warm-up")
     args = ap.parse_args()

@@ -253,7 +253,8 @@ def draw_device_tokens(seed: int, T: int, H: int, D: int, dtype: int, device: st
 # --------------------------------------------------------------------------
 # named decode workloads
 # --------------------------------------------------------------------------
-def decode_workload(n: int, device: Optional[str] = None, bias_on: bool = True) -> DecodeCase:
+def decode_workload(n: int, device: Optional[str] = None, bias_on: bool = True,
+                    num_seqs: Optional[int] = None) -> DecodeCase:
     """The decode workloads by number.
 
     1: tiny fp32, 4 seqs x 2 heads x 64, ctx U[1,64], 32-block permuted pool,
@@ -268,31 +269,33 @@ def decode_workload(n: int, device: Optional[str] = None, bias_on: bool = True) 
        shared permuted pool, scale 1/sqrt(128).
     """
     seed = 1000 + n
+    S = num_seqs
     if n == 1:
-        return make_decode_case("tiny-f32-decode", seed, F32, 4, 2, 64, ctx_range=(1, 64), pool_blocks=32,
+        return make_decode_case("tiny-f32-decode", seed, F32, S or 4, 2, 64, ctx_range=(1, 64), pool_blocks=32,
                                 bias="gauss" if bias_on else "none", bias_stride=64, scale=1 / 8,
                                 device=device)
     if n == 2:
-        return make_decode_case("t5-small-self-decode", seed, BF16, 64, 8, 64, ctx_range=(1, 512),
+        return make_decode_case("t5-small-self-decode", seed, BF16, S or 64, 8, 64, ctx_range=(1, 512),
                                 bias="t5" if bias_on else "none", bias_stride=512, scale=1 / 8, device=device)
     if n == 3:
-        return make_decode_case("t5-large-self-decode", seed, BF16, 256, 16, 64, ctx_range=(1, 2048),
+        return make_decode_case("t5-large-self-decode", seed, BF16, S or 256, 16, 64, ctx_range=(1, 2048),
                                 bias="t5" if bias_on else "none", bias_stride=2048, scale=1 / 8, device=device)
     if n == 5:
-        return make_decode_case("long-ctx-f16-window-decode", seed, F16, 512, 16, 128, ctx_range=(16, 8192),
+        return make_decode_case("long-ctx-f16-window-decode", seed, F16, S or 512, 16, 128, ctx_range=(16, 8192),
                                 log_uniform=True, bias="gauss" if bias_on else "none", bias_stride=8192,
                                 bias_std=0.5, bias_pad=float("nan"), window=4096,
                                 scale=1 / math.sqrt(128), device=device)
     raise ValueError(n)
 
 
-def cross_workload(device: Optional[str] = None) -> DecodeCase:
+def cross_workload(device: Optional[str] = None, num_seqs: Optional[int] = None) -> DecodeCase:
     """Encoder cross-attention decode of the T5-large-shaped step: 256 seqs x
     16 heads x 64, every encoder length 512, its own block table and pool, no
     bias, no window."""
     seed = 1000 + 3 + 100
-    return make_decode_case("t5-large-cross-decode", seed, BF16, 256, 16, 64,
-                            context_lens=np.full(256, 512, dtype=np.int32), bias="none",
+    S = num_seqs or 256
+    return make_decode_case("t5-large-cross-decode", seed, BF16, S, 16, 64,
+                            context_lens=np.full(S, 512, dtype=np.int32), bias="none",
                             scale=1 / 8, device=device)
 
 
