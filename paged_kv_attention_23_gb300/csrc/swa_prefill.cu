@@ -8,26 +8,30 @@
 // sequence of length L, the keys c with
 //   window <= 0: all c (causal: c <= r);  window > 0: |r - c| < W (causal: 0 <= r - c < W)
 //   O_r = sum_c softmax_c(scale * q_r . k_c) v_c
-// Only key tiles that intersect the band are visited: a 128-row query tile at
-// r0 reads keys [r0 - W + 1, r0 + 127 + W - 1] (two 128-key tiles for W = 64),
-// i.e. the "visit only intra-window blocks" principle of the same page.
+// Only key tiles that intersect the band are visited ("visit only
+// intra-window blocks", same page).
 //
-// One persistent CTA per SM, warp-specialised:
-//   warp 0      TMA producer: the query tile (128 x 64) into one of two Q
-//               buffers, K and V tiles (128 keys x 64) into a 3-stage ring; all
-//               tiles land 128-byte swizzled, the layout the MMA reads.
-//   warp 1      TMEM owner and MMA issuer (one thread): S = Q K^T as 4 MMAs
-//               128x128x16 into one of two S buffers in TMEM, then
-//               O_j = P V as 8 MMAs 128x64x16 into one of two O buffers.
-//   warps 2..5  softmax, one thread per query row (the TMEM lane): load the S
-//               row, mask, online max / sum in the log2 domain, write P (bf16)
-//               to shared memory in the swizzled layout, then fold the
-//               previous tile's O into an f32 register accumulator with the
-//               running-max correction; at the end normalise and store.
-// S(j+1) is computed while the softmax works on S(j), and P(j) V(j) runs
-// while the softmax works on S(j+1).  Every wait is bounded: on a timeout the
-// CTA records PKA_DEVCHK_TIMEOUT, every role stops, TMEM is freed, and the
-// kernel returns.
+// Work item = two consecutive 128-row query tiles of one (sequence, head)
+// sharing one stream of 128-key K/V tiles (for W = 64: three key tiles per
+// 256 rows, each query tile multiplying only the two it needs).  One
+// persistent CTA per SM, warp-specialised:
+//   warp 0      TMA producer: both query tiles, then the K/V tiles into a
+//               3-stage ring; everything lands 128-byte swizzled.
+//   warp 1      TMEM owner and MMA issuer (one thread): per key tile and
+//               query tile, S = Q K^T (4 x 128x128x16) into that tile's S
+//               columns, then O += P V (8 x 128x64x16, V read MN-major) into
+//               its O columns.  QK of key tile j+1 is issued before PV of j,
+//               so scores are ready when the softmax finishes tile j.
+//   warps 2..5  softmax of query tile 0, warps 6..9 of query tile 1 (the two
+//               groups ping-pong on the tensor core): one thread per row
+//               loads its S row, frees the S columns at once, masks, takes
+//               the max (3-input max), and writes P = 2^(scale*s - m) as bf16
+//               into swizzled shared memory; the scale is folded into the
+//               exponent's FMA.  O stays in TMEM: the running max is raised
+//               only when a row's max grows by more than 2^8, and only then
+//               is that row of O rescaled in TMEM (rows never see P > 256).
+// Every wait is bounded: on a timeout the CTA records PKA_DEVCHK_TIMEOUT,
+// every role stops, TMEM is freed, and the kernel returns.
 #include <cuda.h>
 
 #include <algorithm>
@@ -46,25 +50,28 @@ constexpr int BN = 128;        // keys per K/V tile
 constexpr int HD = 64;         // head dim
 constexpr int NS = 3;          // K/V stages
 constexpr int MAX_SEQS = 1024; // sequences per launch (the host splits larger batches)
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;  // producer, MMA, 2 x 4 softmax warps
+constexpr float RESCALE_LOG2 = 8.f;
 
-constexpr uint32_t TILE_BYTES = BM * HD * 2;          // 16 KB: one Q, K or V tile
-constexpr uint32_t P_BYTES = BM * BN * 2;             // 32 KB: P as two 64-key blocks
-constexpr uint32_t OFF_Q = 0;                          // 2 x 16 KB
-constexpr uint32_t OFF_KV = 2 * TILE_BYTES;            // NS x (K 16 KB, V 16 KB)
-constexpr uint32_t OFF_P = OFF_KV + NS * 2 * TILE_BYTES; // 2 x 32 KB
+constexpr uint32_t TILE_BYTES = BM * HD * 2;             // 16 KB: one Q, K or V tile
+constexpr uint32_t P_BYTES = BM * BN * 2;                // 32 KB: P as two 64-key blocks
+constexpr uint32_t OFF_Q = 0;                             // 2 query tiles
+constexpr uint32_t OFF_KV = 2 * TILE_BYTES;               // NS x (K, V)
+constexpr uint32_t OFF_P = OFF_KV + NS * 2 * TILE_BYTES;  // 2 x P (one per query tile)
 constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
-constexpr int NBAR = 2 + 2 + NS + NS + 2 + 2 + 2 + 2 + 2;
-constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;      // tmem base, abort flag
+// barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], s_empty[2], p_full[2], o_full[2], o_empty[2]
+constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NS, B_SF = 2 + 2 * NS, B_SE = B_SF + 2, B_PF = B_SE + 2,
+              B_OF = B_PF + 2, B_OE = B_OF + 2, NBAR = B_OE + 2;
+constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, abort flag
 constexpr uint32_t OFF_SCHED = (OFF_MISC + 16 + 127) / 128 * 128;
 constexpr uint32_t SMEM_BYTES = OFF_SCHED + (4 * MAX_SEQS + 1) * 4 + 1024;   // + alignment slack
 
-// TMEM columns: S buffers at 0 and 128, O buffers at 256 and 320
+// TMEM columns: S of query tile w at 128 w, O of query tile w at 256 + 64 w
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_O = 256;
 
 constexpr uint32_t IDESC_QK = tc::idesc_bf16_f32(BM, BN, false, false);  // S = Q K^T, both K-major
-constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(BM, HD, false, true);   // O = P V, V is MN-major
+constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(BM, HD, false, true);   // O += P V, V is MN-major
 
 struct Params {
     __nv_bfloat16 *out;
@@ -74,37 +81,53 @@ struct Params {
     int num_seqs, num_tokens, H, window, causal;
 };
 
-struct Tile {
+// One work item: two query tiles [r0, r0+128) and [r0+128, r0+256) of a
+// (sequence, head) and the key tiles c_lo + 128 j, j < nkv, covering both.
+// Query tile w multiplies key tiles jb[w] .. je[w] (empty when jb > je).
+struct Item {
     int s0, L, h, r0, c_lo, nkv;
+    int jb[2], je[2];
 };
 
 struct Sched {
     const int *cum, *start, *len;
     int nseq, H, window, causal;
-    __device__ __forceinline__ Tile get(int t) const
+    __device__ __forceinline__ Item get(int t) const
     {
         int lo = 0, hi = nseq;                         // cum[lo] <= t < cum[hi]
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (cum[mid] <= t) lo = mid; else hi = mid;
         }
-        Tile T;
-        T.s0 = start[lo];
-        T.L = len[lo];
-        const int nq = (T.L + BM - 1) / BM;
+        Item I;
+        I.s0 = start[lo];
+        I.L = len[lo];
+        const int np = (I.L + 2 * BM - 1) / (2 * BM);
         const int r = t - cum[lo];
-        T.h = r / nq;                                  // q tiles of one head are neighbours: shared K/V in L2
-        T.r0 = (r - T.h * nq) * BM;
-        const int r_last = min(T.r0 + BM, T.L) - 1;
-        int c_lo = 0, c_hi = T.L - 1;
-        if (window > 0) {
-            c_lo = max(0, T.r0 - window + 1);
-            c_hi = min(T.L - 1, r_last + window - 1);
+        I.h = r / np;                                  // pairs of one head are neighbours: shared K/V in L2
+        I.r0 = (r - I.h * np) * 2 * BM;
+        int c_lo = 0, c_hi = -1;
+        int lo_w[2], hi_w[2];
+        for (int w = 0; w < 2; ++w) {
+            const int a = I.r0 + w * BM;
+            if (a >= I.L) { lo_w[w] = 0; hi_w[w] = -1; continue; }
+            const int b = min(a + BM, I.L) - 1;
+            int kl = 0, kh = I.L - 1;
+            if (window > 0) { kl = max(0, a - window + 1); kh = min(I.L - 1, b + window - 1); }
+            if (causal) kh = min(kh, b);
+            lo_w[w] = kl;
+            hi_w[w] = kh;
+            if (w == 0) c_lo = kl;
+            c_hi = max(c_hi, kh);
         }
-        if (causal) c_hi = min(c_hi, r_last);
-        T.c_lo = c_lo;
-        T.nkv = (c_hi - c_lo) / BN + 1;
-        return T;
+        I.c_lo = c_lo;
+        I.nkv = (c_hi - c_lo) / BN + 1;
+        for (int w = 0; w < 2; ++w) {
+            if (hi_w[w] < lo_w[w]) { I.jb[w] = 1; I.je[w] = 0; continue; }
+            I.jb[w] = (lo_w[w] - c_lo) / BN;
+            I.je[w] = (hi_w[w] - c_lo) / BN;
+        }
+        return I;
     }
 };
 
@@ -134,13 +157,8 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     const uint32_t bar0 = sb + OFF_BAR;
     auto BAR = [&](int i) { return bar0 + 8u * i; };
-    // barrier indices
-    const int Q_FULL = 0, Q_EMPTY = 2, KV_FULL = 4, KV_EMPTY = 4 + NS, S_FULL = 4 + 2 * NS, S_EMPTY = S_FULL + 2,
-              P_FULL = S_EMPTY + 2, O_FULL = P_FULL + 2, O_EMPTY = O_FULL + 2;
     uint32_t *tmem_base_sm = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
     int *cum = reinterpret_cast<int *>(smem + OFF_SCHED);
@@ -160,8 +178,8 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NBAR; ++i) {
-            const bool by_softmax = (i >= S_EMPTY && i < S_EMPTY + 2) || (i >= P_FULL && i < P_FULL + 2) ||
-                                    (i >= O_EMPTY && i < O_EMPTY + 2);
+            const bool by_softmax = (i >= B_SE && i < B_SE + 2) || (i >= B_PF && i < B_PF + 2) ||
+                                    (i >= B_OE && i < B_OE + 2);
             mbar_init(BAR(i), by_softmax ? 128 : 1);
         }
         *abort_flag = 0;
@@ -178,7 +196,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             const int Lt = rank_tmp[t];
             rk += (Lt > Ls) || (Lt == Ls && t < s);
         }
-        int a = P.cu_seqlens[s];
+        const int a = P.cu_seqlens[s];
         start[rk] = a < 0 ? 0 : a;
         len[rk] = Ls;
     }
@@ -187,7 +205,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const int per = (S + 31) / 32;
         const int a = min(lane * per, S), b = min(a + per, S);
         int local = 0;
-        for (int i = a; i < b; ++i) local += (len[i] + BM - 1) / BM * P.H;
+        for (int i = a; i < b; ++i) local += (len[i] + 2 * BM - 1) / (2 * BM) * P.H;
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -195,12 +213,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             if (lane >= o) incl += v;
         }
         int run = incl - local;
-        for (int i = a; i < b; ++i) { cum[i] = run; run += (len[i] + BM - 1) / BM * P.H; }
+        for (int i = a; i < b; ++i) { cum[i] = run; run += (len[i] + 2 * BM - 1) / (2 * BM) * P.H; }
         if (lane == 31) cum[S] = incl;
     }
     __syncthreads();
     const Sched sched{cum, start, len, S, P.H, P.window, P.causal};
-    const int total_tiles = cum[S];
+    const int total_items = cum[S];
     const uint32_t tmem = *tmem_base_sm;
 
     if (warp == 0 && lane == 0) {
@@ -209,161 +227,192 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         tc::prefetch_tensormap(&tm_k);
         tc::prefetch_tensormap(&tm_v);
         uint32_t g = 0, wq = 0;
-        for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x, ++wq) {
-            const Tile T = sched.get(t);
-            const uint32_t qb = wq & 1;
-            if (!wait_or_abort(BAR(Q_EMPTY + qb), ((wq >> 1) & 1) ^ 1, abort_flag, P.status)) break;
-            mbar_arrive_expect_tx(BAR(Q_FULL + qb), TILE_BYTES);
-            tc::tma_load_3d(sb + OFF_Q + qb * TILE_BYTES, &tm_q, 0, T.h, T.s0 + T.r0, BAR(Q_FULL + qb));
+        for (int t = blockIdx.x; t < total_items && !*abort_flag; t += gridDim.x, ++wq) {
+            const Item I = sched.get(t);
+            if (!wait_or_abort(BAR(B_QE), (wq & 1) ^ 1, abort_flag, P.status)) break;
+            const bool two = I.r0 + BM < I.L;
+            mbar_arrive_expect_tx(BAR(B_QF), (two ? 2 : 1) * TILE_BYTES);
+            tc::tma_load_3d(sb + OFF_Q, &tm_q, 0, I.h, I.s0 + I.r0, BAR(B_QF));
+            if (two) tc::tma_load_3d(sb + OFF_Q + TILE_BYTES, &tm_q, 0, I.h, I.s0 + I.r0 + BM, BAR(B_QF));
             bool ok = true;
-            for (int j = 0; j < T.nkv; ++j, ++g) {
+            for (int j = 0; j < I.nkv; ++j, ++g) {
                 const uint32_t st = g % NS;
-                if (!wait_or_abort(BAR(KV_EMPTY + st), ((g / NS) & 1) ^ 1, abort_flag, P.status)) { ok = false; break; }
-                const int row = T.s0 + T.c_lo + j * BN;
-                mbar_arrive_expect_tx(BAR(KV_FULL + st), 2 * TILE_BYTES);
-                tc::tma_load_3d(sb + OFF_KV + st * 2 * TILE_BYTES, &tm_k, 0, T.h, row, BAR(KV_FULL + st));
-                tc::tma_load_3d(sb + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES, &tm_v, 0, T.h, row,
-                                BAR(KV_FULL + st));
+                if (!wait_or_abort(BAR(B_KVE + st), ((g / NS) & 1) ^ 1, abort_flag, P.status)) { ok = false; break; }
+                const int row = I.s0 + I.c_lo + j * BN;
+                mbar_arrive_expect_tx(BAR(B_KVF + st), 2 * TILE_BYTES);
+                tc::tma_load_3d(sb + OFF_KV + st * 2 * TILE_BYTES, &tm_k, 0, I.h, row, BAR(B_KVF + st));
+                tc::tma_load_3d(sb + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES, &tm_v, 0, I.h, row, BAR(B_KVF + st));
             }
             if (!ok) break;
         }
     } else if (warp == 1 && lane == 0) {
         // ======================= MMA issuer =======================
         uint32_t g = 0, wq = 0;
-        auto issue_pv = [&](uint32_t gg) -> bool {
-            const uint32_t pb = gg & 1;
-            if (!wait_or_abort(BAR(P_FULL + pb), (gg >> 1) & 1, abort_flag, P.status)) return false;
-            if (!wait_or_abort(BAR(O_EMPTY + pb), ((gg >> 1) & 1) ^ 1, abort_flag, P.status)) return false;
-            tc::fence_after_sync();
-            const uint32_t pa = sb + OFF_P + pb * P_BYTES;
-            const uint32_t va = sb + OFF_KV + (gg % NS) * 2 * TILE_BYTES + TILE_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-                tc::mma_bf16(tmem + COL_O + pb * HD, tc::sw128_desc(pa + (kk >> 2) * (P_BYTES / 2) + (kk & 3) * 32),
-                             tc::sw128_desc(va + kk * 2048), IDESC_PV, kk > 0);
-            tc::commit(BAR(O_FULL + pb));
-            tc::commit(BAR(KV_EMPTY + gg % NS));
-            return true;
-        };
-        for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x, ++wq) {
-            const Tile T = sched.get(t);
-            const uint32_t qb = wq & 1;
-            if (!wait_or_abort(BAR(Q_FULL + qb), (wq >> 1) & 1, abort_flag, P.status)) break;
-            const uint32_t qa = sb + OFF_Q + qb * TILE_BYTES;
+        uint32_t cs[2] = {0, 0}, co[2] = {0, 0};     // per query tile: key tiles done, items done
+        for (int t = blockIdx.x; t < total_items && !*abort_flag; t += gridDim.x, ++wq) {
+            const Item I = sched.get(t);
+            if (!wait_or_abort(BAR(B_QF), wq & 1, abort_flag, P.status)) break;
             bool ok = true;
-            for (int j = 0; j < T.nkv; ++j, ++g) {
-                const uint32_t st = g % NS, sbuf = g & 1;
-                if (!wait_or_abort(BAR(KV_FULL + st), (g / NS) & 1, abort_flag, P.status) ||
-                    !wait_or_abort(BAR(S_EMPTY + sbuf), ((g >> 1) & 1) ^ 1, abort_flag, P.status)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
+            // S = Q_w K_j^T for every query tile w that needs key tile j
+            auto issue_qk = [&](int j) -> bool {
+                const uint32_t gg = g + j, st = gg % NS;
+                if (!wait_or_abort(BAR(B_KVF + st), (gg / NS) & 1, abort_flag, P.status)) return false;
                 const uint32_t ka = sb + OFF_KV + st * 2 * TILE_BYTES;
+                for (int w = 0; w < 2; ++w) {
+                    if (j < I.jb[w] || j > I.je[w]) continue;
+                    const uint32_t c = cs[w] + (j - I.jb[w]);
+                    if (!wait_or_abort(BAR(B_SE + w), (c & 1) ^ 1, abort_flag, P.status)) return false;
+                    tc::fence_after_sync();
+                    const uint32_t qa = sb + OFF_Q + w * TILE_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk)
-                    tc::mma_bf16(tmem + COL_S + sbuf * BN, tc::sw128_desc(qa + kk * 32), tc::sw128_desc(ka + kk * 32),
-                                 IDESC_QK, kk > 0);
-                tc::commit(BAR(S_FULL + sbuf));
-                if (j > 0 && !issue_pv(g - 1)) { ok = false; break; }
+                    for (int kk = 0; kk < HD / 16; ++kk)
+                        tc::mma_bf16(tmem + COL_S + w * BN, tc::sw128_desc(qa + kk * 32), tc::sw128_desc(ka + kk * 32),
+                                     IDESC_QK, kk > 0);
+                    tc::commit(BAR(B_SF + w));
+                }
+                if (j == I.nkv - 1) tc::commit(BAR(B_QE));      // last reader of the query tiles
+                return true;
+            };
+            // O_w += P_w V_j
+            auto issue_pv = [&](int j) -> bool {
+                const uint32_t st = (g + j) % NS;
+                const uint32_t va = sb + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES;
+                for (int w = 0; w < 2; ++w) {
+                    if (j < I.jb[w] || j > I.je[w]) continue;
+                    const uint32_t c = cs[w] + (j - I.jb[w]);
+                    if (!wait_or_abort(BAR(B_PF + w), c & 1, abort_flag, P.status)) return false;
+                    if (j == I.jb[w] && !wait_or_abort(BAR(B_OE + w), (co[w] & 1) ^ 1, abort_flag, P.status))
+                        return false;
+                    tc::fence_after_sync();
+                    const uint32_t pa = sb + OFF_P + w * P_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        tc::mma_bf16(tmem + COL_O + w * HD,
+                                     tc::sw128_desc(pa + (kk >> 2) * (P_BYTES / 2) + (kk & 3) * 32),
+                                     tc::sw128_desc(va + kk * 2048), IDESC_PV, kk > 0 || j > I.jb[w]);
+                    tc::commit(BAR(B_OF + w));
+                }
+                tc::commit(BAR(B_KVE + st));
+                return true;
+            };
+            if (!issue_qk(0)) break;
+            for (int j = 0; j < I.nkv && ok; ++j) {
+                if (j + 1 < I.nkv && !issue_qk(j + 1)) ok = false;
+                if (ok && !issue_pv(j)) ok = false;
             }
-            if (!ok || !issue_pv(g - 1)) break;
-            tc::commit(BAR(Q_EMPTY + qb));
+            if (!ok) break;
+            g += I.nkv;
+            for (int w = 0; w < 2; ++w)
+                if (I.jb[w] <= I.je[w]) { cs[w] += I.je[w] - I.jb[w] + 1; ++co[w]; }
         }
     } else if (warp >= 2) {
-        // ======================= softmax =======================
+        // ======================= softmax (query tile w) =======================
+        const int w = (warp - 2) >> 2;
         const int quarter = warp & 3;                  // TMEM lanes this warp may touch
         const int row = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-        uint32_t g = 0;
-        for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-            const Tile T = sched.get(t);
-            const int rr = T.r0 + row;                 // query position within its sequence
-            int lo = 0, hi = T.L;                      // keys [lo, hi) kept for this row
+        const uint32_t tS = tmem + lane_addr + COL_S + w * BN;
+        const uint32_t tO = tmem + lane_addr + COL_O + w * HD;
+        const uint32_t pbase = sb + OFF_P + w * P_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
+        uint32_t cs = 0, co = 0;
+        for (int t = blockIdx.x; t < total_items && !*abort_flag; t += gridDim.x) {
+            const Item I = sched.get(t);
+            if (I.jb[w] > I.je[w]) continue;           // this query tile lies past the sequence
+            const int rr = I.r0 + w * BM + row;        // query position within its sequence
+            int lo = 0, hi = I.L;                      // keys [lo, hi) kept for this row
             if (P.window > 0) { lo = max(lo, rr - P.window + 1); hi = min(hi, rr + P.window); }
             if (P.causal) hi = min(hi, rr + 1);
-            float O[HD];
-#pragma unroll
-            for (int i = 0; i < HD; ++i) O[i] = 0.f;
-            float m = -INFINITY, l = 0.f, corr_prev = 1.f;
+            float m = -INFINITY, l = 0.f;
             bool ok = true;
-            auto fold_o = [&](uint32_t gg, float c) -> bool {
-                const uint32_t ob = gg & 1;
-                if (!wait_or_abort(BAR(O_FULL + ob), (gg >> 1) & 1, abort_flag, P.status)) return false;
-                tc::fence_after_sync();
-                float o[HD];
-                tc::tmem_ld64(tmem + lane_addr + COL_O + ob * HD, o);
-                tc::fence_before_sync();
-                mbar_arrive(BAR(O_EMPTY + ob));
-#pragma unroll
-                for (int i = 0; i < HD; ++i) O[i] = fmaf(O[i], c, o[i]);
-                return true;
-            };
-            for (int j = 0; j < T.nkv; ++j, ++g) {
-                const uint32_t sbuf = g & 1;
-                if (!wait_or_abort(BAR(S_FULL + sbuf), (g >> 1) & 1, abort_flag, P.status)) { ok = false; break; }
+            for (int j = I.jb[w]; j <= I.je[w]; ++j, ++cs) {
+                if (!wait_or_abort(BAR(B_SF + w), cs & 1, abort_flag, P.status)) { ok = false; break; }
                 tc::fence_after_sync();
                 float x[BN];
-                tc::tmem_ld64(tmem + lane_addr + COL_S + sbuf * BN, x);
-                tc::tmem_ld64(tmem + lane_addr + COL_S + sbuf * BN + 64, x + 64);
+                tc::tmem_ld64(tS, x);
+                tc::tmem_ld64(tS + 64, x + 64);
                 tc::fence_before_sync();
-                mbar_arrive(BAR(S_EMPTY + sbuf));
-                // mask to the kept key range, scale into the log2 domain, tile max
-                const int c0 = T.c_lo + j * BN;
+                mbar_arrive(BAR(B_SE + w));            // S columns free: QK of the next key tile may start
+                // mask to the kept key range; tile max of the raw scores
+                const int c0 = I.c_lo + j * BN;
                 const int ilo = lo - c0, ihi = hi - c0;
-                float mt = -INFINITY;
-                if (ilo <= 0 && ihi >= BN) {
+                if (ilo > 0 || ihi < BN) {
 #pragma unroll
-                    for (int i = 0; i < BN; ++i) { x[i] *= P.scale_log2; mt = fmaxf(mt, x[i]); }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < BN; ++i) {
-                        x[i] = (i >= ilo && i < ihi) ? x[i] * P.scale_log2 : -INFINITY;
-                        mt = fmaxf(mt, x[i]);
-                    }
+                    for (int i = 0; i < BN; ++i) x[i] = (i >= ilo && i < ihi) ? x[i] : -INFINITY;
                 }
-                const float m_new = fmaxf(m, mt);
-                const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                const float corr = ex2(m - m_use);
-                // P = 2^(x - m) as bf16 into the swizzled P buffer; row sum in f32
-                const uint32_t pbase = sb + OFF_P + sbuf * P_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
-                float lt = 0.f;
+                float mx[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float a = x[k * 32];
+#pragma unroll
+                    for (int i = 1; i < 32; i += 2) a = tc::max3(a, x[k * 32 + i], x[k * 32 + i + 1]);
+                    mx[k] = fmaxf(a, x[k * 32 + 31]);
+                }
+                const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * P.scale_log2;
+                // raise the running max only when it grows by more than 2^8
+                const bool raise = mt > m + RESCALE_LOG2;
+                const float m_old = m;
+                if (raise) m = mt;
+                if (j > I.jb[w]) {
+                    // P V of the previous key tile is done: P may be overwritten, O rescaled
+                    if (!wait_or_abort(BAR(B_OF + w), (cs - 1) & 1, abort_flag, P.status)) { ok = false; break; }
+                    tc::fence_after_sync();
+                }
+                if (raise) l *= ex2(m_old - m);
+                // P = 2^(scale * s - m) as bf16 into the swizzled buffer; row sum in f32
+                const float mneg = m == -INFINITY ? 0.f : -m;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < BN / 8; ++c) {
-                    uint32_t w[4];
+                    uint32_t wv[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float p0 = ex2(x[c * 8 + 2 * e] - m_use), p1 = ex2(x[c * 8 + 2 * e + 1] - m_use);
-                        lt += p0 + p1;
+                        const float p0 = ex2(fmaf(x[c * 8 + 2 * e], P.scale_log2, mneg));
+                        const float p1 = ex2(fmaf(x[c * 8 + 2 * e + 1], P.scale_log2, mneg));
+                        ls[e] += p0 + p1;
                         __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
-                        w[e] = *reinterpret_cast<uint32_t *>(&hb);
+                        wv[e] = *reinterpret_cast<uint32_t *>(&hb);
                     }
-                    const uint32_t kb = c >> 3, ch = c & 7;
-                    const uint32_t addr = pbase + kb * (P_BYTES / 2) + ((ch ^ (row & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                                 "r"(w[2]), "r"(w[3])
+                    const uint32_t addr = pbase + (c >> 3) * (P_BYTES / 2) + (((c & 7) ^ (row & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(wv[0]), "r"(wv[1]),
+                                 "r"(wv[2]), "r"(wv[3])
                                  : "memory");
                 }
-                l = fmaf(l, corr, lt);
-                m = m_new;
+                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                if (j > I.jb[w] && __any_sync(kFull, raise)) {
+                    // the running max rose: bring this row's O to the new max (in TMEM)
+                    const float c = raise ? ex2(m_old - m) : 1.f;
+                    float o[HD];
+                    tc::tmem_ld64(tO, o);
+#pragma unroll
+                    for (int i = 0; i < HD; ++i) o[i] *= c;
+                    tc::tmem_st64(tO, o);
+                }
                 fence_proxy_async();                   // P is read by the tensor cores (async proxy)
-                mbar_arrive(BAR(P_FULL + sbuf));
-                if (j > 0 && !fold_o(g - 1, corr_prev)) { ok = false; break; }
-                corr_prev = corr;
+                tc::fence_before_sync();               // orders the O rescale before the next P V
+                mbar_arrive(BAR(B_PF + w));
             }
-            if (!ok || !fold_o(g - 1, corr_prev)) break;
-            if (rr < T.L) {
+            if (!ok) break;
+            // all key tiles done: read O, free the O columns, normalise, store
+            if (!wait_or_abort(BAR(B_OF + w), (cs - 1) & 1, abort_flag, P.status)) break;
+            tc::fence_after_sync();
+            float o[HD];
+            tc::tmem_ld64(tO, o);
+            tc::fence_before_sync();
+            mbar_arrive(BAR(B_OE + w));
+            ++co;
+            if (rr < I.L) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                uint4 *dst = reinterpret_cast<uint4 *>(P.out + ((size_t)(T.s0 + rr) * P.H + T.h) * HD);
+                uint4 *dst = reinterpret_cast<uint4 *>(P.out + ((size_t)(I.s0 + rr) * P.H + I.h) * HD);
 #pragma unroll
                 for (int c = 0; c < HD / 8; ++c) {
                     float v[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = O[c * 8 + e] * inv;
+                    for (int e = 0; e < 8; ++e) v[e] = o[c * 8 + e] * inv;
                     dst[c] = Vec<__nv_bfloat16>::from_f32(v);
                 }
             }
         }
+        (void)co;
     }
 
     // ---- teardown: every role is done with TMEM --------------------------------
@@ -438,7 +487,7 @@ cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream)
     for (int base = 0; base < a.num_seqs; base += MAX_SEQS) {
         P.num_seqs = std::min(MAX_SEQS, a.num_seqs - base);
         P.cu_seqlens = a.cu_seqlens + base;
-        const long long tiles_upper = (long long)P.num_seqs * ((a.max_seqlen + BM - 1) / BM) * a.num_heads;
+        const long long tiles_upper = (long long)P.num_seqs * ((a.max_seqlen + 2 * BM - 1) / (2 * BM)) * a.num_heads;
         const int grid = (int)std::max<long long>(1, std::min<long long>(sms, tiles_upper));
         swa_prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mq, mk, mv, P);
         const cudaError_t e = cudaGetLastError();
