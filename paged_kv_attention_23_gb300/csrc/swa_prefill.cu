@@ -131,6 +131,52 @@ struct Sched {
     }
 };
 
+// (y0, y1) = (x0, x1) * s + (c, c) and (a0, a1) += (y0, y1) as single packed
+// f32x2 instructions (sm_100+): the softmax is issue-bound, so pairs halve
+// the FMA and add work per score.
+__device__ __forceinline__ void fma2(float x0, float x1, float s, float c, float &y0, float &y1)
+{
+    asm("{\n\t.reg .b64 a, m, k, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 m, {%4, %4};\n\tmov.b64 k, {%5, %5};\n\t"
+        "fma.rn.f32x2 d, a, m, k;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(y0), "=f"(y1)
+        : "f"(x0), "f"(x1), "f"(s), "f"(c));
+}
+
+__device__ __forceinline__ void add2(float &a0, float &a1, float y0, float y1)
+{
+    asm("{\n\t.reg .b64 a, y;\n\t"
+        "mov.b64 a, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+        "add.rn.f32x2 a, a, y;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(y0), "f"(y1));
+}
+
+// P = 2^(scale * s - m) for one tile row as bf16 into the swizzled P buffer;
+// returns the f32 row sum.
+__device__ __forceinline__ float write_p_row(const float *x, float scale_log2, float mneg, uint32_t pbase, int row)
+{
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < BN / 8; ++c) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float a0, a1;
+            fma2(x[c * 8 + 2 * e], x[c * 8 + 2 * e + 1], scale_log2, mneg, a0, a1);
+            const float p0 = ex2(a0), p1 = ex2(a1);
+            add2(ls[(e & 1) * 2], ls[(e & 1) * 2 + 1], p0, p1);
+            __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
+            wv[e] = *reinterpret_cast<uint32_t *>(&hb);
+        }
+        const uint32_t addr = pbase + (c >> 3) * (P_BYTES / 2) + (((c & 7) ^ (row & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(wv[0]), "r"(wv[1]), "r"(wv[2]),
+                     "r"(wv[3])
+                     : "memory");
+    }
+    return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+}
+
 // bounded wait that also gives up once another role has aborted
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                               int32_t *status)
@@ -335,7 +381,8 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 // mask to the kept key range; tile max of the raw scores
                 const int c0 = I.c_lo + j * BN;
                 const int ilo = lo - c0, ihi = hi - c0;
-                if (ilo > 0 || ihi < BN) {
+                const bool masked = ilo > 0 || ihi < BN;
+                if (masked) {
 #pragma unroll
                     for (int i = 0; i < BN; ++i) x[i] = (i >= ilo && i < ihi) ? x[i] : -INFINITY;
                 }
@@ -360,24 +407,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 if (raise) l *= ex2(m_old - m);
                 // P = 2^(scale * s - m) as bf16 into the swizzled buffer; row sum in f32
                 const float mneg = m == -INFINITY ? 0.f : -m;
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < BN / 8; ++c) {
-                    uint32_t wv[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float p0 = ex2(fmaf(x[c * 8 + 2 * e], P.scale_log2, mneg));
-                        const float p1 = ex2(fmaf(x[c * 8 + 2 * e + 1], P.scale_log2, mneg));
-                        ls[e] += p0 + p1;
-                        __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
-                        wv[e] = *reinterpret_cast<uint32_t *>(&hb);
-                    }
-                    const uint32_t addr = pbase + (c >> 3) * (P_BYTES / 2) + (((c & 7) ^ (row & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(wv[0]), "r"(wv[1]),
-                                 "r"(wv[2]), "r"(wv[3])
-                                 : "memory");
-                }
-                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                l += write_p_row(x, P.scale_log2, mneg, pbase, row);
                 if (j > I.jb[w] && __any_sync(kFull, raise)) {
                     // the running max rose: bring this row's O to the new max (in TMEM)
                     const float c = raise ? ex2(m_old - m) : 1.f;
