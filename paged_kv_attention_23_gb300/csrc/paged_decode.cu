@@ -480,12 +480,40 @@ size_t decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, const D
     return round_up(sh * 4, 256) + round_up(slots * 8, 256) + round_up(slots * head_dim * 4, 256);
 }
 
-cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream)
+// Streaming warps per CTA of the configuration dispatch_cfg picks.
+static int streaming_warps(pka_dtype dt, int head_dim)
+{
+    const int stage = dt == PKA_F32 ? (head_dim == 64 ? Tr<float, 64>::STAGE : Tr<float, 128>::STAGE)
+                                    : (head_dim == 64 ? Tr<__half, 64>::STAGE : Tr<__half, 128>::STAGE);
+    return stage <= 5000 ? 16 : stage <= 9000 ? 12 : 6;
+}
+
+cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &size_plan, cudaStream_t stream)
 {
     if (a.num_seqs == 0) return cudaSuccess;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // Fewer, larger partitions cost fewer split-K merges (each ends with a
+    // release and an atomic), while enough units keep every warp busy: double
+    // the partition while the batch still yields at least 3 units per
+    // streaming warp of the GPU.  The workspace was sized for size_plan, the
+    // smallest partitions, so it covers any larger ones.
+    DecodePlan plan = size_plan;
+    {
+        long long maxvb = (long long)plan.max_parts * plan.part_blocks;
+        const long long sh = (long long)a.num_seqs * a.num_heads;
+        const long long target = 3ll * sms * streaming_warps(a.dtype, a.head_dim);
+        int pb = plan.part_blocks;
+        long long vb = (a.max_context_len + BS - 1) / BS;
+        if (a.window > 0) vb = std::min<long long>(vb, (a.window + BS - 2) / BS + 1);
+        maxvb = std::max<long long>(1, std::min(maxvb, vb));
+        while (pb < 32 && sh * ((maxvb + 2 * pb - 1) / (2 * pb)) >= target) pb *= 2;
+        if (pb != plan.part_blocks) {
+            plan.part_blocks = pb;
+            plan.max_parts = (int)std::max<long long>(1, (maxvb + pb - 1) / pb);
+        }
+    }
     const size_t sh = (size_t)a.num_seqs * a.num_heads;
     const size_t slots = sh * plan.max_parts;
     unsigned char *ws = static_cast<unsigned char *>(a.workspace);
