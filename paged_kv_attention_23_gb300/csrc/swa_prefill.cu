@@ -17,11 +17,12 @@
 // persistent CTA per SM, warp-specialised:
 //   warp 0      TMA producer: both query tiles, then the K/V tiles into a
 //               3-stage ring; everything lands 128-byte swizzled.
-//   warp 1      TMEM owner and MMA issuer (one thread): per key tile and
-//               query tile, S = Q K^T (4 x 128x128x16) into that tile's S
-//               columns, then O += P V (8 x 128x64x16, V read MN-major) into
-//               its O columns.  QK of key tile j+1 is issued before PV of j,
-//               so scores are ready when the softmax finishes tile j.
+//   warp 1      TMEM owner; with warp 10, one MMA-issuing thread per query
+//               tile (each blocks only on its own tile's barriers): per key
+//               tile, S = Q K^T (4 x 128x128x16) into that tile's S columns,
+//               then O += P V (8 x 128x64x16, V read MN-major) into its O
+//               columns.  QK of key tile j+1 is issued before PV of j, so
+//               scores are ready when the softmax finishes tile j.
 //   warps 2..5  softmax of query tile 0, warps 6..9 of query tile 1 (the two
 //               groups ping-pong on the tensor core): one thread per row
 //               loads its S row, frees the S columns at once, masks, takes
@@ -50,7 +51,7 @@ constexpr int BN = 128;        // keys per K/V tile
 constexpr int HD = 64;         // head dim
 constexpr int NS = 3;          // K/V stages
 constexpr int MAX_SEQS = 1024; // sequences per launch (the host splits larger batches)
-constexpr int NTHREADS = 320;  // producer, MMA, 2 x 4 softmax warps
+constexpr int NTHREADS = 352;  // producer, MMA (tile 0), 2 x 4 softmax warps, MMA (tile 1)
 constexpr float RESCALE_LOG2 = 8.f;
 
 constexpr uint32_t TILE_BYTES = BM * HD * 2;             // 16 KB: one Q, K or V tile
@@ -226,7 +227,8 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         for (int i = 0; i < NBAR; ++i) {
             const bool by_softmax = (i >= B_SE && i < B_SE + 2) || (i >= B_PF && i < B_PF + 2) ||
                                     (i >= B_OE && i < B_OE + 2);
-            mbar_init(BAR(i), by_softmax ? 128 : 1);
+            const bool by_both_mma = i == B_QE || (i >= B_KVE && i < B_KVE + NS);
+            mbar_init(BAR(i), by_softmax ? 128 : by_both_mma ? 2 : 1);
         }
         *abort_flag = 0;
     }
@@ -291,67 +293,65 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             }
             if (!ok) break;
         }
-    } else if (warp == 1 && lane == 0) {
-        // ======================= MMA issuer =======================
-        uint32_t g = 0, wq = 0;
-        uint32_t cs[2] = {0, 0}, co[2] = {0, 0};     // per query tile: key tiles done, items done
+    } else if ((warp == 1 || warp == NTHREADS / 32 - 1) && lane == 0) {
+        // ============ MMA issuer of query tile w (one thread per query tile) ============
+        // Each issuer blocks only on its own query tile's barriers; both read
+        // every K/V stage and query tile, so those are released by two arrivals.
+        const int w = warp == 1 ? 0 : 1;
+        uint32_t g = 0, wq = 0, cs = 0, co = 0;
         for (int t = blockIdx.x; t < total_items && !*abort_flag; t += gridDim.x, ++wq) {
             const Item I = sched.get(t);
             if (!wait_or_abort(BAR(B_QF), wq & 1, abort_flag, P.status)) break;
-            bool ok = true;
-            // S = Q_w K_j^T for every query tile w that needs key tile j
+            const bool mine = I.jb[w] <= I.je[w];
+            if (!mine) mbar_arrive(BAR(B_QE));
+            // S_w = Q_w K_j^T, when query tile w needs key tile j
             auto issue_qk = [&](int j) -> bool {
                 const uint32_t gg = g + j, st = gg % NS;
                 if (!wait_or_abort(BAR(B_KVF + st), (gg / NS) & 1, abort_flag, P.status)) return false;
-                const uint32_t ka = sb + OFF_KV + st * 2 * TILE_BYTES;
-                for (int w = 0; w < 2; ++w) {
-                    if (j < I.jb[w] || j > I.je[w]) continue;
-                    const uint32_t c = cs[w] + (j - I.jb[w]);
-                    if (!wait_or_abort(BAR(B_SE + w), (c & 1) ^ 1, abort_flag, P.status)) return false;
-                    tc::fence_after_sync();
-                    const uint32_t qa = sb + OFF_Q + w * TILE_BYTES;
+                if (j < I.jb[w] || j > I.je[w]) return true;
+                const uint32_t c = cs + (j - I.jb[w]);
+                if (!wait_or_abort(BAR(B_SE + w), (c & 1) ^ 1, abort_flag, P.status)) return false;
+                tc::fence_after_sync();
+                const uint32_t qa = sb + OFF_Q + w * TILE_BYTES, ka = sb + OFF_KV + st * 2 * TILE_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < HD / 16; ++kk)
-                        tc::mma_bf16(tmem + COL_S + w * BN, tc::sw128_desc(qa + kk * 32), tc::sw128_desc(ka + kk * 32),
-                                     IDESC_QK, kk > 0);
-                    tc::commit(BAR(B_SF + w));
-                }
-                if (j == I.nkv - 1) tc::commit(BAR(B_QE));      // last reader of the query tiles
+                for (int kk = 0; kk < HD / 16; ++kk)
+                    tc::mma_bf16(tmem + COL_S + w * BN, tc::sw128_desc(qa + kk * 32), tc::sw128_desc(ka + kk * 32),
+                                 IDESC_QK, kk > 0);
+                tc::commit(BAR(B_SF + w));
+                if (j == I.je[w]) tc::commit(BAR(B_QE));         // last read of Q_w in this item
                 return true;
             };
-            // O_w += P_w V_j
+            // O_w += P_w V_j, then release the K/V stage (or just release it)
             auto issue_pv = [&](int j) -> bool {
                 const uint32_t st = (g + j) % NS;
-                const uint32_t va = sb + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES;
-                for (int w = 0; w < 2; ++w) {
-                    if (j < I.jb[w] || j > I.je[w]) continue;
-                    const uint32_t c = cs[w] + (j - I.jb[w]);
-                    if (!wait_or_abort(BAR(B_PF + w), c & 1, abort_flag, P.status)) return false;
-                    if (j == I.jb[w] && !wait_or_abort(BAR(B_OE + w), (co[w] & 1) ^ 1, abort_flag, P.status))
-                        return false;
-                    tc::fence_after_sync();
-                    const uint32_t pa = sb + OFF_P + w * P_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        tc::mma_bf16(tmem + COL_O + w * HD,
-                                     tc::sw128_desc(pa + (kk >> 2) * (P_BYTES / 2) + (kk & 3) * 32),
-                                     tc::sw128_desc(va + kk * 2048), IDESC_PV, kk > 0 || j > I.jb[w]);
-                    tc::commit(BAR(B_OF + w));
+                if (j < I.jb[w] || j > I.je[w]) {
+                    mbar_arrive(BAR(B_KVE + st));
+                    return true;
                 }
+                const uint32_t c = cs + (j - I.jb[w]);
+                if (!wait_or_abort(BAR(B_PF + w), c & 1, abort_flag, P.status)) return false;
+                if (j == I.jb[w] && !wait_or_abort(BAR(B_OE + w), (co & 1) ^ 1, abort_flag, P.status)) return false;
+                tc::fence_after_sync();
+                const uint32_t pa = sb + OFF_P + w * P_BYTES;
+                const uint32_t va = sb + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    tc::mma_bf16(tmem + COL_O + w * HD, tc::sw128_desc(pa + (kk >> 2) * (P_BYTES / 2) + (kk & 3) * 32),
+                                 tc::sw128_desc(va + kk * 2048), IDESC_PV, kk > 0 || j > I.jb[w]);
+                tc::commit(BAR(B_OF + w));
                 tc::commit(BAR(B_KVE + st));
                 return true;
             };
-            if (!issue_qk(0)) break;
+            bool ok = issue_qk(0);
             for (int j = 0; j < I.nkv && ok; ++j) {
                 if (j + 1 < I.nkv && !issue_qk(j + 1)) ok = false;
                 if (ok && !issue_pv(j)) ok = false;
             }
             if (!ok) break;
             g += I.nkv;
-            for (int w = 0; w < 2; ++w)
-                if (I.jb[w] <= I.je[w]) { cs[w] += I.je[w] - I.jb[w] + 1; ++co[w]; }
+            if (mine) { cs += I.je[w] - I.jb[w] + 1; ++co; }
         }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < 10) {
         // ======================= softmax (query tile w) =======================
         const int w = (warp - 2) >> 2;
         const int quarter = warp & 3;                  // TMEM lanes this warp may touch
