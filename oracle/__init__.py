@@ -13,6 +13,10 @@ Functions and the passages they follow:
   table for decoder self-attention, another for encoder cross-attention);
   causal sliding window keeping the W most recent keys ("[V1] Add sliding
   window support to Flex Attention backend").
+* ``paged_decode_t5`` — the same with the bias read from a T5 relative-
+  position table [H, num_buckets] at column min(ctx - 1 - j, num_buckets - 1)
+  (same page: capped distance, last value reused; computing the T5 bias in
+  the kernel instead of materialising it).
 * ``prefill`` — the same softmax attention for every row of a packed varlen
   batch, mask = full / causal / bidirectional band |i-j| < W / causal band
   ("[V1] Add sliding window support to Flex Attention backend").
@@ -57,6 +61,9 @@ def _load():
         lib.oracle_paged_decode.argtypes = [P, P, P, P, P, P, P, I, ctypes.c_double, I, I, I, I, I, I, I,
                                             P, I, I]
         lib.oracle_paged_decode.restype = None
+        lib.oracle_paged_decode_t5.argtypes = [P, P, P, P, P, P, P, I, I, ctypes.c_double, I, I, I, I, I, I,
+                                               P, I, I]
+        lib.oracle_paged_decode_t5.restype = None
         lib.oracle_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_double, I, P,
                                        ctypes.c_longlong, I]
         lib.oracle_prefill.restype = None
@@ -105,6 +112,24 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, bias, window, 
     lib.oracle_paged_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(cl), _ptr(bias),
                             int(window), float(scale), int(block_size), S, H, D, int(bt.shape[1]), stride,
                             int(dtype), _ptr(pr), n, int(nthreads or default_threads()))
+    return out if pr is not None else out.reshape(S, H, D)
+
+
+def paged_decode_t5(q, k_cache, v_cache, block_tables, context_lens, bias_table, window, scale, block_size,
+                    dtype, pairs=None, nthreads=None) -> np.ndarray:
+    """Decode with the T5 bias read from its [H, num_buckets] table."""
+    lib = _load()
+    q = _c(q); k_cache = _c(k_cache); v_cache = _c(v_cache)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    tab = _c(bias_table, np.float32)
+    S, H, D = q.shape
+    pr = _c(pairs, np.int32) if pairs is not None else None
+    n = len(pr) if pr is not None else S * H
+    out = np.zeros((n, D), dtype=np.float64)
+    lib.oracle_paged_decode_t5(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(cl), _ptr(tab),
+                               int(tab.shape[1]), int(window), float(scale), int(block_size), S, H, D,
+                               int(bt.shape[1]), int(dtype), _ptr(pr), n, int(nthreads or default_threads()))
     return out if pr is not None else out.reshape(S, H, D)
 
 

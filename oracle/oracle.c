@@ -27,6 +27,10 @@
  *     itself included ("[V1] Add sliding window support to Flex Attention
  *     backend", causal sliding window).  ctx_s = 0 gives a zero row.
  *
+ *   oracle_paged_decode_t5 — the same with A[s,h,j] taken from a T5 relative-
+ *     position table, bias_table[h, min(ctx_s - 1 - j, num_buckets - 1)], in
+ *     place of a materialised A (the in-kernel T5 bias the same page proposes).
+ *
  *   oracle_prefill — for every query row i of a packed variable-length batch
  *     (cu_seqlens), softmax attention over the keys j of the same sequence
  *     that the mask keeps, with r, c the positions inside the sequence:
@@ -159,6 +163,8 @@ struct decode_ctx {
     const void *q, *k_cache, *v_cache;
     const int32_t *block_tables, *context_lens;
     const float *bias;
+    const float *bias_table;    /* [H, num_buckets] relative-position table, or NULL */
+    int num_buckets;
     const int32_t *pairs;       /* optional list of (s, h) pairs */
     int window;
     double scale;
@@ -187,7 +193,16 @@ static void decode_item(long long item, void *p)
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
             dot += load_elem(c->q, qoff + d, c->dtype) * load_elem(c->k_cache, row + d, c->dtype);
-        double a = c->bias ? (double)c->bias[((size_t)s * H + h) * c->bias_row_stride + j] : 0.0;
+        double a = 0.0;
+        if (c->bias) {
+            a = (double)c->bias[((size_t)s * H + h) * c->bias_row_stride + j];
+        } else if (c->bias_table) {
+            /* key j lies (ctx - 1 - j) positions behind the query; distances past
+               the table's last column reuse that column */
+            int d = (ctx - 1) - j;
+            if (d > c->num_buckets - 1) d = c->num_buckets - 1;
+            a = (double)c->bias_table[(size_t)h * c->num_buckets + d];
+        }
         x[t] = c->scale * (dot + a);
         vrow[t] = row;
     }
@@ -205,9 +220,29 @@ void oracle_paged_decode(double *out, const void *q, const void *k_cache, const 
                          int bias_row_stride, int dtype, const int32_t *pairs, int num_pairs,
                          int nthreads)
 {
-    struct decode_ctx c = {out, q, k_cache, v_cache, block_tables, context_lens, bias, pairs,
+    struct decode_ctx c = {out, q, k_cache, v_cache, block_tables, context_lens, bias, NULL, 0, pairs,
                            window, scale, block_size, num_seqs, num_heads, head_dim,
                            max_blocks_per_seq, bias_row_stride, dtype};
+    long long n = pairs ? num_pairs : (long long)num_seqs * num_heads;
+    run_items(decode_item, &c, n, nthreads);
+}
+
+/* Paged decode with the T5 relative-position bias read from its table instead
+ * of a materialised A: A[s,h,j] = bias_table[h, min(ctx_s - 1 - j, num_buckets - 1)]
+ * ("PagedAttention: Support custom attention bias for T5 model (1/2)": the
+ * relative distance is capped, larger distances reuse the last value, and the
+ * page proposes computing the T5 bias in the kernel instead of materialising
+ * it).  Otherwise identical to oracle_paged_decode. */
+void oracle_paged_decode_t5(double *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *context_lens,
+                            const float *bias_table, int num_buckets, int window, double scale,
+                            int block_size, int num_seqs, int num_heads, int head_dim,
+                            int max_blocks_per_seq, int dtype, const int32_t *pairs, int num_pairs,
+                            int nthreads)
+{
+    struct decode_ctx c = {out, q, k_cache, v_cache, block_tables, context_lens, NULL, bias_table,
+                           num_buckets, pairs, window, scale, block_size, num_seqs, num_heads,
+                           head_dim, max_blocks_per_seq, 0, dtype};
     long long n = pairs ? num_pairs : (long long)num_seqs * num_heads;
     run_items(decode_item, &c, n, nthreads);
 }

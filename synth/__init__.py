@@ -124,6 +124,7 @@ class DecodeCase:
     window: int
     scale: float
     device_kv: object = None            # (key, value) torch tensors when drawn on device
+    bias_table: Optional[np.ndarray] = None  # f32 [H, 129] when the bias is T5-style
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -217,6 +218,7 @@ def make_decode_case(name: str, seed: int, dtype: int, num_seqs: int, num_heads:
         device_kv = draw_device_tokens(seed, T, H, D, dtype, device)
     stride = bias_stride if bias_stride is not None else (int(context_lens.max()) if S else 0)
     A = None
+    table = None
     if bias == "gauss":
         A = (rng.standard_normal((S, H, stride), dtype=np.float32) * np.float32(bias_std)).astype(np.float32)
         for s in range(S):
@@ -229,7 +231,7 @@ def make_decode_case(name: str, seed: int, dtype: int, num_seqs: int, num_heads:
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     return DecodeCase(name, dtype, S, H, D, block_size, pool, context_lens, bt, slot, tok_off,
-                      q, key, value, A, window, float(scale), device_kv)
+                      q, key, value, A, window, float(scale), device_kv, table)
 
 
 def draw_device_tokens(seed: int, T: int, H: int, D: int, dtype: int, device: str):

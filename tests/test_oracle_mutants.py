@@ -29,6 +29,7 @@ MUTANTS = {
     "scatter_layout": ("(((size_t)blk * num_heads + h) * block_size + off) * rowb",
                        "(((size_t)blk * block_size + off) * num_heads + h) * rowb"),
     "f16_exponent_bias": ("expo - 25", "expo - 24"),
+    "t5_distance_off_by_one": ("int d = (ctx - 1) - j;", "int d = ctx - j;"),
 }
 
 
@@ -44,6 +45,7 @@ def _pin_suite():
     for w, c in ((-1, 1), (3, 0), (64, 1)):
         yield lambda w=w, c=c: pins.test_prefill_matches_bruteforce(w, c, pins.BF16)
     yield lambda: pins.test_reshape_and_cache_round_trip_and_skip(pins.F16)
+    yield lambda: pins.test_t5_table_decode_equals_materialised_bias(-1, 129)
 
 
 def _build_mutant(name, tmpdir):
@@ -63,7 +65,8 @@ def test_pins_catch_planted_mistake(name, monkeypatch):
     with tempfile.TemporaryDirectory() as d:
         so = _build_mutant(name, d)
         mut = ctypes.CDLL(so)
-        for fn in ("oracle_paged_decode", "oracle_prefill", "oracle_reshape_and_cache", "oracle_widen"):
+        for fn in ("oracle_paged_decode", "oracle_paged_decode_t5", "oracle_prefill", "oracle_reshape_and_cache",
+                   "oracle_widen"):
             getattr(mut, fn).argtypes = getattr(real, fn).argtypes
             getattr(mut, fn).restype = getattr(real, fn).restype
         monkeypatch.setattr(oracle, "_lib", mut)

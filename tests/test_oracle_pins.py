@@ -433,3 +433,34 @@ def test_reshape_and_cache_round_trip_and_skip(dtype):
     kb = kc.transpose(0, 2, 1, 3).reshape(case.num_blocks * 16, -1)
     pb = poison.transpose(0, 2, 1, 3).reshape(case.num_blocks * 16, -1)
     assert kb[~written].tobytes() == pb[~written].tobytes()
+
+
+# ---------------------------------------------------------------------------
+# decode with the T5 bias read from its table
+# ---------------------------------------------------------------------------
+def run_oracle_decode_t5(case, table, **kw):
+    kc, vc = fill_cache_numpy(case)
+    return oracle.paged_decode_t5(case.q, kc, vc, case.block_tables, case.context_lens, table, case.window,
+                                  case.scale, case.block_size, case.dtype, **kw)
+
+
+@pytest.mark.parametrize("window", [-1, 7, 200])
+@pytest.mark.parametrize("buckets", [1, 5, 129])
+def test_t5_table_decode_equals_materialised_bias(window, buckets):
+    """Reading A from the table equals brute force with A materialised by the
+    (fixture-pinned) T5 clamp, for any number of table columns."""
+    case = small_case(dtype=BF16, ctx=(1, 3, 16, 17, 150, 260), H=3, bias="none", window=window)
+    table = np.random.default_rng(9).standard_normal((3, buckets)).astype(np.float32)
+    A = np.zeros((case.num_seqs, 3, 264), dtype=np.float32)
+    for s, c in enumerate(case.context_lens):
+        d = np.minimum((int(c) - 1) - np.arange(int(c)), buckets - 1)
+        A[s, :, :c] = table[:, d]
+    got = run_oracle_decode_t5(case, table)
+    case.bias = A
+    np.testing.assert_allclose(got, brute_decode(case), rtol=1e-12, atol=1e-12)
+
+
+def test_t5_table_constant_rows_equal_no_bias():
+    case = small_case(dtype=F32, ctx=(5, 40, 77), H=2, bias="none")
+    table = np.repeat(np.array([[0.75], [-2.5]], dtype=np.float32), 129, axis=1)
+    np.testing.assert_allclose(run_oracle_decode_t5(case, table), run_oracle_decode(case), rtol=0, atol=1e-13)
