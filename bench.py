@@ -174,14 +174,17 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # decode workloads
 # ---------------------------------------------------------------------------
-def decode_alg_bytes(case, bias_on: bool) -> dict:
+def decode_alg_bytes(case, bias_on: bool, t5_table: bool = False) -> dict:
     """Algorithmic bytes of one decode call: visible K and V rows, bias
-    entries of visible keys, q and out rows, block-table entries, context
-    lengths."""
+    entries of visible keys (or, with the T5 table computed in the kernel,
+    the table), q and out rows, block-table entries, context lengths."""
     n = case.visible().astype(np.int64)
     H, D, elt = case.num_heads, case.head_dim, ELT_BYTES[case.dtype]
     kv = int((2 * H * n * D * elt).sum())
-    bias = int((4 * H * n).sum()) if (bias_on and case.bias is not None) else 0
+    if bias_on and t5_table and case.bias_table is not None:
+        bias = int(case.bias_table.size * 4)
+    else:
+        bias = int((4 * H * n).sum()) if (bias_on and case.bias is not None) else 0
     other = int(case.num_seqs * 2 * H * D * elt + (4 * ((n + case.block_size - 1) // case.block_size)).sum()
                 + 4 * case.num_seqs)
     return {"kv": kv, "bias": bias, "other": other, "total": kv + bias + other}
@@ -253,6 +256,9 @@ class DecodeSide:
         self.bt = torch.from_numpy(np.ascontiguousarray(case.block_tables)).to(device)
         self.cl = torch.from_numpy(case.context_lens).to(device)
         self.bias = torch.from_numpy(case.bias).to(device) if case.bias is not None else None
+        self.table = (torch.from_numpy(case.bias_table).to(device) if getattr(case, "bias_table", None) is not None
+                      else None)
+        self.use_table = False
         self.out = torch.empty((case.num_seqs, H, D), dtype=tdt, device=device)
         self.ws = torch.zeros(pka.paged_attn_decode_workspace_size(case.num_seqs, H, D, case.max_context_len,
                                                                    case.window), dtype=torch.uint8, device=device)
@@ -264,6 +270,7 @@ class DecodeSide:
         for n in ("kc", "vc", "new_k", "new_v", "slots", "q", "bt", "cl", "out"):
             setattr(c, n, getattr(self, n).clone())
         c.bias = self.bias.clone() if self.bias is not None else None
+        c.table = self.table.clone() if self.table is not None else None
         return c
 
     def nbytes(self):
@@ -275,6 +282,10 @@ class DecodeSide:
 
     def decode(self, pka, bias_on=True):
         c = self.case
+        if bias_on and self.use_table and self.table is not None:
+            pka.paged_attn_decode_t5bias(self.out, self.q, self.kc, self.vc, self.bt, self.cl, self.table, c.window,
+                                         c.scale, max_context_len=c.max_context_len, workspace=self.ws)
+            return
         pka.paged_attn_decode(self.out, self.q, self.kc, self.vc, self.bt, self.cl,
                               self.bias if bias_on else None, c.window, c.scale, max_context_len=c.max_context_len,
                               workspace=self.ws)
@@ -298,11 +309,13 @@ def run_decode(args, rank, world, local, peaks):
     big = args.workload in ("t5-large-decode", "long-ctx-decode")
     cases = build_decode_sides(args.workload, device, big, args.num_seqs)
     sides = [DecodeSide(c, pka, device) for c in cases]
+    for sd in sides:
+        sd.use_table = args.t5_table
     if args.no_cpu_baseline:
         for c in cases:               # the token arrays are only needed again by the CPU leg
             c.device_kv = None
         torch.cuda.empty_cache()
-    bytes_on = [decode_alg_bytes(c, True) for c in cases]
+    bytes_on = [decode_alg_bytes(c, True, args.t5_table) for c in cases]
     bytes_off = [decode_alg_bytes(c, False) for c in cases]
     step_bytes = sum(b["total"] for b in bytes_on)
     per_copy = sum(s.nbytes() for s in sides)
@@ -374,7 +387,9 @@ def run_decode(args, rank, world, local, peaks):
     }
     cfg = {"workload": args.workload, "num_seqs": [c.num_seqs for c in cases], "num_heads": cases[0].num_heads,
            "head_dim": cases[0].head_dim, "block_size": 16,
-           "window": [c.window for c in cases], "bias": [c.bias is not None for c in cases],
+           "window": [c.window for c in cases],
+           "bias": [("t5 table in kernel" if args.t5_table and c.bias_table is not None else "materialised")
+                    if c.bias is not None else None for c in cases],
            "l2": f"inputs rotated over {copies} copies ({per_copy * copies / 2**20:.0f} MiB > L2)"
            if copies > 1 else f"inputs {per_copy / 2**20:.0f} MiB > L2", "parallelism": f"replicas x{world}"}
     return {"value": value, "unit": "GB/s", "ms_per_step": ms_step, "dtype": synth.DTYPE_NAMES[cases[0].dtype],
@@ -389,7 +404,11 @@ def decode_e2e(args, sides, pka, step_bytes, world):
     host_in = []
     h2d = 0
     for s in sides:
-        names = ["q", "new_k", "new_v", "slots", "bt", "cl"] + (["bias"] if s.bias is not None else [])
+        names = ["q", "new_k", "new_v", "slots", "bt", "cl"]
+        if s.use_table and s.table is not None:
+            names.append("table")
+        elif s.bias is not None:
+            names.append("bias")
         pairs = []
         for n in names:
             d = getattr(s, n)
@@ -681,6 +700,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--t5-table", action="store_true",
+                    help="T5-bias decode workloads: compute the bias in the kernel from its [H,129] table")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="profiling only: fewer sequences than the named decode workload")
     ap.add_argument("--clock-soak", type=float, default=1.5,

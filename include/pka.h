@@ -151,6 +151,32 @@ PKA_API pka_status pka_paged_attn_decode(void *out, const void *q, const void *k
                                  size_t workspace_bytes, int32_t *status, void *stream);
 
 /*
+ * pka_paged_attn_decode_t5bias — pka_paged_attn_decode with the T5 relative-
+ * position bias computed in the kernel from its table instead of a
+ * materialised A ("PagedAttention: Support custom attention bias for T5 model
+ * (1/2)": the page proposes computing the T5 relative-position bias in the
+ * kernel, and its first review comment caps the relative distance — T5-large
+ * uses 128 — with larger distances reusing the last value):
+ *   A[s,h,j] = bias_table[h, min(ctx_s - 1 - j, num_buckets - 1)]
+ * (key j lies ctx_s - 1 - j positions behind the query).  No bias rows are
+ * read and nothing is padded to max_seq_len.
+ *   bias_table  f32 [num_heads, num_buckets], 4-byte aligned;
+ *               num_heads * num_buckets <= PKA_MAX_BIAS_TABLE
+ *               (PKA_ERR_UNSUPPORTED beyond; it is cached in shared memory)
+ * Every other argument, the workspace and the errors are as for
+ * pka_paged_attn_decode (no attn_bias / bias_row_stride).
+ */
+#define PKA_MAX_BIAS_TABLE 3072
+
+PKA_API pka_status pka_paged_attn_decode_t5bias(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                                const int32_t *block_tables, const int32_t *context_lens,
+                                                const float *bias_table, int num_buckets, int sliding_window,
+                                                float scale, int block_size, int num_seqs, int num_heads,
+                                                int head_dim, int max_blocks_per_seq, int num_blocks,
+                                                int max_context_len, pka_dtype dtype, void *workspace,
+                                                size_t workspace_bytes, int32_t *status, void *stream);
+
+/*
  * pka_paged_attn_decode_noalloc — pka_paged_attn_decode for callers that
  * cannot allocate device memory.  The pages have no counterpart: this is an
  * interface convenience, not part of the method.

@@ -13,6 +13,7 @@ import os
 import threading
 
 __all__ = ["PkaError", "load", "build", "lib_path", "reshape_and_cache", "paged_attn_decode",
+           "paged_attn_decode_t5bias",
            "paged_attn_decode_workspace_size", "swa_prefill", "DecodeWorkspace", "DTYPE_CODE",
            "DEVCHK_BLOCK_ID", "DEVCHK_CONTEXT_LEN", "DEVCHK_SLOT", "DEVCHK_TIMEOUT", "DEVCHK_CU_SEQLENS",
            "EXPORTED_SYMBOLS"]
@@ -25,7 +26,7 @@ DEVCHK_BLOCK_ID, DEVCHK_CONTEXT_LEN, DEVCHK_SLOT, DEVCHK_TIMEOUT, DEVCHK_CU_SEQL
 
 EXPORTED_SYMBOLS = ("pka_status_string", "pka_version", "pka_reshape_and_cache",
                     "pka_paged_attn_decode_workspace_size", "pka_paged_attn_decode",
-                    "pka_paged_attn_decode_noalloc", "pka_swa_prefill")
+                    "pka_paged_attn_decode_noalloc", "pka_paged_attn_decode_t5bias", "pka_swa_prefill")
 
 _lib = None
 _lock = threading.Lock()
@@ -65,6 +66,9 @@ def load():
         lib.pka_paged_attn_decode.argtypes = [P, P, P, P, P, P, P, I, F, I, I, I, I, I, I, I, I, I, P,
                                               ctypes.c_size_t, P, P]
         lib.pka_paged_attn_decode.restype = I
+        lib.pka_paged_attn_decode_t5bias.argtypes = [P, P, P, P, P, P, P, I, I, F, I, I, I, I, I, I, I, I, P,
+                                                     ctypes.c_size_t, P, P]
+        lib.pka_paged_attn_decode_t5bias.restype = I
         lib.pka_swa_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P]
         lib.pka_swa_prefill.restype = I
         _lib = lib
@@ -186,6 +190,38 @@ def paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, attn
                                      _ptr(context_lens), _ptr(attn_bias), int(sliding_window), float(scale), bs, S,
                                      H, D, mbps, stride, nb, int(max_context_len), _dtype_code(q), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
+    return out
+
+
+def paged_attn_decode_t5bias(out, q, k_cache, v_cache, block_tables, context_lens, bias_table, sliding_window=-1,
+                             scale=None, max_context_len=None, workspace=None, status=None, stream=None):
+    """Paged decode with the T5 relative-position bias computed in the kernel:
+    A[s,h,j] = bias_table[h, min(ctx_s - 1 - j, num_buckets - 1)]."""
+    torch = _torch()
+    _need(out, "out", ndim=3); _need(q, "q", ndim=3)
+    _need(k_cache, "k_cache", ndim=4); _need(v_cache, "v_cache", ndim=4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(bias_table, "bias_table", torch.float32, 2)
+    S, H, D = q.shape
+    nb, _, bs, _ = k_cache.shape
+    mbps = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = mbps * bs
+    if scale is None:
+        scale = D ** -0.5
+    lib = load()
+    need = int(lib.pka_paged_attn_decode_workspace_size(S, H, D, int(max_context_len), int(sliding_window)))
+    if workspace is None:
+        dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
+        workspace = _default_ws.setdefault(dev, DecodeWorkspace(q.device)).get(need)
+    _check("pka_paged_attn_decode_t5bias",
+           lib.pka_paged_attn_decode_t5bias(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                            _ptr(context_lens), _ptr(bias_table), bias_table.shape[1],
+                                            int(sliding_window), float(scale), bs, S, H, D, mbps, nb,
+                                            int(max_context_len), _dtype_code(q), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(), _ptr(status),
+                                            _stream(stream)))
     return out
 
 

@@ -48,6 +48,7 @@ namespace {
 
 constexpr int BS = 16;                   // tokens per cache block (the only size built)
 constexpr int MAX_SEQS_PER_LAUNCH = 1024;
+constexpr int MAX_TABLE_FLOATS = PKA_MAX_BIAS_TABLE;   // T5 table cached in shared memory
 
 template <typename T, int D> struct Tr {
     static constexpr int ELT = sizeof(T);
@@ -74,6 +75,7 @@ struct Params {
     const unsigned char *q, *k_cache, *v_cache;
     const int32_t *block_tables, *context_lens;
     const float *bias;
+    const float *bias_table;     // [H, num_buckets] T5 relative-position table, or NULL
     int32_t *status;
     unsigned *counters;
     float2 *ws_ml;
@@ -81,6 +83,7 @@ struct Params {
     float scale_log2;
     int window, seq_base, num_seqs, H, mbps, num_blocks, max_ctx, part_blocks, max_parts;
     long long bias_stride;
+    int num_buckets;
 };
 
 struct Unit {
@@ -169,6 +172,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)NW * NSTAGE * R::STAGE) + warp * NSTAGE;
     int *cum = reinterpret_cast<int *>(smem + (size_t)NW * NSTAGE * R::STAGE + NW * NSTAGE * 8);
     int *ctxs = cum + P.num_seqs + 1;
+    float *table_sm = reinterpret_cast<float *>(ctxs + P.num_seqs);
 
     // ---- per-sequence partition counts -> prefix sums (whole CTA) ----------
     for (int s = threadIdx.x; s < P.num_seqs; s += blockDim.x) {
@@ -186,6 +190,8 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
         }
         cum[s + 1] = npart * P.H;
     }
+    if (P.bias_table)
+        for (int i = threadIdx.x; i < P.H * P.num_buckets; i += blockDim.x) table_sm[i] = __ldg(P.bias_table + i);
     if (lane == 0)
         for (int i = 0; i < NSTAGE; ++i) mbar_init(smem_u32(&bars[i]), 32);
     fence_barrier_init();
@@ -214,6 +220,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
     if (gw >= total_units) return;                    // no CTA-wide sync after this point
 
     const bool has_bias = P.bias != nullptr;
+    const bool has_table = P.bias_table != nullptr;
 
     // ---- producer state (issue side) ---------------------------------------
     int pk = 0;                                        // unit ordinal of the issue side
@@ -305,7 +312,14 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
             float d = DT::dot(qreg, stp + R::K_OFF + key * R::ROW, q_first, q_rot);
             d += __shfl_xor_sync(kFull, d, 1);
             const int j = (cu.b0 + cb) * BS + key;
-            const float bv = has_bias ? reinterpret_cast<const float *>(stp + R::B_OFF)[key] : 0.f;
+            float bv = 0.f;
+            if (has_bias) {
+                bv = reinterpret_cast<const float *>(stp + R::B_OFF)[key];
+            } else if (has_table) {
+                // T5 relative position: distance ctx-1-j, capped at the last column
+                const int dist = min(max(cu.ctx - 1 - j, 0), P.num_buckets - 1);
+                bv = table_sm[cu.h * P.num_buckets + dist];
+            }
             const float x = (j >= cu.start && j < cu.ctx) ? (d + bv) * P.scale_log2 : -INFINITY;
             float mb = fmaxf(x, __shfl_xor_sync(kFull, x, 2));
             mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 4));
@@ -418,7 +432,8 @@ template <typename T, int D, int NSTAGE, int NW> struct Config {
     using R = Tr<T, D>;
     static size_t smem_bytes(int nseq)
     {
-        return (size_t)NW * NSTAGE * R::STAGE + (size_t)NW * NSTAGE * 8 + (size_t)(2 * nseq + 1) * 4;
+        return (size_t)NW * NSTAGE * R::STAGE + (size_t)NW * NSTAGE * 8 + (size_t)(2 * nseq + 1) * 4 +
+               (size_t)MAX_TABLE_FLOATS * 4;
     }
     static cudaError_t launch(const Params &P, int sms, cudaStream_t stream)
     {
@@ -538,6 +553,8 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &size_plan
     P.part_blocks = plan.part_blocks;
     P.max_parts = plan.max_parts;
     P.bias_stride = a.bias_row_stride;
+    P.bias_table = a.bias_table;
+    P.num_buckets = a.num_buckets;
     for (int base = 0; base < a.num_seqs; base += MAX_SEQS_PER_LAUNCH) {
         P.seq_base = base;
         P.num_seqs = std::min(MAX_SEQS_PER_LAUNCH, a.num_seqs - base);

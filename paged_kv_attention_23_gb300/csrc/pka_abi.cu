@@ -93,6 +93,8 @@ pka_status pka_paged_attn_decode(void *out, const void *q, const void *k_cache, 
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.bias = attn_bias;
+    a.bias_table = nullptr;
+    a.num_buckets = 0;
     a.status = status;
     a.scale = scale;
     a.window = sliding_window;
@@ -103,6 +105,50 @@ pka_status pka_paged_attn_decode(void *out, const void *q, const void *k_cache, 
     a.num_blocks = num_blocks;
     a.max_context_len = max_context_len;
     a.bias_row_stride = attn_bias ? bias_row_stride : 0;
+    a.dtype = dtype;
+    a.workspace = workspace;
+    return from_cuda(pka::launch_paged_decode(a, plan, static_cast<cudaStream_t>(stream)));
+}
+
+pka_status pka_paged_attn_decode_t5bias(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                        const int32_t *block_tables, const int32_t *context_lens,
+                                        const float *bias_table, int num_buckets, int sliding_window, float scale,
+                                        int block_size, int num_seqs, int num_heads, int head_dim,
+                                        int max_blocks_per_seq, int num_blocks, int max_context_len, pka_dtype dtype,
+                                        void *workspace, size_t workspace_bytes, int32_t *status, void *stream)
+{
+    if (!bias_table || num_buckets < 1 || num_heads < 1 || (long long)num_heads * num_buckets > PKA_MAX_BIAS_TABLE)
+        return num_buckets >= 1 && num_heads >= 1 && bias_table ? PKA_ERR_UNSUPPORTED : PKA_ERR_INVALID_ARG;
+    if (!aligned(bias_table, 4)) return PKA_ERR_INVALID_ARG;
+    // every other argument is checked exactly as for the materialised-bias call
+    const pka_status probe = pka_paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, nullptr,
+                                                   sliding_window, scale, block_size, num_seqs, num_heads, head_dim,
+                                                   max_blocks_per_seq, 0, num_blocks, max_context_len, dtype,
+                                                   nullptr, 0, status, stream);
+    if (probe != PKA_ERR_WORKSPACE) return probe;
+    const pka::DecodePlan plan = pka::decode_plan(max_context_len, sliding_window, block_size);
+    const size_t need = pka::decode_workspace_bytes(num_seqs, num_heads, head_dim, plan);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PKA_ERR_WORKSPACE;
+    pka::DecodeArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.bias = nullptr;
+    a.bias_table = bias_table;
+    a.num_buckets = num_buckets;
+    a.status = status;
+    a.scale = scale;
+    a.window = sliding_window;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.head_dim = head_dim;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.max_context_len = max_context_len;
+    a.bias_row_stride = 0;
     a.dtype = dtype;
     a.workspace = workspace;
     return from_cuda(pka::launch_paged_decode(a, plan, static_cast<cudaStream_t>(stream)));

@@ -34,6 +34,8 @@ struct DecodeArgs {
     const void *q, *k_cache, *v_cache;
     const int32_t *block_tables, *context_lens;
     const float *bias;
+    const float *bias_table;   // T5 relative-position table [H, num_buckets] or NULL
+    int num_buckets;
     int32_t *status;
     float scale;
     int window, num_seqs, num_heads, head_dim, max_blocks_per_seq, num_blocks, max_context_len;

@@ -63,6 +63,17 @@ class GpuDecode:
         self.out = torch.empty((case.num_seqs, H, D), dtype=tdt, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
+    def run_t5(self, workspace=None):
+        """Decode with the bias computed in the kernel from the case's T5 table."""
+        import torch
+        c = self.case
+        tab = torch.from_numpy(c.bias_table).to(self.q.device)
+        self.pka.paged_attn_decode_t5bias(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+                                          self.context_lens, tab, c.window, c.scale,
+                                          max_context_len=c.max_context_len, workspace=workspace,
+                                          status=self.status)
+        return self.out
+
     def run(self, bias=True, window=None, workspace=None):
         c = self.case
         self.pka.paged_attn_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
@@ -70,6 +81,17 @@ class GpuDecode:
                                    c.window if window is None else window, c.scale,
                                    max_context_len=c.max_context_len, workspace=workspace, status=self.status)
         return self.out
+
+
+def oracle_decode_t5(case, pairs=None):
+    import oracle
+    H, D, bs = case.num_heads, case.head_dim, case.block_size
+    shape = (case.num_blocks, H, bs, D)
+    kc = np.zeros(shape, dtype=case.key.dtype)
+    vc = np.zeros(shape, dtype=case.key.dtype)
+    oracle.reshape_and_cache(kc, vc, case.key, case.value, case.slot_mapping, bs)
+    return oracle.paged_decode_t5(case.q, kc, vc, case.block_tables, case.context_lens, case.bias_table,
+                                  case.window, case.scale, bs, case.dtype, pairs=pairs)
 
 
 def oracle_decode(case, bias=True, window=None, pairs=None):

@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import TOL, GpuDecode, max_err, oracle_decode, to_dev, to_f64, to_host_storage, torch_dtype
+from helpers import TOL, GpuDecode, max_err, oracle_decode, oracle_decode_t5, to_dev, to_f64, to_host_storage, torch_dtype
 from synth import BF16, F16, F32
 
 pytestmark = pytest.mark.gpu
@@ -276,3 +276,38 @@ def test_api_rejects_bad_arguments(cuda_lib):
     small = torch.zeros(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(cuda_lib.PkaError):
         g.run(workspace=small)
+
+
+# ---------------------------------------------------------------------------
+# T5 bias computed in the kernel from its table
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("n", [2, 3])
+def test_t5_table_decode_parity(cuda_lib, n):
+    """The T5-shaped workloads with the bias read from the [H, 129] table
+    inside the kernel: matches the oracle, and the materialised-bias kernel."""
+    case = synth.decode_workload(n)
+    g = GpuDecode(case, cuda_lib)
+    got = to_f64(g.run_t5(), case.dtype).copy()
+    _check(got, oracle_decode_t5(case), case.dtype, f"t5 table workload {n}")
+    mat = to_f64(g.run(), case.dtype)
+    assert max_err(got, mat) <= TOL[case.dtype]
+    assert int(g.status.item()) == 0
+
+
+@pytest.mark.parametrize("window", [-1, 5, 40])
+@pytest.mark.parametrize("buckets", [1, 17, 129])
+def test_t5_table_decode_edges(cuda_lib, window, buckets):
+    case = synth.make_decode_case("t5edge", 60 + buckets, F16, len(EDGE_CTX), 4, 128,
+                                  context_lens=np.array(EDGE_CTX), pool_blocks=120, window=window, scale=0.2)
+    case.bias_table = np.random.default_rng(buckets).standard_normal((4, buckets)).astype(np.float32)
+    g = GpuDecode(case, cuda_lib)
+    _check(to_f64(g.run_t5(), F16), oracle_decode_t5(case), F16, "t5 edges")
+
+
+def test_t5_table_too_large_is_unsupported(cuda_lib):
+    import torch
+    case = synth.decode_workload(1)
+    g = GpuDecode(case, cuda_lib)
+    case.bias_table = np.zeros((2, 4000), dtype=np.float32)       # 8000 floats > the shared-memory cache
+    with pytest.raises(cuda_lib.PkaError):
+        g.run_t5()
