@@ -20,6 +20,9 @@ Functions and the passages they follow:
 * ``prefill`` — the same softmax attention for every row of a packed varlen
   batch, mask = full / causal / bidirectional band |i-j| < W / causal band
   ("[V1] Add sliding window support to Flex Attention backend").
+* ``prefill_chunked`` — keys restricted to the query's own chunk of C
+  positions, bidirectional or causal (the chunked local attention layers the
+  same page discusses).
 * ``reshape_and_cache`` — the plain scatter of new K/V rows into cache blocks
   (the cross-attention KV caching step named in "Add Encoder-decoder model
   support and T5 Model support").
@@ -67,6 +70,9 @@ def _load():
         lib.oracle_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_double, I, P,
                                        ctypes.c_longlong, I]
         lib.oracle_prefill.restype = None
+        lib.oracle_prefill_chunked.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_double, I, P,
+                                               ctypes.c_longlong, I]
+        lib.oracle_prefill_chunked.restype = None
         lib.oracle_reshape_and_cache.argtypes = [P, P, P, P, P, ctypes.c_longlong, I, I, I, I]
         lib.oracle_reshape_and_cache.restype = None
         lib.oracle_widen.argtypes = [P, ctypes.c_longlong, I]
@@ -144,6 +150,21 @@ def prefill(q, k, v, cu_seqlens, window, causal, scale, dtype, rows=None, nthrea
     out = np.zeros((nr, H, D), dtype=np.float64)
     lib.oracle_prefill(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, H, D, int(window),
                        int(causal), float(scale), int(dtype), _ptr(rr), nr, int(nthreads or default_threads()))
+    return out
+
+
+def prefill_chunked(q, k, v, cu_seqlens, chunk, causal, scale, dtype, rows=None, nthreads=None) -> np.ndarray:
+    """Chunked local attention prefill in double: [T or len(rows), H, D]."""
+    lib = _load()
+    q = _c(q); k = _c(k); v = _c(v)
+    cu = _c(cu_seqlens, np.int32)
+    T, H, D = q.shape
+    rr = _c(rows, np.int64) if rows is not None else None
+    nr = len(rr) if rr is not None else int(cu[-1])
+    out = np.zeros((nr, H, D), dtype=np.float64)
+    lib.oracle_prefill_chunked(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, H, D, int(chunk),
+                               int(causal), float(scale), int(dtype), _ptr(rr), nr,
+                               int(nthreads or default_threads()))
     return out
 
 

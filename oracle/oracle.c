@@ -41,6 +41,9 @@
  *     ("[V1] Add sliding window support to Flex Attention backend":
  *     bidirectional attention with a sliding window for encoder-only models.)
  *
+ *   oracle_prefill_chunked — the same with keys restricted to the query's
+ *     own chunk of `chunk` positions (chunked local attention, same page).
+ *
  *   oracle_reshape_and_cache — the plain scatter of token rows into cache
  *     blocks, cache[slot / bs, h, slot % bs, :] = key[t, h, :]; slot < 0 skips
  *     the token.  Byte copies, so the result is exact.
@@ -256,11 +259,13 @@ struct prefill_ctx {
     const int64_t *rows;        /* optional list of token rows */
     int num_seqs, num_heads, head_dim, window, causal, dtype;
     double scale;
+    int chunk;                  /* > 0: keys only from the query's own chunk of this many positions */
 };
 
-static int mask_keeps(int r, int c, int window, int causal)
+static int mask_keeps(int r, int c, int window, int causal, int chunk)
 {
     if (causal && c > r) return 0;
+    if (chunk > 0 && r / chunk != c / chunk) return 0;
     if (window > 0) {
         int d = r - c;
         if (d < 0) d = -d;
@@ -287,7 +292,7 @@ static void prefill_item(long long item, void *p)
     int n = 0;
     const size_t qoff = ((size_t)i * H + h) * D;
     for (int col = 0; col < L; ++col) {
-        if (!mask_keeps(r, col, c->window, c->causal)) continue;
+        if (!mask_keeps(r, col, c->window, c->causal, c->chunk)) continue;
         const size_t row = ((size_t)(s0 + col) * H + h) * D;
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
@@ -309,7 +314,23 @@ void oracle_prefill(double *out, const void *q, const void *k, const void *v,
                     const int64_t *rows, long long num_rows, int nthreads)
 {
     struct prefill_ctx c = {out, q, k, v, cu_seqlens, rows, num_seqs, num_heads, head_dim,
-                            window, causal, dtype, scale};
+                            window, causal, dtype, scale, 0};
+    long long nr = rows ? num_rows : (long long)cu_seqlens[num_seqs];
+    run_items(prefill_item, &c, nr * num_heads, nthreads);
+}
+
+/* Chunked local attention: a query at position r of its sequence sees only
+ * the keys of its own chunk, positions [r / chunk * chunk, r / chunk * chunk
+ * + chunk) (causal: and c <= r) — the block-diagonal "chunked local
+ * attention" layers that "[V1] Add sliding window support to Flex Attention
+ * backend" discusses beside the sliding window. */
+void oracle_prefill_chunked(double *out, const void *q, const void *k, const void *v,
+                            const int32_t *cu_seqlens, int num_seqs, int num_heads, int head_dim,
+                            int chunk, int causal, double scale, int dtype,
+                            const int64_t *rows, long long num_rows, int nthreads)
+{
+    struct prefill_ctx c = {out, q, k, v, cu_seqlens, rows, num_seqs, num_heads, head_dim,
+                            -1, causal, dtype, scale, chunk};
     long long nr = rows ? num_rows : (long long)cu_seqlens[num_seqs];
     run_items(prefill_item, &c, nr * num_heads, nthreads);
 }

@@ -30,6 +30,8 @@ MUTANTS = {
                        "(((size_t)blk * block_size + off) * num_heads + h) * rowb"),
     "f16_exponent_bias": ("expo - 25", "expo - 24"),
     "t5_distance_off_by_one": ("int d = (ctx - 1) - j;", "int d = ctx - j;"),
+    "chunk_boundary_shifted": ("if (chunk > 0 && r / chunk != c / chunk) return 0;",
+                               "if (chunk > 0 && (r + 1) / chunk != (c + 1) / chunk) return 0;"),
 }
 
 
@@ -46,6 +48,7 @@ def _pin_suite():
         yield lambda w=w, c=c: pins.test_prefill_matches_bruteforce(w, c, pins.BF16)
     yield lambda: pins.test_reshape_and_cache_round_trip_and_skip(pins.F16)
     yield lambda: pins.test_t5_table_decode_equals_materialised_bias(-1, 129)
+    yield pins.test_chunked_matches_bruteforce
 
 
 def _build_mutant(name, tmpdir):
@@ -65,8 +68,8 @@ def test_pins_catch_planted_mistake(name, monkeypatch):
     with tempfile.TemporaryDirectory() as d:
         so = _build_mutant(name, d)
         mut = ctypes.CDLL(so)
-        for fn in ("oracle_paged_decode", "oracle_paged_decode_t5", "oracle_prefill", "oracle_reshape_and_cache",
-                   "oracle_widen"):
+        for fn in ("oracle_paged_decode", "oracle_paged_decode_t5", "oracle_prefill", "oracle_prefill_chunked",
+                   "oracle_reshape_and_cache", "oracle_widen"):
             getattr(mut, fn).argtypes = getattr(real, fn).argtypes
             getattr(mut, fn).restype = getattr(real, fn).restype
         monkeypatch.setattr(oracle, "_lib", mut)

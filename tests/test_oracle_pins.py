@@ -464,3 +464,48 @@ def test_t5_table_constant_rows_equal_no_bias():
     case = small_case(dtype=F32, ctx=(5, 40, 77), H=2, bias="none")
     table = np.repeat(np.array([[0.75], [-2.5]], dtype=np.float32), 129, axis=1)
     np.testing.assert_allclose(run_oracle_decode_t5(case, table), run_oracle_decode(case), rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# chunked local attention prefill
+# ---------------------------------------------------------------------------
+def _split_into_chunks(cu, C):
+    """cu_seqlens of the same tokens cut into chunks of C positions."""
+    out = [0]
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        for s in range(a, e, C):
+            out.append(min(s + C, e))
+    return np.array(out, dtype=np.int32)
+
+
+@pytest.mark.parametrize("C", [1, 3, 16, 64, 1000])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_chunked_equals_full_attention_over_the_chunks(C, causal):
+    """Chunked attention over a sequence is exactly (causal or full) attention
+    over the packed batch of its chunks."""
+    case = synth.make_prefill_case("pin", 18, [1, 7, 70, 130], 2, 64, -1, causal, BF16)
+    got = oracle.prefill_chunked(case.q, case.k, case.v, case.cu_seqlens, C, causal, case.scale, BF16)
+    ref = oracle.prefill(case.q, case.k, case.v, _split_into_chunks(case.cu_seqlens, C), -1, causal,
+                         case.scale, BF16)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_chunked_matches_bruteforce():
+    case = synth.make_prefill_case("pin", 19, [5, 40, 100], 2, 64, -1, 0, BF16)
+    q = synth.decode_to_f32(case.q, BF16).astype(np.float64)
+    k = synth.decode_to_f32(case.k, BF16).astype(np.float64)
+    v = synth.decode_to_f32(case.v, BF16).astype(np.float64)
+    C = 16
+    ref = np.zeros_like(q)
+    cu = case.cu_seqlens
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        r = np.arange(e - a)
+        keep = (r[:, None] // C) == (r[None, :] // C)
+        lg = np.einsum("ihd,jhd->hij", q[a:e], k[a:e]) * case.scale
+        lg = np.where(keep[None], lg, -np.inf)
+        w = np.exp(lg - lg.max(axis=2, keepdims=True)); w /= w.sum(axis=2, keepdims=True)
+        ref[a:e] = np.einsum("hij,jhd->ihd", w, v[a:e])
+    got = oracle.prefill_chunked(case.q, case.k, case.v, cu, C, 0, case.scale, BF16)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
