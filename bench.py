@@ -17,6 +17,8 @@ batch of seeded synthetic input, already resident in HBM:
         window 4096, bias [512,16,8192] N(0,0.25) NaN-padded.
   encoder-prefill    32 packed sequences U[128,8192], 12 heads x 64 bf16,
         three layers: full, window 64, window 64 (bidirectional).
+  chunked-prefill    the same sequences, one chunked-local layer (chunks of
+        1024 positions, causal within the chunk).
 
 metric/unit: decode workloads report algorithmic KV+bias bytes per second
 (GB/s); the prefill workload reports TFLOP/s (4*D per kept (query, key) pair
@@ -456,7 +458,10 @@ def run_prefill(args, rank, world, local, peaks):
     pka.load()
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    layers = [synth.prefill_workload(l, device=device) for l in range(3)]
+    if args.workload == "chunked-prefill":
+        layers = [synth.chunked_prefill_workload(device=device)]
+    else:
+        layers = [synth.prefill_workload(l, device=device) for l in range(3)]
     flops = [prefill_flops(c) for c in layers]
     cu = torch.from_numpy(layers[0].cu_seqlens).to(device)
     outs = [torch.empty_like(c.device_qkv[0]) for c in layers]
@@ -466,7 +471,10 @@ def run_prefill(args, rank, world, local, peaks):
             q, kk, v = c.device_qkv
             if events is not None:
                 events[j][0][k].record()
-            pka.swa_prefill(outs[j], q, kk, v, cu, c.max_seqlen, c.window, c.causal, c.scale)
+            if c.chunk > 0:
+                pka.chunked_prefill(outs[j], q, kk, v, cu, c.max_seqlen, c.chunk, c.causal, c.scale)
+            else:
+                pka.swa_prefill(outs[j], q, kk, v, cu, c.max_seqlen, c.window, c.causal, c.scale)
             if events is not None:
                 events[j][1][k].record()
 
@@ -488,7 +496,7 @@ def run_prefill(args, rank, world, local, peaks):
     torch.cuda.synchronize(); barrier(world)
     clk = clocks.stop()
     ms_step = max_over_ranks(t0.elapsed_time(t1), world) / K
-    launch_ms = per_launch_ms(lambda ev: [step(ev, k) for k in range(K)], 3, K)
+    launch_ms = per_launch_ms(lambda ev: [step(ev, k) for k in range(K)], len(layers), K)
     value = sum(flops) * world / (ms_step * 1e-3) / 1e12
     ach = flops[0] / (launch_ms[0] * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
@@ -505,10 +513,12 @@ def run_prefill(args, rank, world, local, peaks):
              "flops_per_step": sum(flops)}
     e2e = prefill_e2e(args, layers, pka, cu, outs, sum(flops), world) if not args.no_e2e else None
     cfg = {"workload": args.workload, "num_seqs": layers[0].num_seqs, "num_tokens": layers[0].num_tokens,
-           "num_heads": 12, "head_dim": 64, "windows": [c.window for c in layers], "causal": 0,
+           "num_heads": 12, "head_dim": 64, "windows": [c.window for c in layers],
+           "chunks": [c.chunk for c in layers], "causal": layers[0].causal,
            "l2": f"q/k/v {qkv_bytes[0] * 3 / 4 / 2**20:.0f} MiB per layer > L2", "parallelism": f"replicas x{world}"}
     return {"value": value, "unit": "TFLOP/s", "ms_per_step": ms_step, "dtype": "bf16", "config": cfg,
-            "roofline": roof, "e2e": e2e, "clocks": clk, "gpu_launches": 3 * K, "extra": extra, "cases": layers}
+            "roofline": roof, "e2e": e2e, "clocks": clk, "gpu_launches": len(layers) * K, "extra": extra,
+            "cases": layers}
 
 
 def prefill_e2e(args, layers, pka, cu, outs, flops, world):
@@ -623,11 +633,16 @@ def oracle_prefill_sample(layers, budget_s: float, seed: int = 0):
         for c, (q, k, v) in zip(layers, host):
             rows = np.sort(rng.choice(c.num_tokens, size=64, replace=False)).astype(np.int64)
             t = time.time()
-            oracle.prefill(q, k, v, c.cu_seqlens, c.window, c.causal, c.scale, BF16, rows=rows, nthreads=threads)
+            if c.chunk > 0:
+                oracle.prefill_chunked(q, k, v, c.cu_seqlens, c.chunk, c.causal, c.scale, BF16, rows=rows,
+                                       nthreads=threads)
+            else:
+                oracle.prefill(q, k, v, c.cu_seqlens, c.window, c.causal, c.scale, BF16, rows=rows,
+                               nthreads=threads)
             secs += time.time() - t
             flops += 4 * c.head_dim * c.num_heads * _kept_keys(c, rows)
             nrows += len(rows)
-    desc = f"{nrows} query rows drawn at random over the 3 layers (all heads), fp64 oracle, {secs:.1f} s"
+    desc = f"{nrows} query rows drawn at random over the {len(layers)} layer(s) (all heads), fp64 oracle, {secs:.1f} s"
     return flops, secs, threads, desc
 
 
@@ -637,7 +652,10 @@ def _kept_keys(c, rows):
     for i in rows:
         b = int(np.searchsorted(cu, i, side="right") - 1)
         L = int(cu[b + 1] - cu[b]); r = int(i - cu[b])
-        if c.window > 0:
+        if c.chunk > 0:
+            lo = r // c.chunk * c.chunk
+            hi = min(L - 1, lo + c.chunk - 1)
+        elif c.window > 0:
             lo, hi = max(0, r - c.window + 1), min(L - 1, r + c.window - 1)
         else:
             lo, hi = 0, L - 1
@@ -649,7 +667,7 @@ def _kept_keys(c, rows):
 
 def cpu_baseline(res, args):
     budget = args.cpu_seconds
-    if args.workload == "encoder-prefill":
+    if args.workload in ("encoder-prefill", "chunked-prefill"):
         f, s, th, desc = oracle_prefill_sample(res["cases"], budget)
         return {"value": round(f / s / 1e12, 6), "unit": "TFLOP/s", "cores": th, "kind": "oracle", "sample": desc}
     b, s, th, desc = oracle_decode_sample(res["cases"], budget)
@@ -661,8 +679,9 @@ def run_reference(args, rank, world):
     bounded sample per step."""
     if rank != 0:
         return None
-    if args.workload == "encoder-prefill":
-        layers = [synth.prefill_workload(l) for l in range(3)]
+    if args.workload in ("encoder-prefill", "chunked-prefill"):
+        layers = ([synth.chunked_prefill_workload()] if args.workload == "chunked-prefill"
+                  else [synth.prefill_workload(l) for l in range(3)])
         per = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
         oracle_prefill_sample(layers, 0.5)
         f, s, th, desc = oracle_prefill_sample(layers, per * args.steps)
@@ -695,7 +714,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
     ap.add_argument("--workload", default="t5-small-decode",
-                    choices=sorted(DECODE_WORKLOADS) + ["encoder-prefill"])
+                    choices=sorted(DECODE_WORKLOADS) + ["encoder-prefill", "chunked-prefill"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -715,7 +734,7 @@ def main():
             print(json.dumps(line), flush=True)
         return
     peaks = measured_peaks()
-    if args.workload == "encoder-prefill":
+    if args.workload in ("encoder-prefill", "chunked-prefill"):
         res = run_prefill(args, rank, world, local, peaks)
     else:
         res = run_decode(args, rank, world, local, peaks)

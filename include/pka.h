@@ -241,6 +241,21 @@ PKA_API pka_status pka_swa_prefill(void *out, const void *q, const void *k, cons
                            int num_heads, int head_dim, int window, int causal, float scale,
                            pka_dtype dtype, int32_t *status, void *stream);
 
+/*
+ * pka_chunked_prefill — chunked local attention over a packed variable-length
+ * batch: the block-diagonal "chunked local attention" layers that "[V1] Add
+ * sliding window support to Flex Attention backend" discusses beside the
+ * sliding window (Llama4: full and chunked-local layers).  A token at
+ * position r of its sequence attends to the keys of its own chunk,
+ *   c in [r / chunk * chunk, min(L, r / chunk * chunk + chunk))   (causal: and c <= r),
+ * with the same softmax, layout, tensor-core kernel, key-tile skipping and
+ * errors as pka_swa_prefill (no window).  chunk >= 1.
+ */
+PKA_API pka_status pka_chunked_prefill(void *out, const void *q, const void *k, const void *v,
+                                       const int32_t *cu_seqlens, int num_seqs, int num_tokens, int max_seqlen,
+                                       int num_heads, int head_dim, int chunk, int causal, float scale,
+                                       pka_dtype dtype, int32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

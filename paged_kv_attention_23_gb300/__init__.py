@@ -13,7 +13,7 @@ import os
 import threading
 
 __all__ = ["PkaError", "load", "build", "lib_path", "reshape_and_cache", "paged_attn_decode",
-           "paged_attn_decode_t5bias",
+           "paged_attn_decode_t5bias", "chunked_prefill",
            "paged_attn_decode_workspace_size", "swa_prefill", "DecodeWorkspace", "DTYPE_CODE",
            "DEVCHK_BLOCK_ID", "DEVCHK_CONTEXT_LEN", "DEVCHK_SLOT", "DEVCHK_TIMEOUT", "DEVCHK_CU_SEQLENS",
            "EXPORTED_SYMBOLS"]
@@ -26,7 +26,8 @@ DEVCHK_BLOCK_ID, DEVCHK_CONTEXT_LEN, DEVCHK_SLOT, DEVCHK_TIMEOUT, DEVCHK_CU_SEQL
 
 EXPORTED_SYMBOLS = ("pka_status_string", "pka_version", "pka_reshape_and_cache",
                     "pka_paged_attn_decode_workspace_size", "pka_paged_attn_decode",
-                    "pka_paged_attn_decode_noalloc", "pka_paged_attn_decode_t5bias", "pka_swa_prefill")
+                    "pka_paged_attn_decode_noalloc", "pka_paged_attn_decode_t5bias", "pka_swa_prefill",
+                    "pka_chunked_prefill")
 
 _lib = None
 _lock = threading.Lock()
@@ -71,6 +72,8 @@ def load():
         lib.pka_paged_attn_decode_t5bias.restype = I
         lib.pka_swa_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P]
         lib.pka_swa_prefill.restype = I
+        lib.pka_chunked_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P]
+        lib.pka_chunked_prefill.restype = I
         _lib = lib
         return lib
 
@@ -240,4 +243,22 @@ def swa_prefill(out, q, k, v, cu_seqlens, max_seqlen, window=-1, causal=0, scale
            lib.pka_swa_prefill(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T,
                                int(max_seqlen), H, D, int(window), int(causal), float(scale), _dtype_code(q),
                                _ptr(status), _stream(stream)))
+    return out
+
+
+def chunked_prefill(out, q, k, v, cu_seqlens, max_seqlen, chunk, causal=1, scale=None, status=None, stream=None):
+    """Packed varlen prefill with chunked local attention: each token sees the
+    keys of its own chunk of ``chunk`` positions (causal: up to itself)."""
+    torch = _torch()
+    for n, t in (("out", out), ("q", q), ("k", k), ("v", v)):
+        _need(t, n, ndim=3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, H, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    lib = load()
+    _check("pka_chunked_prefill",
+           lib.pka_chunked_prefill(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+                                   T, int(max_seqlen), H, D, int(chunk), int(causal), float(scale), _dtype_code(q),
+                                   _ptr(status), _stream(stream)))
     return out

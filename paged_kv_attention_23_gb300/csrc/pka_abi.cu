@@ -184,6 +184,42 @@ pka_status pka_swa_prefill(void *out, const void *q, const void *k, const void *
     a.head_dim = head_dim;
     a.window = window;
     a.causal = causal;
+    a.chunk = 0;
+    return from_cuda(pka::launch_swa_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
+pka_status pka_chunked_prefill(void *out, const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                               int num_seqs, int num_tokens, int max_seqlen, int num_heads, int head_dim, int chunk,
+                               int causal, float scale, pka_dtype dtype, int32_t *status, void *stream)
+{
+    if (chunk < 1) return PKA_ERR_INVALID_ARG;
+    // every other argument is checked as for the sliding-window prefill
+    if (num_seqs < 0 || num_tokens < 0 || max_seqlen < 0 || num_heads < 1 || !std::isfinite(scale) ||
+        (causal != 0 && causal != 1) || !dtype_ok(dtype))
+        return PKA_ERR_INVALID_ARG;
+    if (dtype != PKA_BF16) return PKA_ERR_UNSUPPORTED;
+    if (head_dim != 64) return PKA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || num_tokens == 0) return PKA_OK;
+    if (!out || !q || !k || !v || !cu_seqlens) return PKA_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(cu_seqlens, 4) ||
+        !aligned(status, 4))
+        return PKA_ERR_INVALID_ARG;
+    pka::PrefillArgs a;
+    a.out = out;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.cu_seqlens = cu_seqlens;
+    a.status = status;
+    a.scale = scale;
+    a.num_seqs = num_seqs;
+    a.num_tokens = num_tokens;
+    a.max_seqlen = max_seqlen;
+    a.num_heads = num_heads;
+    a.head_dim = head_dim;
+    a.window = -1;
+    a.causal = causal;
+    a.chunk = chunk;
     return from_cuda(pka::launch_swa_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 

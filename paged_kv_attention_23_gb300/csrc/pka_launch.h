@@ -54,6 +54,7 @@ struct PrefillArgs {
     int32_t *status;
     float scale;
     int num_seqs, num_tokens, max_seqlen, num_heads, head_dim, window, causal;
+    int chunk;   // > 0: chunked local attention (window must be -1)
 };
 
 cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream);

@@ -7,6 +7,7 @@
 // models, layers alternating full / window): for query position r of a
 // sequence of length L, the keys c with
 //   window <= 0: all c (causal: c <= r);  window > 0: |r - c| < W (causal: 0 <= r - c < W)
+//   chunk > 0 (chunked local attention, same page): c in r's chunk of C positions (causal: c <= r)
 //   O_r = sum_c softmax_c(scale * q_r . k_c) v_c
 // Only key tiles that intersect the band are visited ("visit only
 // intra-window blocks", same page).
@@ -79,7 +80,7 @@ struct Params {
     const int32_t *cu_seqlens;
     int32_t *status;
     float scale_log2;
-    int num_seqs, num_tokens, H, window, causal;
+    int num_seqs, num_tokens, H, window, causal, chunk;
 };
 
 // One work item: two query tiles [r0, r0+128) and [r0+128, r0+256) of a
@@ -92,7 +93,7 @@ struct Item {
 
 struct Sched {
     const int *cum, *start, *len;
-    int nseq, H, window, causal;
+    int nseq, H, window, causal, chunk;
     __device__ __forceinline__ Item get(int t) const
     {
         int lo = 0, hi = nseq;                         // cum[lo] <= t < cum[hi]
@@ -114,7 +115,8 @@ struct Sched {
             if (a >= I.L) { lo_w[w] = 0; hi_w[w] = -1; continue; }
             const int b = min(a + BM, I.L) - 1;
             int kl = 0, kh = I.L - 1;
-            if (window > 0) { kl = max(0, a - window + 1); kh = min(I.L - 1, b + window - 1); }
+            if (chunk > 0) { kl = a / chunk * chunk; kh = min(I.L - 1, b / chunk * chunk + chunk - 1); }
+            else if (window > 0) { kl = max(0, a - window + 1); kh = min(I.L - 1, b + window - 1); }
             if (causal) kh = min(kh, b);
             lo_w[w] = kl;
             hi_w[w] = kh;
@@ -265,7 +267,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         if (lane == 31) cum[S] = incl;
     }
     __syncthreads();
-    const Sched sched{cum, start, len, S, P.H, P.window, P.causal};
+    const Sched sched{cum, start, len, S, P.H, P.window, P.causal, P.chunk};
     const int total_items = cum[S];
     const uint32_t tmem = *tmem_base_sm;
 
@@ -366,7 +368,8 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             if (I.jb[w] > I.je[w]) continue;           // this query tile lies past the sequence
             const int rr = I.r0 + w * BM + row;        // query position within its sequence
             int lo = 0, hi = I.L;                      // keys [lo, hi) kept for this row
-            if (P.window > 0) { lo = max(lo, rr - P.window + 1); hi = min(hi, rr + P.window); }
+            if (P.chunk > 0) { lo = rr / P.chunk * P.chunk; hi = min(hi, lo + P.chunk); }
+            else if (P.window > 0) { lo = max(lo, rr - P.window + 1); hi = min(hi, rr + P.window); }
             if (P.causal) hi = min(hi, rr + 1);
             float m = -INFINITY, l = 0.f;
             bool ok = true;
@@ -514,6 +517,7 @@ cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream)
     P.H = a.num_heads;
     P.window = a.window;
     P.causal = a.causal;
+    P.chunk = a.chunk;
     for (int base = 0; base < a.num_seqs; base += MAX_SEQS) {
         P.num_seqs = std::min(MAX_SEQS, a.num_seqs - base);
         P.cu_seqlens = a.cu_seqlens + base;

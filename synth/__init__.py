@@ -318,6 +318,7 @@ class PrefillCase:
     causal: int
     scale: float
     device_qkv: object = None
+    chunk: int = 0                      # > 0: chunked local attention (window must be -1)
 
     @property
     def num_seqs(self) -> int:
@@ -337,6 +338,11 @@ class PrefillCase:
         W = self.window
         for L in np.diff(self.cu_seqlens).astype(np.int64):
             L = int(L)
+            if self.chunk > 0:
+                for a in range(0, L, self.chunk):
+                    c = min(self.chunk, L - a)
+                    tot += c * (c + 1) // 2 if self.causal else c * c
+                continue
             if W <= 0:
                 tot += L * (L + 1) // 2 if self.causal else L * L
             else:
@@ -389,3 +395,16 @@ def prefill_workload(layer: int, device: Optional[str] = None, seqlens=None) -> 
     W = ENCODER_LAYER_WINDOWS[layer % 3]
     return make_prefill_case(f"encoder-prefill-layer{layer}-w{W}", 1004 * 10 + layer, seqlens, 12, 64,
                              W, 0, BF16, 1 / 8, device)
+
+
+CHUNKED_PREFILL_CHUNK = 1024
+
+
+def chunked_prefill_workload(device: Optional[str] = None, seqlens=None) -> PrefillCase:
+    """Chunked local attention (decoder-style, causal within each chunk of
+    1024 positions) over the same 32 packed sequences, 12 heads x 64, bf16."""
+    if seqlens is None:
+        seqlens = prefill_seqlens()
+    c = make_prefill_case("chunked-prefill-c1024", 1004 * 10 + 9, seqlens, 12, 64, -1, 1, BF16, 1 / 8, device)
+    c.chunk = CHUNKED_PREFILL_CHUNK
+    return c
