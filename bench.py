@@ -12,7 +12,9 @@ batch of seeded synthetic input, already resident in HBM:
   tiny-decode        4 x 2 x 64 fp32, contexts U[1,64], Gaussian bias.
   t5-large-decode    decoder self-attention (256 x 16 x 64 bf16, contexts
         U[1,2048], T5 bias padded to 2048) + encoder cross-attention (own block
-        table, encoder length 512, no bias), each after its reshape_and_cache.
+        table, encoder length 512, no bias), both after their reshape_and_cache;
+        the two attention calls go out as one fused launch
+        (--separate-launches: one each).
   long-ctx-decode    512 x 16 x 128 fp16, contexts log-U[16,8192], causal
         window 4096, bias [512,16,8192] N(0,0.25) NaN-padded.
   encoder-prefill    32 packed sequences U[128,8192], 12 heads x 64 bf16,
@@ -282,6 +284,17 @@ class DecodeSide:
     def reshape(self, pka):
         pka.reshape_and_cache(self.new_k, self.new_v, self.kc, self.vc, self.slots)
 
+    def problem(self, bias_on=True):
+        """This side as one problem of the fused launch."""
+        c = self.case
+        pr = dict(out=self.out, q=self.q, k_cache=self.kc, v_cache=self.vc, block_tables=self.bt, context_lens=self.cl,
+                  sliding_window=c.window, scale=c.scale, max_context_len=c.max_context_len, workspace=self.ws)
+        if bias_on and self.use_table and self.table is not None:
+            pr["bias_table"] = self.table
+        elif bias_on and self.bias is not None:
+            pr["attn_bias"] = self.bias
+        return pr
+
     def decode(self, pka, bias_on=True):
         c = self.case
         if bias_on and self.use_table and self.table is not None:
@@ -291,6 +304,24 @@ class DecodeSide:
         pka.paged_attn_decode(self.out, self.q, self.kc, self.vc, self.bt, self.cl,
                               self.bias if bias_on else None, c.window, c.scale, max_context_len=c.max_context_len,
                               workspace=self.ws)
+
+
+def decode_all(pka, sides, fused, bias_on=True, events=None, k=0):
+    """The step's attention calls: one fused launch over all sides, or one
+    launch per side; events[j] brackets launch j."""
+    if fused:
+        if events is not None:
+            events[0][0][k].record()
+        pka.paged_attn_decode_multi([s.problem(bias_on and s.bias is not None) for s in sides])
+        if events is not None:
+            events[0][1][k].record()
+        return
+    for j, s in enumerate(sides):
+        if events is not None:
+            events[j][0][k].record()
+        s.decode(pka, bias_on and s.bias is not None)
+        if events is not None:
+            events[j][1][k].record()
 
 
 def build_decode_sides(workload, device, on_device_draw, num_seqs=None):
@@ -325,14 +356,13 @@ def run_decode(args, rank, world, local, peaks):
     rot = [sides] + [[s.clone() for s in sides] for _ in range(copies - 1)]
     torch.cuda.synchronize()
 
+    fused = len(sides) > 1 and not args.separate_launches
+    nlaunch = 1 if fused else len(sides)
+
     def step(i, bias_on=True, events=None):
-        for j, s in enumerate(rot[i % copies]):
+        for s in rot[i % copies]:
             s.reshape(pka)
-            if events is not None:
-                events[j][0][i].record()
-            s.decode(pka, bias_on and s.bias is not None)
-            if events is not None:
-                events[j][1][i].record()
+        decode_all(pka, rot[i % copies], fused, bias_on, events, i)
 
     clocks = ClockSampler(gpu_id(local))
     clocks.start()
@@ -361,10 +391,13 @@ def run_decode(args, rank, world, local, peaks):
     ms_step = total_ms / K
     # per-launch durations: the same K steps eagerly, queued behind a GPU-side
     # sleep so the host is ahead and events see kernel time, not launch gaps
-    launch_ms = per_launch_ms(lambda ev: [step(k, True, ev) for k in range(K)], len(sides), K)
+    launch_ms = per_launch_ms(lambda ev: [step(k, True, ev) for k in range(K)], nlaunch, K)
     off_ms = None
     if any(s.bias is not None for s in sides):
-        off_ms = sum(per_launch_ms(lambda ev: [step(k, False, ev) for k in range(K)], len(sides), K))
+        off_ms = sum(per_launch_ms(lambda ev: [step(k, False, ev) for k in range(K)], nlaunch, K))
+    if fused:                          # one launch carries every side's bytes
+        bytes_on = [{k: sum(b[k] for b in bytes_on) for k in bytes_on[0]}]
+        bytes_off = [{k: sum(b[k] for b in bytes_off) for k in bytes_off[0]}]
 
     value = step_bytes * world / (ms_step * 1e-3) / 1e9
     # dominant kernel: the decode launch carrying the most bytes
@@ -375,7 +408,7 @@ def run_decode(args, rank, world, local, peaks):
             "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
             "kernel": "paged_decode_kernel", "alg_bytes_per_launch": bytes_on[jd]["total"],
             "launch_ms": round(launch_ms[jd], 5), "peak_src": peaks["src"] + " hbm_gbs (copy)"}
-    e2e = decode_e2e(args, sides, pka, step_bytes, world) if not args.no_e2e else None
+    e2e = decode_e2e(args, sides, pka, step_bytes, world, fused) if not args.no_e2e else None
     seqs = sum(c.num_seqs for c in cases[:1])
     extra = {
         "decode_ms_per_launch": [round(x, 5) for x in launch_ms],
@@ -393,13 +426,14 @@ def run_decode(args, rank, world, local, peaks):
            "bias": [("t5 table in kernel" if args.t5_table and c.bias_table is not None else "materialised")
                     if c.bias is not None else None for c in cases],
            "l2": f"inputs rotated over {copies} copies ({per_copy * copies / 2**20:.0f} MiB > L2)"
-           if copies > 1 else f"inputs {per_copy / 2**20:.0f} MiB > L2", "parallelism": f"replicas x{world}"}
+           if copies > 1 else f"inputs {per_copy / 2**20:.0f} MiB > L2", "parallelism": f"replicas x{world}",
+           "attention_launches": "one fused launch (self + cross)" if fused else "one per attention type"}
     return {"value": value, "unit": "GB/s", "ms_per_step": ms_step, "dtype": synth.DTYPE_NAMES[cases[0].dtype],
             "config": cfg, "roofline": roof, "e2e": e2e, "clocks": clk,
-            "gpu_launches": K * 2 * len(sides), "extra": extra, "cases": cases}
+            "gpu_launches": K * (len(sides) + nlaunch), "extra": extra, "cases": cases}
 
 
-def decode_e2e(args, sides, pka, step_bytes, world):
+def decode_e2e(args, sides, pka, step_bytes, world, fused=False):
     """The same step through the public API from pinned host buffers: copy the
     step's inputs host->device, run it, read the output back."""
     import torch
@@ -423,11 +457,12 @@ def decode_e2e(args, sides, pka, step_bytes, world):
     d2h = sum(o.numel() * o.element_size() for o in outs)
 
     def step():
-        for s, pairs, o in zip(sides, host_in, outs):
+        for s, pairs in zip(sides, host_in):
             for h, d in pairs:
                 d.copy_(h, non_blocking=True)
             s.reshape(pka)
-            s.decode(pka, s.bias is not None)
+        decode_all(pka, sides, fused)
+        for s, o in zip(sides, outs):
             o.copy_(s.out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -716,6 +751,8 @@ def main():
     ap.add_argument("--workload", default="t5-small-decode",
                     choices=sorted(DECODE_WORKLOADS) + ["encoder-prefill", "chunked-prefill"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--separate-launches", action="store_true",
+                    help="t5-large-decode: one decode launch per attention type instead of one fused launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)

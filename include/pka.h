@@ -177,6 +177,64 @@ PKA_API pka_status pka_paged_attn_decode_t5bias(void *out, const void *q, const 
                                                 size_t workspace_bytes, int32_t *status, void *stream);
 
 /*
+ * pka_paged_attn_decode_multi — several decode problems in one launch.  An
+ * encoder-decoder decode step attends twice per layer: decoder self-attention
+ * over the generated tokens' cache blocks and cross-attention over the
+ * prompt's ("Add Encoder-decoder model support and T5 Model support": the two
+ * attention types keep separate block tables, and cross-attention's context
+ * is the encoder length, fixed for the request).  Both go into one grid here:
+ * each problem keeps its own q/out, caches, block table, context lengths,
+ * bias, window, scale and workspace, and every problem computes exactly what
+ * pka_paged_attn_decode (or, with bias_table, pka_paged_attn_decode_t5bias)
+ * computes for it alone.  The problems only share one launch (a single
+ * launch latency and one tail instead of two).
+ *
+ *   problems      host array of num_problems descriptors (read during the
+ *                 call only); each field means what the argument of the same
+ *                 name means for pka_paged_attn_decode.  bias_table /
+ *                 num_buckets select the in-kernel T5 bias as for
+ *                 pka_paged_attn_decode_t5bias; a problem has attn_bias or
+ *                 bias_table, not both.  When two problems both use a table
+ *                 it must be the same table (same pointer and num_buckets:
+ *                 it is cached once in shared memory).
+ *   num_problems  1 or 2 (PKA_ERR_UNSUPPORTED beyond)
+ *   block_size, num_heads, head_dim, dtype   shared by all problems
+ *   workspace     each problem's own workspace field: sized by
+ *                 pka_paged_attn_decode_workspace_size for that problem,
+ *                 zero-filled before first use and left zero, as for
+ *                 pka_paged_attn_decode; the problems' workspaces must not
+ *                 overlap.  PKA_ERR_WORKSPACE if any is missing or short.
+ *   status        one int32 device word or NULL for all problems
+ * Problems with num_seqs == 0 are skipped.  The problems' out arrays must
+ * not overlap (PKA_ERR_INVALID_ARG).  Errors are those of the single-problem calls, checked per
+ * problem before anything is enqueued.
+ */
+typedef struct {
+    void *out;
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    const float *attn_bias;      /* or NULL */
+    const float *bias_table;     /* or NULL: T5 table [num_heads, num_buckets] */
+    int num_buckets;
+    int sliding_window;
+    float scale;
+    int num_seqs;
+    int max_blocks_per_seq;
+    int bias_row_stride;
+    int num_blocks;
+    int max_context_len;
+    void *workspace;
+    size_t workspace_bytes;
+} pka_decode_problem;
+
+PKA_API pka_status pka_paged_attn_decode_multi(const pka_decode_problem *problems, int num_problems,
+                                               int block_size, int num_heads, int head_dim, pka_dtype dtype,
+                                               int32_t *status, void *stream);
+
+/*
  * pka_paged_attn_decode_noalloc — pka_paged_attn_decode for callers that
  * cannot allocate device memory.  The pages have no counterpart: this is an
  * interface convenience, not part of the method.

@@ -13,7 +13,7 @@ import os
 import threading
 
 __all__ = ["PkaError", "load", "build", "lib_path", "reshape_and_cache", "paged_attn_decode",
-           "paged_attn_decode_t5bias", "chunked_prefill",
+           "paged_attn_decode_t5bias", "paged_attn_decode_multi", "chunked_prefill",
            "paged_attn_decode_workspace_size", "swa_prefill", "DecodeWorkspace", "DTYPE_CODE",
            "DEVCHK_BLOCK_ID", "DEVCHK_CONTEXT_LEN", "DEVCHK_SLOT", "DEVCHK_TIMEOUT", "DEVCHK_CU_SEQLENS",
            "EXPORTED_SYMBOLS"]
@@ -26,8 +26,19 @@ DEVCHK_BLOCK_ID, DEVCHK_CONTEXT_LEN, DEVCHK_SLOT, DEVCHK_TIMEOUT, DEVCHK_CU_SEQL
 
 EXPORTED_SYMBOLS = ("pka_status_string", "pka_version", "pka_reshape_and_cache",
                     "pka_paged_attn_decode_workspace_size", "pka_paged_attn_decode",
-                    "pka_paged_attn_decode_noalloc", "pka_paged_attn_decode_t5bias", "pka_swa_prefill",
-                    "pka_chunked_prefill")
+                    "pka_paged_attn_decode_noalloc", "pka_paged_attn_decode_t5bias",
+                    "pka_paged_attn_decode_multi", "pka_swa_prefill", "pka_chunked_prefill")
+
+
+class DecodeProblem(ctypes.Structure):
+    """The C struct pka_decode_problem (one problem of pka_paged_attn_decode_multi)."""
+    _fields_ = [("out", ctypes.c_void_p), ("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p),
+                ("v_cache", ctypes.c_void_p), ("block_tables", ctypes.c_void_p), ("context_lens", ctypes.c_void_p),
+                ("attn_bias", ctypes.c_void_p), ("bias_table", ctypes.c_void_p), ("num_buckets", ctypes.c_int),
+                ("sliding_window", ctypes.c_int), ("scale", ctypes.c_float), ("num_seqs", ctypes.c_int),
+                ("max_blocks_per_seq", ctypes.c_int), ("bias_row_stride", ctypes.c_int),
+                ("num_blocks", ctypes.c_int), ("max_context_len", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 _lib = None
 _lock = threading.Lock()
@@ -70,6 +81,8 @@ def load():
         lib.pka_paged_attn_decode_t5bias.argtypes = [P, P, P, P, P, P, P, I, I, F, I, I, I, I, I, I, I, I, P,
                                                      ctypes.c_size_t, P, P]
         lib.pka_paged_attn_decode_t5bias.restype = I
+        lib.pka_paged_attn_decode_multi.argtypes = [ctypes.POINTER(DecodeProblem), I, I, I, I, I, P, P]
+        lib.pka_paged_attn_decode_multi.restype = I
         lib.pka_swa_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P]
         lib.pka_swa_prefill.restype = I
         lib.pka_chunked_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P]
@@ -226,6 +239,60 @@ def paged_attn_decode_t5bias(out, q, k_cache, v_cache, block_tables, context_len
                                             workspace.numel() * workspace.element_size(), _ptr(status),
                                             _stream(stream)))
     return out
+
+
+def paged_attn_decode_multi(problems, status=None, stream=None):
+    """Several paged decodes in one launch (at most two: an encoder-decoder
+    step's self- and cross-attention).  ``problems`` is a sequence of dicts
+    with the keyword arguments of ``paged_attn_decode`` — out, q, k_cache,
+    v_cache, block_tables, context_lens and optionally attn_bias or
+    bias_table, sliding_window, scale, max_context_len, workspace.  All share
+    num_heads, head_dim, block size and dtype; each gets its own workspace."""
+    torch = _torch()
+    lib = load()
+    arr = (DecodeProblem * max(1, len(problems)))()
+    keep = []
+    H = D = bs = dt = None
+    for i, pr in enumerate(problems):
+        out, q, kc, vc = pr["out"], pr["q"], pr["k_cache"], pr["v_cache"]
+        bt, cl = pr["block_tables"], pr["context_lens"]
+        bias, table = pr.get("attn_bias"), pr.get("bias_table")
+        _need(out, "out", ndim=3); _need(q, "q", ndim=3)
+        _need(kc, "k_cache", ndim=4); _need(vc, "v_cache", ndim=4)
+        _need(bt, "block_tables", torch.int32, 2)
+        _need(cl, "context_lens", torch.int32, 1)
+        if bias is not None:
+            _need(bias, "attn_bias", torch.float32, 3)
+        if table is not None:
+            _need(table, "bias_table", torch.float32, 2)
+        S, h, d = q.shape
+        nb, _, b, _ = kc.shape
+        if H is not None and (h, d, b, _dtype_code(q)) != (H, D, bs, dt):
+            raise ValueError("paged_attn_decode_multi: problems must share num_heads, head_dim, block size and dtype")
+        H, D, bs, dt = h, d, b, _dtype_code(q)
+        mbps = bt.shape[1]
+        stride = bias.shape[2] if bias is not None else 0
+        w = int(pr.get("sliding_window", -1))
+        mcl = pr.get("max_context_len")
+        if mcl is None:
+            mcl = mbps * bs if bias is None else min(mbps * bs, stride)
+        scale = pr.get("scale")
+        if scale is None:
+            scale = D ** -0.5
+        need = int(lib.pka_paged_attn_decode_workspace_size(S, H, D, int(mcl), w))
+        ws = pr.get("workspace")
+        if ws is None:
+            dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
+            ws = _default_ws.setdefault((dev, "multi", i), DecodeWorkspace(q.device)).get(need)
+        keep.append(ws)
+        arr[i] = DecodeProblem(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(cl), _ptr(bias), _ptr(table),
+                               table.shape[1] if table is not None else 0, w, float(scale), S, mbps, stride, nb,
+                               int(mcl), _ptr(ws), ws.numel() * ws.element_size())
+    if not problems:
+        raise ValueError("paged_attn_decode_multi needs at least one problem")
+    _check("pka_paged_attn_decode_multi",
+           lib.pka_paged_attn_decode_multi(arr, len(problems), bs, H, D, dt, _ptr(status), _stream(stream)))
+    return [pr["out"] for pr in problems]
 
 
 def swa_prefill(out, q, k, v, cu_seqlens, max_seqlen, window=-1, causal=0, scale=None, status=None, stream=None):

@@ -70,26 +70,39 @@ template <typename T, int D> struct Tr {
     static_assert(NC % 8 == 0 && 32 % NC == 0, "row must be 8, 16 or 32 chunks");
 };
 
-struct Params {
+// One decode problem of a launch: decoder self-attention and encoder
+// cross-attention of a step are two problems with their own block tables.
+constexpr int MAX_PROBLEMS = 2;
+struct Prob {
     void *out;
     const unsigned char *q, *k_cache, *v_cache;
     const int32_t *block_tables, *context_lens;
     const float *bias;
     const float *bias_table;     // [H, num_buckets] T5 relative-position table, or NULL
-    int32_t *status;
     unsigned *counters;
     float2 *ws_ml;
     float *ws_acc;
     float scale_log2;
-    int window, seq_base, num_seqs, H, mbps, num_blocks, max_ctx, part_blocks, max_parts;
+    int window, seq_base, num_seqs, mbps, num_blocks, max_ctx, part_blocks, max_parts, num_buckets;
     long long bias_stride;
-    int num_buckets;
+};
+
+struct Params {
+    Prob pr[MAX_PROBLEMS];
+    int nprob;
+    int num_seqs;                // sequences of this launch over all problems (problem 0's first)
+    int H;
+    int32_t *status;
 };
 
 struct Unit {
     int s;       // sequence index within this launch
+    int prob;    // which problem
+    int gs;      // sequence index within that problem
     int h, p, npart, ctx, start, b0, nb;
 };
+
+__device__ __forceinline__ int prob_of(int s, const Params &P) { return (P.nprob > 1 && s >= P.pr[0].num_seqs) ? 1 : 0; }
 
 // Unit u -> (s, h, p) by binary search in the per-sequence prefix sums.
 __device__ __forceinline__ Unit unit_of(int u, const int *cum, const int *ctxs, const Params &P)
@@ -101,18 +114,21 @@ __device__ __forceinline__ Unit unit_of(int u, const int *cum, const int *ctxs, 
     }
     Unit U;
     U.s = lo;
+    U.prob = prob_of(lo, P);
+    const Prob &R = P.pr[U.prob];
+    U.gs = R.seq_base + lo - (U.prob ? P.pr[0].num_seqs : 0);
     U.npart = (cum[lo + 1] - cum[lo]) / P.H;
     const int r = u - cum[lo];
     U.h = r / U.npart;
     U.p = r - U.h * U.npart;
     U.ctx = ctxs[lo];
-    U.start = (P.window > 0 && U.ctx > P.window) ? U.ctx - P.window : 0;
+    U.start = (R.window > 0 && U.ctx > R.window) ? U.ctx - R.window : 0;
     if (U.ctx == 0) {
         U.b0 = 0; U.nb = 0;
     } else {
         const int last = (U.ctx - 1) / BS;
-        U.b0 = U.start / BS + U.p * P.part_blocks;
-        U.nb = min(P.part_blocks, last + 1 - U.b0);
+        U.b0 = U.start / BS + U.p * R.part_blocks;
+        U.nb = min(R.part_blocks, last + 1 - U.b0);
     }
     return U;
 }
@@ -120,7 +136,7 @@ __device__ __forceinline__ Unit unit_of(int u, const int *cum, const int *ctxs, 
 __device__ __forceinline__ int load_bt(const Unit &U, const Params &P, int lane)
 {
     if (lane < U.nb)
-        return __ldg(P.block_tables + (size_t)(P.seq_base + U.s) * P.mbps + U.b0 + lane);
+        return __ldg(P.pr[U.prob].block_tables + (size_t)U.gs * P.pr[U.prob].mbps + U.b0 + lane);
     return 0;
 }
 
@@ -176,22 +192,29 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
 
     // ---- per-sequence partition counts -> prefix sums (whole CTA) ----------
     for (int s = threadIdx.x; s < P.num_seqs; s += blockDim.x) {
-        int c = __ldg(P.context_lens + P.seq_base + s);
-        if (c < 0 || c > P.max_ctx || c > P.mbps * BS) {
+        const int pi = prob_of(s, P);
+        const Prob &R = P.pr[pi];
+        int c = __ldg(R.context_lens + R.seq_base + s - (pi ? P.pr[0].num_seqs : 0));
+        if (c < 0 || c > R.max_ctx || c > R.mbps * BS) {
             flag_status(P.status, PKA_DEVCHK_CONTEXT_LEN);
-            c = c < 0 ? 0 : min(c, min(P.max_ctx, P.mbps * BS));
+            c = c < 0 ? 0 : min(c, min(R.max_ctx, R.mbps * BS));
         }
         ctxs[s] = c;
         int npart = 1;
         if (c > 0) {
-            const int start = (P.window > 0 && c > P.window) ? c - P.window : 0;
+            const int start = (R.window > 0 && c > R.window) ? c - R.window : 0;
             const int nblk = (c - 1) / BS - start / BS + 1;
-            npart = min((nblk + P.part_blocks - 1) / P.part_blocks, P.max_parts);
+            npart = min((nblk + R.part_blocks - 1) / R.part_blocks, R.max_parts);
         }
         cum[s + 1] = npart * P.H;
     }
-    if (P.bias_table)
-        for (int i = threadIdx.x; i < P.H * P.num_buckets; i += blockDim.x) table_sm[i] = __ldg(P.bias_table + i);
+    // a T5 bias table is cached in shared memory; when both problems of a
+    // launch use one, the host has checked that it is the same table
+    {
+        const Prob &TP = P.pr[(P.nprob > 1 && P.pr[0].bias_table == nullptr) ? 1 : 0];
+        if (TP.bias_table)
+            for (int i = threadIdx.x; i < P.H * TP.num_buckets; i += blockDim.x) table_sm[i] = __ldg(TP.bias_table + i);
+    }
     if (lane == 0)
         for (int i = 0; i < NSTAGE; ++i) mbar_init(smem_u32(&bars[i]), 32);
     fence_barrier_init();
@@ -219,8 +242,6 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
     const int nwt = gridDim.x * NW;
     if (gw >= total_units) return;                    // no CTA-wide sync after this point
 
-    const bool has_bias = P.bias != nullptr;
-    const bool has_table = P.bias_table != nullptr;
 
     // ---- producer state (issue side) ---------------------------------------
     int pk = 0;                                        // unit ordinal of the issue side
@@ -261,26 +282,27 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
             const int stage = issued % NSTAGE;
             const uint32_t st = st_base + stage * R::STAGE;
             const uint32_t bar = smem_u32(&bars[stage]);
+            const Prob &PP = P.pr[pu.prob];
             int phys = __shfl_sync(kFull, pbt, pib);
-            if ((unsigned)phys >= (unsigned)P.num_blocks) {
+            if ((unsigned)phys >= (unsigned)PP.num_blocks) {
                 if (lane == 0) flag_status(P.status, PKA_DEVCHK_BLOCK_ID);
                 phys = 0;
             }
-            const int gs = P.seq_base + pu.s;
+            const int gs = pu.gs;
             if (lane == 0) {
                 mbar_expect_tx(bar, 2 * R::CHUNK);
                 const size_t off = ((size_t)phys * P.H + pu.h) * (size_t)R::CHUNK;
-                bulk_g2s(st + R::K_OFF, P.k_cache + off, R::CHUNK, bar);
-                bulk_g2s(st + R::V_OFF, P.v_cache + off, R::CHUNK, bar);
+                bulk_g2s(st + R::K_OFF, PP.k_cache + off, R::CHUNK, bar);
+                bulk_g2s(st + R::V_OFF, PP.v_cache + off, R::CHUNK, bar);
             }
-            if (has_bias && lane < BS) {
+            if (PP.bias != nullptr && lane < BS) {
                 const int j = (pu.b0 + pib) * BS + lane;
                 const bool ok = j >= pu.start && j < pu.ctx;
-                const float *src = P.bias + ((size_t)gs * P.H + pu.h) * P.bias_stride + (ok ? j : 0);
+                const float *src = PP.bias + ((size_t)gs * P.H + pu.h) * PP.bias_stride + (ok ? j : 0);
                 cp_async_4(st + R::B_OFF + lane * 4, src, ok ? 4u : 0u);
             }
             if (pib == 0 && lane < R::NC)
-                cp_async_16(st + R::Q_OFF + lane * 16, P.q + ((size_t)gs * P.H + pu.h) * R::ROW + lane * 16);
+                cp_async_16(st + R::Q_OFF + lane * 16, PP.q + ((size_t)gs * P.H + pu.h) * R::ROW + lane * 16);
             cp_async_arrive_noinc(bar);
             ++issued;
             if (++pib >= pu.nb) {
@@ -294,6 +316,8 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
         const int u = gw + ck * nwt;
         if (u >= total_units) break;
         const Unit cu = unit_of(u, cum, ctxs, P);
+        const Prob &CP = P.pr[cu.prob];
+        const bool has_bias = CP.bias != nullptr, has_table = CP.bias_table != nullptr;
         m_run = -INFINITY;
         l_run = 0.f;
 #pragma unroll
@@ -317,10 +341,10 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
                 bv = reinterpret_cast<const float *>(stp + R::B_OFF)[key];
             } else if (has_table) {
                 // T5 relative position: distance ctx-1-j, capped at the last column
-                const int dist = min(max(cu.ctx - 1 - j, 0), P.num_buckets - 1);
-                bv = table_sm[cu.h * P.num_buckets + dist];
+                const int dist = min(max(cu.ctx - 1 - j, 0), CP.num_buckets - 1);
+                bv = table_sm[cu.h * CP.num_buckets + dist];
             }
-            const float x = (j >= cu.start && j < cu.ctx) ? (d + bv) * P.scale_log2 : -INFINITY;
+            const float x = (j >= cu.start && j < cu.ctx) ? (d + bv) * CP.scale_log2 : -INFINITY;
             float mb = fmaxf(x, __shfl_xor_sync(kFull, x, 2));
             mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 4));
             mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 8));
@@ -356,42 +380,41 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
         for (int x = R::NC; x < 32; x <<= 1)
 #pragma unroll
             for (int e = 0; e < R::EPC; ++e) acc[e] += __shfl_xor_sync(kFull, acc[e], x);
-        const int gs = P.seq_base + cu.s;
-        const size_t sh = (size_t)gs * P.H + cu.h;
+        const size_t sh = (size_t)cu.gs * P.H + cu.h;
         if (cu.npart == 1) {
             const float inv = l > 0.f ? 1.f / l : 0.f;
             if (lane < R::NC) {
                 float o[R::EPC];
 #pragma unroll
                 for (int e = 0; e < R::EPC; ++e) o[e] = acc[e] * inv;
-                reinterpret_cast<uint4 *>(static_cast<unsigned char *>(P.out) + sh * R::ROW)[lane] =
+                reinterpret_cast<uint4 *>(static_cast<unsigned char *>(CP.out) + sh * R::ROW)[lane] =
                     Vec<T>::from_f32(o);
             }
             continue;
         }
-        const size_t slot = sh * P.max_parts + cu.p;
+        const size_t slot = sh * CP.max_parts + cu.p;
         if (lane < R::NC) {
-            float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + slot * D + lane * R::EPC);
+            float4 *dst = reinterpret_cast<float4 *>(CP.ws_acc + slot * D + lane * R::EPC);
 #pragma unroll
             for (int e = 0; e < R::EPC; e += 4)
                 __stcg(dst + e / 4, make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]));
         }
-        if (lane == 0) __stcg(P.ws_ml + slot, make_float2(m_run, l));
+        if (lane == 0) __stcg(CP.ws_ml + slot, make_float2(m_run, l));
         __syncwarp();
         unsigned old = 0;
-        if (lane == 0) old = atom_inc_acq_rel(P.counters + sh, (unsigned)(cu.npart - 1));
+        if (lane == 0) old = atom_inc_acq_rel(CP.counters + sh, (unsigned)(cu.npart - 1));
         old = __shfl_sync(kFull, old, 0);
         if (old != (unsigned)(cu.npart - 1)) continue;
 
         // last partition of (s, h): merge, write out, return the slots to zero
-        const size_t base = sh * P.max_parts;
+        const size_t base = sh * CP.max_parts;
         float M = -INFINITY;
-        for (int i = lane; i < cu.npart; i += 32) M = fmaxf(M, __ldcg(P.ws_ml + base + i).x);
+        for (int i = lane; i < cu.npart; i += 32) M = fmaxf(M, __ldcg(CP.ws_ml + base + i).x);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
         float L = 0.f;
         for (int i = lane; i < cu.npart; i += 32) {
-            const float2 ml = __ldcg(P.ws_ml + base + i);
+            const float2 ml = __ldcg(CP.ws_ml + base + i);
             L += ml.y * ex2(ml.x - M);
         }
 #pragma unroll
@@ -400,8 +423,8 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
 #pragma unroll
         for (int e = 0; e < R::DPL; ++e) o_acc[e] = 0.f;
         for (int i = 0; i < cu.npart; ++i) {
-            const float w = ex2(__ldcg(P.ws_ml + base + i).x - M);
-            float *src = P.ws_acc + (base + i) * D + lane * R::DPL;
+            const float w = ex2(__ldcg(CP.ws_ml + base + i).x - M);
+            float *src = CP.ws_acc + (base + i) * D + lane * R::DPL;
             if constexpr (R::DPL == 4) {
                 const float4 a4 = __ldcg(reinterpret_cast<const float4 *>(src));
                 o_acc[0] = fmaf(w, a4.x, o_acc[0]); o_acc[1] = fmaf(w, a4.y, o_acc[1]);
@@ -414,9 +437,9 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
             }
         }
         __syncwarp();
-        for (int i = lane; i < cu.npart; i += 32) __stcg(P.ws_ml + base + i, make_float2(0.f, 0.f));
+        for (int i = lane; i < cu.npart; i += 32) __stcg(CP.ws_ml + base + i, make_float2(0.f, 0.f));
         const float inv = L > 0.f ? 1.f / L : 0.f;
-        T *dst = reinterpret_cast<T *>(static_cast<unsigned char *>(P.out) + sh * R::ROW) + lane * R::DPL;
+        T *dst = reinterpret_cast<T *>(static_cast<unsigned char *>(CP.out) + sh * R::ROW) + lane * R::DPL;
 #pragma unroll
         for (int e = 0; e < R::DPL; ++e) {
             const float v = o_acc[e] * inv;
@@ -450,7 +473,8 @@ template <typename T, int D, int NSTAGE, int NW> struct Config {
             if (occ < 1) occ = 1;
         });
         if (attr_err != cudaSuccess) return attr_err;
-        const long long units_upper = (long long)P.num_seqs * P.H * P.max_parts;
+        long long units_upper = 0;
+        for (int i = 0; i < P.nprob; ++i) units_upper += (long long)P.pr[i].num_seqs * P.H * P.pr[i].max_parts;
         long long grid = std::min<long long>((long long)sms * occ, (units_upper + NW - 1) / NW);
         if (grid < 1) grid = 1;
         kern<<<(unsigned)grid, NW * 32, smem, stream>>>(P);
@@ -503,74 +527,124 @@ static int streaming_warps(pka_dtype dt, int head_dim)
     return stage <= 5000 ? 16 : stage <= 9000 ? 12 : 6;
 }
 
-cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &size_plan, cudaStream_t stream)
+static cudaError_t dispatch(const Params &P, pka_dtype dt, int head_dim, int sms, cudaStream_t stream)
 {
-    if (a.num_seqs == 0) return cudaSuccess;
+    if (head_dim == 64) {
+        if (dt == PKA_F32) return dispatch_cfg<float, 64>(P, sms, stream);
+        if (dt == PKA_F16) return dispatch_cfg<__half, 64>(P, sms, stream);
+        return dispatch_cfg<__nv_bfloat16, 64>(P, sms, stream);
+    }
+    if (dt == PKA_F32) return dispatch_cfg<float, 128>(P, sms, stream);
+    if (dt == PKA_F16) return dispatch_cfg<__half, 128>(P, sms, stream);
+    return dispatch_cfg<__nv_bfloat16, 128>(P, sms, stream);
+}
+
+cudaError_t launch_paged_decode_multi(const DecodeArgs *a, const DecodePlan *size_plans, int n, cudaStream_t stream)
+{
+    if (n < 1 || n > MAX_PROBLEMS) return cudaErrorInvalidValue;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int H = a[0].num_heads;
     // Fewer, larger partitions cost fewer split-K merges (each ends with a
     // release and an atomic), while enough units keep every warp busy: double
-    // the partition while the batch still yields at least 3 units per
-    // streaming warp of the GPU.  The workspace was sized for size_plan, the
-    // smallest partitions, so it covers any larger ones.
-    DecodePlan plan = size_plan;
-    {
-        long long maxvb = (long long)plan.max_parts * plan.part_blocks;
-        const long long sh = (long long)a.num_seqs * a.num_heads;
-        const long long target = 3ll * sms * streaming_warps(a.dtype, a.head_dim);
-        int pb = plan.part_blocks;
-        long long vb = (a.max_context_len + BS - 1) / BS;
-        if (a.window > 0) vb = std::min<long long>(vb, (a.window + BS - 2) / BS + 1);
-        maxvb = std::max<long long>(1, std::min(maxvb, vb));
-        while (pb < 32 && sh * ((maxvb + 2 * pb - 1) / (2 * pb)) >= target) pb *= 2;
-        if (pb != plan.part_blocks) {
-            plan.part_blocks = pb;
-            plan.max_parts = (int)std::max<long long>(1, (maxvb + pb - 1) / pb);
-        }
+    // a problem's partition (the one with the most partitions first) while the
+    // launch still yields at least 3 units per streaming warp of the GPU.  Each
+    // workspace was sized for its size plan, the smallest partitions, so it
+    // covers any larger ones.
+    DecodePlan plan[MAX_PROBLEMS];
+    long long maxvb[MAX_PROBLEMS], sh[MAX_PROBLEMS];
+    for (int i = 0; i < n; ++i) {
+        plan[i] = size_plans[i];
+        long long vb = (a[i].max_context_len + BS - 1) / BS;
+        if (a[i].window > 0) vb = std::min<long long>(vb, (a[i].window + BS - 2) / BS + 1);
+        maxvb[i] = std::max<long long>(1, std::min((long long)plan[i].max_parts * plan[i].part_blocks, vb));
+        sh[i] = (long long)a[i].num_seqs * H;
     }
-    const size_t sh = (size_t)a.num_seqs * a.num_heads;
-    const size_t slots = sh * plan.max_parts;
-    unsigned char *ws = static_cast<unsigned char *>(a.workspace);
-    Params P;
-    P.out = a.out;
-    P.q = static_cast<const unsigned char *>(a.q);
-    P.k_cache = static_cast<const unsigned char *>(a.k_cache);
-    P.v_cache = static_cast<const unsigned char *>(a.v_cache);
-    P.block_tables = a.block_tables;
-    P.context_lens = a.context_lens;
-    P.bias = a.bias;
-    P.status = a.status;
-    P.counters = reinterpret_cast<unsigned *>(ws);
-    P.ws_ml = reinterpret_cast<float2 *>(ws + round_up(sh * 4, 256));
-    P.ws_acc = reinterpret_cast<float *>(ws + round_up(sh * 4, 256) + round_up(slots * 8, 256));
-    P.scale_log2 = a.scale * 1.4426950408889634f;
-    P.window = a.window;
-    P.H = a.num_heads;
-    P.mbps = a.max_blocks_per_seq;
-    P.num_blocks = a.num_blocks;
-    P.max_ctx = a.max_context_len;
-    P.part_blocks = plan.part_blocks;
-    P.max_parts = plan.max_parts;
-    P.bias_stride = a.bias_row_stride;
-    P.bias_table = a.bias_table;
-    P.num_buckets = a.num_buckets;
-    for (int base = 0; base < a.num_seqs; base += MAX_SEQS_PER_LAUNCH) {
-        P.seq_base = base;
-        P.num_seqs = std::min(MAX_SEQS_PER_LAUNCH, a.num_seqs - base);
-        cudaError_t e;
-        if (a.head_dim == 64) {
-            if (a.dtype == PKA_F32) e = dispatch_cfg<float, 64>(P, sms, stream);
-            else if (a.dtype == PKA_F16) e = dispatch_cfg<__half, 64>(P, sms, stream);
-            else e = dispatch_cfg<__nv_bfloat16, 64>(P, sms, stream);
-        } else {
-            if (a.dtype == PKA_F32) e = dispatch_cfg<float, 128>(P, sms, stream);
-            else if (a.dtype == PKA_F16) e = dispatch_cfg<__half, 128>(P, sms, stream);
-            else e = dispatch_cfg<__nv_bfloat16, 128>(P, sms, stream);
+    auto parts = [&](int i, int pb) { return (maxvb[i] + pb - 1) / pb; };
+    const long long target = 3ll * sms * streaming_warps(a[0].dtype, a[0].head_dim);
+    int pb[MAX_PROBLEMS];
+    for (int i = 0; i < n; ++i) pb[i] = plan[i].part_blocks;
+    for (;;) {
+        long long total = 0;
+        for (int i = 0; i < n; ++i) total += sh[i] * parts(i, pb[i]);
+        int pick = -1;
+        for (int i = 0; i < n; ++i) {
+            if (pb[i] >= 32 || sh[i] == 0) continue;
+            if (total - sh[i] * (parts(i, pb[i]) - parts(i, 2 * pb[i])) < target) continue;
+            if (pick < 0 || parts(i, pb[i]) > parts(pick, pb[pick])) pick = i;
         }
+        if (pick < 0) break;
+        pb[pick] *= 2;
+    }
+    Prob pr[MAX_PROBLEMS];
+    for (int i = 0; i < n; ++i) {
+        if (pb[i] != plan[i].part_blocks) {
+            plan[i].part_blocks = pb[i];
+            plan[i].max_parts = (int)parts(i, pb[i]);
+        }
+        const size_t shi = (size_t)sh[i];
+        const size_t slots = shi * plan[i].max_parts;
+        unsigned char *ws = static_cast<unsigned char *>(a[i].workspace);
+        Prob &R = pr[i];
+        R.out = a[i].out;
+        R.q = static_cast<const unsigned char *>(a[i].q);
+        R.k_cache = static_cast<const unsigned char *>(a[i].k_cache);
+        R.v_cache = static_cast<const unsigned char *>(a[i].v_cache);
+        R.block_tables = a[i].block_tables;
+        R.context_lens = a[i].context_lens;
+        R.bias = a[i].bias;
+        R.bias_table = a[i].bias_table;
+        R.num_buckets = a[i].num_buckets;
+        R.counters = reinterpret_cast<unsigned *>(ws);
+        R.ws_ml = reinterpret_cast<float2 *>(ws + round_up(shi * 4, 256));
+        R.ws_acc = reinterpret_cast<float *>(ws + round_up(shi * 4, 256) + round_up(slots * 8, 256));
+        R.scale_log2 = a[i].scale * 1.4426950408889634f;
+        R.window = a[i].window;
+        R.mbps = a[i].max_blocks_per_seq;
+        R.num_blocks = a[i].num_blocks;
+        R.max_ctx = a[i].max_context_len;
+        R.part_blocks = plan[i].part_blocks;
+        R.max_parts = plan[i].max_parts;
+        R.bias_stride = a[i].bias_row_stride;
+        R.seq_base = 0;
+        R.num_seqs = a[i].num_seqs;
+    }
+    // The sequences of all problems, problem 0's first, go out in launches of
+    // at most MAX_SEQS_PER_LAUNCH; a launch may hold the tail of one problem
+    // and the head of the next.
+    long long total_seqs = 0, first[MAX_PROBLEMS];
+    for (int i = 0; i < n; ++i) {
+        first[i] = total_seqs;
+        total_seqs += a[i].num_seqs;
+    }
+    for (long long base = 0; base < total_seqs; base += MAX_SEQS_PER_LAUNCH) {
+        const long long end = std::min<long long>(total_seqs, base + MAX_SEQS_PER_LAUNCH);
+        Params P;
+        P.nprob = 0;
+        P.num_seqs = 0;
+        P.H = H;
+        P.status = a[0].status;
+        for (int i = 0; i < n; ++i) {
+            const long long lo = std::max(base, first[i]), hi = std::min(end, first[i] + a[i].num_seqs);
+            if (lo >= hi) continue;
+            Prob R = pr[i];
+            R.seq_base = (int)(lo - first[i]);
+            R.num_seqs = (int)(hi - lo);
+            P.pr[P.nprob++] = R;
+            P.num_seqs += R.num_seqs;
+        }
+        if (P.nprob == 0) continue;
+        if (P.nprob < MAX_PROBLEMS) P.pr[1] = P.pr[0];   // never read: keeps the struct defined
+        const cudaError_t e = dispatch(P, a[0].dtype, a[0].head_dim, sms, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &size_plan, cudaStream_t stream)
+{
+    return launch_paged_decode_multi(&a, &size_plan, 1, stream);
 }
 
 }  // namespace pka

@@ -15,6 +15,59 @@ int elt_bytes(pka_dtype d) { return d == PKA_F32 ? 4 : 2; }
 
 pka_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA; }
 
+// Every check of one decode problem, in the order the single-problem entry
+// points apply them; on PKA_OK fills the launch arguments (a.num_seqs == 0:
+// nothing to launch).
+pka_status prepare_decode(const pka_decode_problem &p, int block_size, int num_heads, int head_dim,
+                          pka_dtype dtype, int32_t *status, pka::DecodeArgs &a, pka::DecodePlan &plan)
+{
+    if (p.bias_table) {
+        if (p.attn_bias || p.num_buckets < 1 || num_heads < 1) return PKA_ERR_INVALID_ARG;
+        if ((long long)num_heads * p.num_buckets > PKA_MAX_BIAS_TABLE) return PKA_ERR_UNSUPPORTED;
+        if (!aligned(p.bias_table, 4)) return PKA_ERR_INVALID_ARG;
+    }
+    if (p.num_seqs < 0 || num_heads < 1 || p.max_blocks_per_seq < 1 || p.num_blocks < 1 || p.max_context_len < 0 ||
+        !dtype_ok(dtype) || !std::isfinite(p.scale))
+        return PKA_ERR_INVALID_ARG;
+    if (p.sliding_window != -1 && p.sliding_window < 1) return PKA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PKA_ERR_UNSUPPORTED;
+    if (block_size != 16) return PKA_ERR_UNSUPPORTED;
+    if ((long long)p.max_context_len > (long long)p.max_blocks_per_seq * block_size) return PKA_ERR_INVALID_ARG;
+    if (p.attn_bias && (p.bias_row_stride < p.max_context_len || p.bias_row_stride < 1)) return PKA_ERR_INVALID_ARG;
+    a.num_seqs = 0;
+    if (p.num_seqs == 0) return PKA_OK;
+    if (!p.out || !p.q || !p.k_cache || !p.v_cache || !p.block_tables || !p.context_lens) return PKA_ERR_INVALID_ARG;
+    if (!aligned(p.out, 16) || !aligned(p.q, 16) || !aligned(p.k_cache, 16) || !aligned(p.v_cache, 16) ||
+        !aligned(p.block_tables, 4) || !aligned(p.context_lens, 4) || !aligned(p.attn_bias, 4) ||
+        !aligned(status, 4))
+        return PKA_ERR_INVALID_ARG;
+    plan = pka::decode_plan(p.max_context_len, p.sliding_window, block_size);
+    const size_t need = pka::decode_workspace_bytes(p.num_seqs, num_heads, head_dim, plan);
+    if (!p.workspace || !aligned(p.workspace, 256) || p.workspace_bytes < need) return PKA_ERR_WORKSPACE;
+    a.out = p.out;
+    a.q = p.q;
+    a.k_cache = p.k_cache;
+    a.v_cache = p.v_cache;
+    a.block_tables = p.block_tables;
+    a.context_lens = p.context_lens;
+    a.bias = p.attn_bias;
+    a.bias_table = p.bias_table;
+    a.num_buckets = p.bias_table ? p.num_buckets : 0;
+    a.status = status;
+    a.scale = p.scale;
+    a.window = p.sliding_window;
+    a.num_seqs = p.num_seqs;
+    a.num_heads = num_heads;
+    a.head_dim = head_dim;
+    a.max_blocks_per_seq = p.max_blocks_per_seq;
+    a.num_blocks = p.num_blocks;
+    a.max_context_len = p.max_context_len;
+    a.bias_row_stride = p.attn_bias ? p.bias_row_stride : 0;
+    a.dtype = dtype;
+    a.workspace = p.workspace;
+    return PKA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -68,45 +121,13 @@ pka_status pka_paged_attn_decode(void *out, const void *q, const void *k_cache, 
                                  int max_context_len, pka_dtype dtype, void *workspace,
                                  size_t workspace_bytes, int32_t *status, void *stream)
 {
-    if (num_seqs < 0 || num_heads < 1 || max_blocks_per_seq < 1 || num_blocks < 1 || max_context_len < 0 ||
-        !dtype_ok(dtype) || !std::isfinite(scale))
-        return PKA_ERR_INVALID_ARG;
-    if (sliding_window != -1 && sliding_window < 1) return PKA_ERR_INVALID_ARG;
-    if (head_dim != 64 && head_dim != 128) return PKA_ERR_UNSUPPORTED;
-    if (block_size != 16) return PKA_ERR_UNSUPPORTED;
-    if ((long long)max_context_len > (long long)max_blocks_per_seq * block_size) return PKA_ERR_INVALID_ARG;
-    if (attn_bias && (bias_row_stride < max_context_len || bias_row_stride < 1)) return PKA_ERR_INVALID_ARG;
-    if (num_seqs == 0) return PKA_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKA_ERR_INVALID_ARG;
-    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(attn_bias, 4) ||
-        !aligned(status, 4))
-        return PKA_ERR_INVALID_ARG;
-    const pka::DecodePlan plan = pka::decode_plan(max_context_len, sliding_window, block_size);
-    const size_t need = pka::decode_workspace_bytes(num_seqs, num_heads, head_dim, plan);
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PKA_ERR_WORKSPACE;
+    const pka_decode_problem p = {out, q, k_cache, v_cache, block_tables, context_lens, attn_bias, nullptr, 0,
+                                  sliding_window, scale, num_seqs, max_blocks_per_seq, bias_row_stride,
+                                  num_blocks, max_context_len, workspace, workspace_bytes};
     pka::DecodeArgs a;
-    a.out = out;
-    a.q = q;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
-    a.block_tables = block_tables;
-    a.context_lens = context_lens;
-    a.bias = attn_bias;
-    a.bias_table = nullptr;
-    a.num_buckets = 0;
-    a.status = status;
-    a.scale = scale;
-    a.window = sliding_window;
-    a.num_seqs = num_seqs;
-    a.num_heads = num_heads;
-    a.head_dim = head_dim;
-    a.max_blocks_per_seq = max_blocks_per_seq;
-    a.num_blocks = num_blocks;
-    a.max_context_len = max_context_len;
-    a.bias_row_stride = attn_bias ? bias_row_stride : 0;
-    a.dtype = dtype;
-    a.workspace = workspace;
+    pka::DecodePlan plan;
+    const pka_status st = prepare_decode(p, block_size, num_heads, head_dim, dtype, status, a, plan);
+    if (st != PKA_OK || a.num_seqs == 0) return st;
     return from_cuda(pka::launch_paged_decode(a, plan, static_cast<cudaStream_t>(stream)));
 }
 
@@ -117,41 +138,49 @@ pka_status pka_paged_attn_decode_t5bias(void *out, const void *q, const void *k_
                                         int max_blocks_per_seq, int num_blocks, int max_context_len, pka_dtype dtype,
                                         void *workspace, size_t workspace_bytes, int32_t *status, void *stream)
 {
-    if (!bias_table || num_buckets < 1 || num_heads < 1 || (long long)num_heads * num_buckets > PKA_MAX_BIAS_TABLE)
-        return num_buckets >= 1 && num_heads >= 1 && bias_table ? PKA_ERR_UNSUPPORTED : PKA_ERR_INVALID_ARG;
-    if (!aligned(bias_table, 4)) return PKA_ERR_INVALID_ARG;
-    // every other argument is checked exactly as for the materialised-bias call
-    const pka_status probe = pka_paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, nullptr,
-                                                   sliding_window, scale, block_size, num_seqs, num_heads, head_dim,
-                                                   max_blocks_per_seq, 0, num_blocks, max_context_len, dtype,
-                                                   nullptr, 0, status, stream);
-    if (probe != PKA_ERR_WORKSPACE) return probe;
-    const pka::DecodePlan plan = pka::decode_plan(max_context_len, sliding_window, block_size);
-    const size_t need = pka::decode_workspace_bytes(num_seqs, num_heads, head_dim, plan);
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PKA_ERR_WORKSPACE;
+    if (!bias_table) return PKA_ERR_INVALID_ARG;
+    const pka_decode_problem p = {out, q, k_cache, v_cache, block_tables, context_lens, nullptr, bias_table,
+                                  num_buckets, sliding_window, scale, num_seqs, max_blocks_per_seq, 0,
+                                  num_blocks, max_context_len, workspace, workspace_bytes};
     pka::DecodeArgs a;
-    a.out = out;
-    a.q = q;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
-    a.block_tables = block_tables;
-    a.context_lens = context_lens;
-    a.bias = nullptr;
-    a.bias_table = bias_table;
-    a.num_buckets = num_buckets;
-    a.status = status;
-    a.scale = scale;
-    a.window = sliding_window;
-    a.num_seqs = num_seqs;
-    a.num_heads = num_heads;
-    a.head_dim = head_dim;
-    a.max_blocks_per_seq = max_blocks_per_seq;
-    a.num_blocks = num_blocks;
-    a.max_context_len = max_context_len;
-    a.bias_row_stride = 0;
-    a.dtype = dtype;
-    a.workspace = workspace;
+    pka::DecodePlan plan;
+    const pka_status st = prepare_decode(p, block_size, num_heads, head_dim, dtype, status, a, plan);
+    if (st != PKA_OK || a.num_seqs == 0) return st;
     return from_cuda(pka::launch_paged_decode(a, plan, static_cast<cudaStream_t>(stream)));
+}
+
+pka_status pka_paged_attn_decode_multi(const pka_decode_problem *problems, int num_problems, int block_size,
+                                       int num_heads, int head_dim, pka_dtype dtype, int32_t *status, void *stream)
+{
+    if (!problems || num_problems < 1) return PKA_ERR_INVALID_ARG;
+    if (num_problems > 2) return PKA_ERR_UNSUPPORTED;
+    pka::DecodeArgs a[2];
+    pka::DecodePlan plan[2];
+    size_t need[2] = {0, 0};
+    int n = 0;
+    for (int i = 0; i < num_problems; ++i) {
+        const pka_status st = prepare_decode(problems[i], block_size, num_heads, head_dim, dtype, status, a[n],
+                                             plan[n]);
+        if (st != PKA_OK) return st;
+        if (a[n].num_seqs == 0) continue;
+        need[n] = pka::decode_workspace_bytes(a[n].num_seqs, num_heads, head_dim, plan[n]);
+        ++n;
+    }
+    if (n == 2) {
+        auto overlap = [](const void *p, size_t pn, const void *q, size_t qn) {
+            const uintptr_t x = reinterpret_cast<uintptr_t>(p), y = reinterpret_cast<uintptr_t>(q);
+            return x < y + qn && y < x + pn;
+        };
+        const size_t out_bytes = (size_t)num_heads * head_dim * elt_bytes(dtype);
+        if (overlap(a[0].out, out_bytes * a[0].num_seqs, a[1].out, out_bytes * a[1].num_seqs))
+            return PKA_ERR_INVALID_ARG;
+        if (overlap(a[0].workspace, need[0], a[1].workspace, need[1])) return PKA_ERR_WORKSPACE;
+        if (a[0].bias_table && a[1].bias_table &&
+            (a[0].bias_table != a[1].bias_table || a[0].num_buckets != a[1].num_buckets))
+            return PKA_ERR_UNSUPPORTED;
+    }
+    if (n == 0) return PKA_OK;
+    return from_cuda(pka::launch_paged_decode_multi(a, plan, n, static_cast<cudaStream_t>(stream)));
 }
 
 pka_status pka_swa_prefill(void *out, const void *q, const void *k, const void *v, const int32_t *cu_seqlens,

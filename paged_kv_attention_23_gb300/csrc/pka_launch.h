@@ -46,6 +46,10 @@ struct DecodeArgs {
 
 cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
 
+// Up to two problems (same heads, head_dim and dtype, num_seqs >= 1 each) in
+// one grid; a.status of the first problem is the status word of the launch.
+cudaError_t launch_paged_decode_multi(const DecodeArgs *a, const DecodePlan *plans, int n, cudaStream_t stream);
+
 // ---- sliding-window prefill ----------------------------------------------------
 struct PrefillArgs {
     void *out;

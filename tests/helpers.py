@@ -74,6 +74,20 @@ class GpuDecode:
                                           status=self.status)
         return self.out
 
+    def problem(self, mode="bias", workspace=None):
+        """This case as one problem of paged_attn_decode_multi; mode is
+        "bias" (materialised A), "t5" (in-kernel table) or "none"."""
+        import torch
+        c = self.case
+        pr = dict(out=self.out, q=self.q, k_cache=self.k_cache, v_cache=self.v_cache, block_tables=self.block_tables,
+                  context_lens=self.context_lens, sliding_window=c.window, scale=c.scale,
+                  max_context_len=c.max_context_len, workspace=workspace)
+        if mode == "bias":
+            pr["attn_bias"] = self.bias
+        elif mode == "t5":
+            pr["bias_table"] = torch.from_numpy(c.bias_table).to(self.q.device)
+        return pr
+
     def run(self, bias=True, window=None, workspace=None):
         c = self.case
         self.pka.paged_attn_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,

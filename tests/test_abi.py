@@ -111,3 +111,54 @@ def test_product_package_never_imports_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
                 assert "oracle.c" not in src and "liboracle" not in src, f
+
+
+def test_decode_problem_struct_matches_the_header(tmp_path):
+    """The binding's ctypes mirror of pka_decode_problem has the C layout:
+    compile a probe against include/pka.h with the host compiler."""
+    import subprocess
+    fields = [f[0] for f in pka.DecodeProblem._fields_]
+    src = tmp_path / "layout.c"
+    body = "".join(f'  printf("%zu ", offsetof(pka_decode_problem, {f}));\n' for f in fields)
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "pka.h"\nint main(void) {\n' + body +
+                   '  printf("%zu\\n", sizeof(pka_decode_problem));\n  return 0;\n}\n')
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = [int(x) for x in subprocess.check_output([str(exe)]).split()]
+    want = [getattr(pka.DecodeProblem, f).offset for f in fields] + [ctypes.sizeof(pka.DecodeProblem)]
+    assert got == want
+
+
+def test_multi_decode_argument_checks_need_no_gpu(lib):
+    f = lib.pka_paged_attn_decode_multi
+    P = pka.DecodeProblem
+
+    def prob(**kw):
+        d = dict(num_seqs=0, sliding_window=-1, scale=0.125, max_blocks_per_seq=4, num_blocks=8, max_context_len=64)
+        d.update(kw)
+        return P(**d)
+
+    arr = lambda *ps: (P * len(ps))(*ps)
+    assert f(None, 1, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
+    assert f(arr(prob()), 0, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
+    assert f(arr(prob(), prob(), prob()), 3, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_UNSUPPORTED
+    assert f(arr(prob(), prob()), 2, 16, 2, 64, 2, NULL, NULL) == pka.PKA_OK        # nothing to do
+    assert f(arr(prob(), prob(sliding_window=0)), 2, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
+    assert f(arr(prob()), 1, 16, 2, 96, 2, NULL, NULL) == pka.PKA_ERR_UNSUPPORTED
+    fake = 4096
+    both = dict(attn_bias=fake, bias_row_stride=64, bias_table=fake, num_buckets=4)
+    assert f(arr(prob(**both)), 1, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG   # bias and table
+    assert f(arr(prob(bias_table=fake, num_buckets=2000)), 1, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_UNSUPPORTED
+    bufs = dict(out=fake, q=fake, k_cache=fake, v_cache=fake, block_tables=fake, context_lens=fake)
+    assert f(arr(prob(num_seqs=1, **bufs)), 1, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_WORKSPACE
+    ws, wsb = 1 << 20, 1 << 16
+    two = arr(prob(num_seqs=1, workspace=ws, workspace_bytes=wsb, **bufs),
+              prob(num_seqs=1, workspace=ws + 512, workspace_bytes=wsb, **dict(bufs, out=fake * 2)))
+    assert f(two, 2, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_WORKSPACE                   # workspaces overlap
+    two = arr(prob(num_seqs=1, workspace=ws, workspace_bytes=wsb, **bufs),
+              prob(num_seqs=1, workspace=ws * 2, workspace_bytes=wsb, **bufs))
+    assert f(two, 2, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG                 # outputs overlap
+    two = arr(prob(num_seqs=1, workspace=ws, workspace_bytes=wsb, bias_table=fake, num_buckets=4, **bufs),
+              prob(num_seqs=1, workspace=ws * 2, workspace_bytes=wsb, bias_table=fake * 4, num_buckets=4,
+                   **dict(bufs, out=fake * 2)))
+    assert f(two, 2, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_UNSUPPORTED                 # two tables

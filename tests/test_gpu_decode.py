@@ -311,3 +311,81 @@ def test_t5_table_too_large_is_unsupported(cuda_lib):
     case.bias_table = np.zeros((2, 4000), dtype=np.float32)       # 8000 floats > the shared-memory cache
     with pytest.raises(cuda_lib.PkaError):
         g.run_t5()
+
+
+# ---------------------------------------------------------------------------
+# self- and cross-attention decode in one launch
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("self_mode", ["bias", "t5"])
+def test_multi_self_and_cross_parity(cuda_lib, self_mode):
+    """The T5-large-shaped step: decoder self-attention (T5 bias, materialised
+    or from the table) and encoder cross-attention (its own block table and
+    pool, encoder length 512, no bias) in one launch; each matches the oracle
+    and the single-problem call."""
+    sc, cc = synth.decode_workload(3), synth.cross_workload()
+    gs, gc = GpuDecode(sc, cuda_lib), GpuDecode(cc, cuda_lib)
+    cuda_lib.paged_attn_decode_multi([gs.problem(self_mode), gc.problem("none")], status=gs.status)
+    got_s, got_c = to_f64(gs.out, sc.dtype).copy(), to_f64(gc.out, cc.dtype).copy()
+    ref_s = oracle_decode_t5(sc) if self_mode == "t5" else oracle_decode(sc)
+    _check(got_s, ref_s, sc.dtype, "multi self")
+    _check(got_c, oracle_decode(cc), cc.dtype, "multi cross")
+    assert int(gs.status.item()) == 0
+    one_s = to_f64(gs.run_t5() if self_mode == "t5" else gs.run(), sc.dtype)
+    assert max_err(got_s, one_s) <= TOL[sc.dtype]
+
+
+@pytest.mark.parametrize("dtype,D", [(F32, 128), (F16, 64)])
+def test_multi_spans_launch_boundary(cuda_lib, dtype, D):
+    """1300 sequences over two problems take two launches, the first holding
+    all of problem 0 and the head of problem 1; the problems differ in window,
+    bias, scale, pool and block-table width."""
+    a = synth.make_decode_case("multi-a", 71, dtype, 700, 2, D, ctx_range=(0, 70), bias="gauss", bias_stride=80,
+                               window=23, scale=0.3)
+    b = synth.make_decode_case("multi-b", 72, dtype, 600, 2, D, ctx_range=(1, 200), pool_blocks=5000,
+                               max_blocks_per_seq=16, scale=0.05)
+    ga, gb = GpuDecode(a, cuda_lib), GpuDecode(b, cuda_lib)
+    cuda_lib.paged_attn_decode_multi([ga.problem("bias"), gb.problem("none")], status=ga.status)
+    _check(to_f64(ga.out, dtype), oracle_decode(a), dtype, "problem 0")
+    _check(to_f64(gb.out, dtype), oracle_decode(b), dtype, "problem 1")
+    assert int(ga.status.item()) == 0
+
+
+def test_multi_empty_problem_and_both_tables(cuda_lib):
+    """A problem with no sequences is skipped; two problems may share one T5
+    table, cached once."""
+    import torch
+    a = synth.decode_workload(2)
+    b = synth.make_decode_case("multi-c", 73, BF16, 17, 8, 64, ctx_range=(1, 300))
+    b.bias_table = a.bias_table
+    ga, gb = GpuDecode(a, cuda_lib), GpuDecode(b, cuda_lib)
+    pa, pb = ga.problem("t5"), gb.problem("t5")
+    pb["bias_table"] = pa["bias_table"]
+    cuda_lib.paged_attn_decode_multi([pa, pb], status=ga.status)
+    _check(to_f64(ga.out, BF16), oracle_decode_t5(a), BF16, "table problem 0")
+    _check(to_f64(gb.out, BF16), oracle_decode_t5(b), BF16, "table problem 1")
+    empty = dict(gb.problem("none"), out=gb.out[:0], q=gb.q[:0], block_tables=gb.block_tables[:0],
+                 context_lens=gb.context_lens[:0])
+    ga.out.zero_()
+    cuda_lib.paged_attn_decode_multi([empty, ga.problem("bias")], status=ga.status)
+    _check(to_f64(ga.out, BF16), oracle_decode(a), BF16, "after empty problem")
+    assert int(ga.status.item()) == 0
+
+
+def test_multi_rejects_bad_problem_sets(cuda_lib):
+    import torch
+    a, b = synth.decode_workload(2), synth.make_decode_case("multi-d", 74, BF16, 5, 8, 64)
+    ga, gb = GpuDecode(a, cuda_lib), GpuDecode(b, cuda_lib)
+    with pytest.raises(cuda_lib.PkaError, match="UNSUPPORTED"):          # three problems
+        cuda_lib.paged_attn_decode_multi([ga.problem("none"), gb.problem("none"), gb.problem("none")])
+    with pytest.raises(cuda_lib.PkaError, match="INVALID_ARG"):          # overlapping outputs
+        cuda_lib.paged_attn_decode_multi([ga.problem("none"), dict(gb.problem("none"), out=ga.out[:5])])
+    ws = torch.zeros(1 << 22, dtype=torch.uint8, device="cuda")
+    with pytest.raises(cuda_lib.PkaError, match="WORKSPACE"):            # one workspace for both
+        cuda_lib.paged_attn_decode_multi([ga.problem("none", workspace=ws), gb.problem("none", workspace=ws)])
+    pa, pb = ga.problem("t5"), gb.problem("none")
+    pb["bias_table"] = pa["bias_table"].clone()
+    with pytest.raises(cuda_lib.PkaError, match="UNSUPPORTED"):          # two different tables
+        cuda_lib.paged_attn_decode_multi([pa, pb])
+    with pytest.raises(ValueError):                                       # different head counts
+        c = synth.make_decode_case("multi-e", 75, BF16, 3, 4, 64)
+        cuda_lib.paged_attn_decode_multi([ga.problem("none"), GpuDecode(c, cuda_lib).problem("none")])
