@@ -23,6 +23,15 @@ Functions and the passages they follow:
 * ``prefill_chunked`` — keys restricted to the query's own chunk of C
   positions, bidirectional or causal (the chunked local attention layers the
   same page discusses).
+* ``prefill_biased`` — ``prefill`` with an additive relative-position bias
+  rel_bias[h, B-1 + clamp(r - c, -(B-1), B-1)] inside the scaled logits: the
+  T5 bias of an encoder's bidirectional self-attention ("Add Encoder-decoder
+  model support and T5 Model support"; capped distance as in the T5-bias
+  page).  A causal layer reads only the non-negative half = the decode table.
+* ``paged_prefill`` — prefill of each sequence's newest Lq tokens against its
+  ctx keys in the paged cache, read through the block table passed in (same
+  encoder-decoder page: prefill and decode kernels both read the separate
+  cross-attention blocks); query row r sits at key position ctx - Lq + r.
 * ``reshape_and_cache`` — the plain scatter of new K/V rows into cache blocks
   (the cross-attention KV caching step named in "Add Encoder-decoder model
   support and T5 Model support").
@@ -73,6 +82,12 @@ def _load():
         lib.oracle_prefill_chunked.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_double, I, P,
                                                ctypes.c_longlong, I]
         lib.oracle_prefill_chunked.restype = None
+        lib.oracle_prefill_biased.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_double, I, P, I, P,
+                                              ctypes.c_longlong, I]
+        lib.oracle_prefill_biased.restype = None
+        lib.oracle_paged_prefill.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double, P, I, I,
+                                             P, ctypes.c_longlong, I]
+        lib.oracle_paged_prefill.restype = None
         lib.oracle_reshape_and_cache.argtypes = [P, P, P, P, P, ctypes.c_longlong, I, I, I, I]
         lib.oracle_reshape_and_cache.restype = None
         lib.oracle_widen.argtypes = [P, ctypes.c_longlong, I]
@@ -165,6 +180,46 @@ def prefill_chunked(q, k, v, cu_seqlens, chunk, causal, scale, dtype, rows=None,
     lib.oracle_prefill_chunked(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, H, D, int(chunk),
                                int(causal), float(scale), int(dtype), _ptr(rr), nr,
                                int(nthreads or default_threads()))
+    return out
+
+
+def prefill_biased(q, k, v, cu_seqlens, window, causal, scale, dtype, rel_bias, rows=None,
+                   nthreads=None) -> np.ndarray:
+    """Prefill with the relative-position bias rel_bias [H, 2B-1]:
+    x = scale * (q.k + rel_bias[h, B-1 + clamp(r - c, -(B-1), B-1)])."""
+    lib = _load()
+    q = _c(q); k = _c(k); v = _c(v)
+    cu = _c(cu_seqlens, np.int32)
+    rb = _c(rel_bias, np.float32)
+    T, H, D = q.shape
+    assert rb.shape[0] == H and rb.shape[1] % 2 == 1
+    rr = _c(rows, np.int64) if rows is not None else None
+    nr = len(rr) if rr is not None else int(cu[-1])
+    out = np.zeros((nr, H, D), dtype=np.float64)
+    lib.oracle_prefill_biased(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, H, D, int(window),
+                              int(causal), float(scale), int(dtype), _ptr(rb), (rb.shape[1] + 1) // 2, _ptr(rr), nr,
+                              int(nthreads or default_threads()))
+    return out
+
+
+def paged_prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, context_lens, window, causal, scale, block_size,
+                  dtype, rel_bias=None, rows=None, nthreads=None) -> np.ndarray:
+    """Prefill of each sequence's last Lq tokens against its ctx paged keys:
+    query row r at key position ctx - Lq + r.  [T or len(rows), H, D] double."""
+    lib = _load()
+    q = _c(q); kc = _c(k_cache); vc = _c(v_cache)
+    bt = _c(block_tables, np.int32)
+    cu = _c(cu_seqlens_q, np.int32)
+    cl = _c(context_lens, np.int32)
+    rb = _c(rel_bias, np.float32) if rel_bias is not None else None
+    T, H, D = q.shape
+    rr = _c(rows, np.int64) if rows is not None else None
+    nr = len(rr) if rr is not None else int(cu[-1])
+    out = np.zeros((nr, H, D), dtype=np.float64)
+    lib.oracle_paged_prefill(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(cu), _ptr(cl), len(cu) - 1, H, D,
+                             int(block_size), bt.shape[1], int(window), int(causal), float(scale), _ptr(rb),
+                             (rb.shape[1] + 1) // 2 if rb is not None else 0, int(dtype), _ptr(rr), nr,
+                             int(nthreads or default_threads()))
     return out
 
 

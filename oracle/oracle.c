@@ -44,6 +44,31 @@
  *   oracle_prefill_chunked — the same with keys restricted to the query's
  *     own chunk of `chunk` positions (chunked local attention, same page).
  *
+ *   oracle_prefill_biased — oracle_prefill with an additive relative-position
+ *     bias inside the softmax, x = scale * (q . k + A) as in the formula above,
+ *     where A depends only on the signed distance d = r - c between the query
+ *     and key positions and saturates at num_buckets - 1 in either direction:
+ *         A[h, r, c] = rel_bias[h, (num_buckets - 1) + clamp(d, -(num_buckets - 1), num_buckets - 1)]
+ *     rel_bias is [H, 2 * num_buckets - 1].  This is the T5 bias of an
+ *     encoder's bidirectional self-attention ("Add Encoder-decoder model
+ *     support and T5 Model support": T5 adds a custom bias in its attention;
+ *     "PagedAttention: Support custom attention bias for T5 model (1/2)": the
+ *     distance is capped and larger distances reuse the last value).  A causal
+ *     layer only reads the non-negative half, which is the decode table.
+ *
+ *   oracle_paged_prefill — prefill of the newest tokens of each sequence
+ *     against keys held in the paged cache ("Add Encoder-decoder model
+ *     support and T5 Model support": prompt and generated tokens keep their KV
+ *     blocks apart, and prefill as well as decode kernels read cross-attention
+ *     keys through their block table).  Sequence s has Lq_s query rows
+ *     (cu_seqlens_q) and ctx_s keys (context_lens) behind block-table row s;
+ *     query row r sits at key position p = ctx_s - Lq_s + r (the queries are
+ *     the last Lq_s tokens, already written to the cache).  The mask is
+ *     oracle_prefill's with r replaced by p and keys c in [0, ctx_s); the
+ *     optional bias is oracle_prefill_biased's with d = p - c.  With
+ *     causal = 0 and no window or bias, p plays no part: every query attends
+ *     to all ctx_s keys (a decoder prompt's cross-attention to the encoder).
+ *
  *   oracle_reshape_and_cache — the plain scatter of token rows into cache
  *     blocks, cache[slot / bs, h, slot % bs, :] = key[t, h, :]; slot < 0 skips
  *     the token.  Byte copies, so the result is exact.
@@ -260,7 +285,20 @@ struct prefill_ctx {
     int num_seqs, num_heads, head_dim, window, causal, dtype;
     double scale;
     int chunk;                  /* > 0: keys only from the query's own chunk of this many positions */
+    const float *rel_bias;      /* optional [H, 2 * num_buckets - 1] relative-position bias */
+    int num_buckets;
 };
+
+/* The relative-position bias for a query d positions after its key (d < 0:
+ * before it); distances beyond num_buckets - 1 either way reuse the end
+ * columns. */
+static double rel_term(const float *rel_bias, int num_buckets, int h, int d)
+{
+    const int cap = num_buckets - 1;
+    if (d > cap) d = cap;
+    if (d < -cap) d = -cap;
+    return (double)rel_bias[(size_t)h * (2 * num_buckets - 1) + cap + d];
+}
 
 static int mask_keeps(int r, int c, int window, int causal, int chunk)
 {
@@ -297,7 +335,8 @@ static void prefill_item(long long item, void *p)
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
             dot += load_elem(c->q, qoff + d, c->dtype) * load_elem(c->k, row + d, c->dtype);
-        x[n] = c->scale * dot;
+        const double bias = c->rel_bias ? rel_term(c->rel_bias, c->num_buckets, h, r - col) : 0.0;
+        x[n] = c->scale * (dot + bias);
         vrow[n] = row;
         ++n;
     }
@@ -314,7 +353,7 @@ void oracle_prefill(double *out, const void *q, const void *k, const void *v,
                     const int64_t *rows, long long num_rows, int nthreads)
 {
     struct prefill_ctx c = {out, q, k, v, cu_seqlens, rows, num_seqs, num_heads, head_dim,
-                            window, causal, dtype, scale, 0};
+                            window, causal, dtype, scale, 0, NULL, 0};
     long long nr = rows ? num_rows : (long long)cu_seqlens[num_seqs];
     run_items(prefill_item, &c, nr * num_heads, nthreads);
 }
@@ -330,9 +369,84 @@ void oracle_prefill_chunked(double *out, const void *q, const void *k, const voi
                             const int64_t *rows, long long num_rows, int nthreads)
 {
     struct prefill_ctx c = {out, q, k, v, cu_seqlens, rows, num_seqs, num_heads, head_dim,
-                            -1, causal, dtype, scale, chunk};
+                            -1, causal, dtype, scale, chunk, NULL, 0};
     long long nr = rows ? num_rows : (long long)cu_seqlens[num_seqs];
     run_items(prefill_item, &c, nr * num_heads, nthreads);
+}
+
+/* Prefill with the relative-position bias A[h, r, c] = rel_bias[h, cap +
+ * clamp(r - c, -cap, cap)], cap = num_buckets - 1, added to q . k before the
+ * scale (the T5 bias of an encoder's self-attention). */
+void oracle_prefill_biased(double *out, const void *q, const void *k, const void *v,
+                           const int32_t *cu_seqlens, int num_seqs, int num_heads, int head_dim,
+                           int window, int causal, double scale, int dtype, const float *rel_bias,
+                           int num_buckets, const int64_t *rows, long long num_rows, int nthreads)
+{
+    struct prefill_ctx c = {out, q, k, v, cu_seqlens, rows, num_seqs, num_heads, head_dim,
+                            window, causal, dtype, scale, 0, rel_bias, num_buckets};
+    long long nr = rows ? num_rows : (long long)cu_seqlens[num_seqs];
+    run_items(prefill_item, &c, nr * num_heads, nthreads);
+}
+
+/* ---- prefill against the paged cache -------------------------------------- */
+
+struct paged_prefill_ctx {
+    double *out;
+    const void *q, *k_cache, *v_cache;
+    const int32_t *cu_seqlens_q, *context_lens, *block_tables;
+    const float *rel_bias;
+    const int64_t *rows;
+    int num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq, window, causal, num_buckets, dtype;
+    double scale;
+};
+
+static void paged_prefill_item(long long item, void *p)
+{
+    const struct paged_prefill_ctx *c = (const struct paged_prefill_ctx *)p;
+    const int H = c->num_heads, D = c->head_dim, bs = c->block_size;
+    const long long row_i = item / H;
+    const int h = (int)(item % H);
+    const long long i = c->rows ? c->rows[row_i] : row_i;
+    int b = 0;
+    while (b + 1 <= c->num_seqs && c->cu_seqlens_q[b + 1] <= i) ++b;
+    const int Lq = c->cu_seqlens_q[b + 1] - c->cu_seqlens_q[b];
+    const int ctx = c->context_lens[b];
+    const int pos = ctx - Lq + (int)(i - c->cu_seqlens_q[b]);   /* the query's own key position */
+    double *o = c->out + (size_t)item * D;
+    double *x = (double *)malloc(sizeof(double) * (ctx > 0 ? ctx : 1));
+    size_t *vrow = (size_t *)malloc(sizeof(size_t) * (ctx > 0 ? ctx : 1));
+    int n = 0;
+    const size_t qoff = ((size_t)i * H + h) * D;
+    for (int col = 0; col < ctx; ++col) {
+        if (!mask_keeps(pos, col, c->window, c->causal, 0)) continue;
+        const int32_t blk = c->block_tables[(size_t)b * c->max_blocks_per_seq + col / bs];
+        const size_t row = (((size_t)blk * H + h) * bs + (col % bs)) * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += load_elem(c->q, qoff + d, c->dtype) * load_elem(c->k_cache, row + d, c->dtype);
+        const double bias = c->rel_bias ? rel_term(c->rel_bias, c->num_buckets, h, pos - col) : 0.0;
+        x[n] = c->scale * (dot + bias);
+        vrow[n] = row;
+        ++n;
+    }
+    softmax_combine(o, x, vrow, n, c->v_cache, c->dtype, D);
+    free(x);
+    free(vrow);
+}
+
+/* out: double [num_rows, H, D] for the listed query rows (rows == NULL: all
+ * cu_seqlens_q[num_seqs] rows in order). */
+void oracle_paged_prefill(double *out, const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_tables, const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                          int num_seqs, int num_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                          int window, int causal, double scale, const float *rel_bias, int num_buckets, int dtype,
+                          const int64_t *rows, long long num_rows, int nthreads)
+{
+    struct paged_prefill_ctx c = {out, q, k_cache, v_cache, cu_seqlens_q, context_lens, block_tables,
+                                  rel_bias, rows, num_seqs, num_heads, head_dim, block_size,
+                                  max_blocks_per_seq, window, causal, num_buckets, dtype, scale};
+    long long nr = rows ? num_rows : (long long)cu_seqlens_q[num_seqs];
+    run_items(paged_prefill_item, &c, nr * num_heads, nthreads);
 }
 
 /* ---- reshape_and_cache --------------------------------------------------- */

@@ -319,6 +319,7 @@ class PrefillCase:
     scale: float
     device_qkv: object = None
     chunk: int = 0                      # > 0: chunked local attention (window must be -1)
+    rel_bias: Optional[np.ndarray] = None   # f32 [H, 2B-1] signed relative-position bias, or None
 
     @property
     def num_seqs(self) -> int:
@@ -408,3 +409,139 @@ def chunked_prefill_workload(device: Optional[str] = None, seqlens=None) -> Pref
     c = make_prefill_case("chunked-prefill-c1024", 1004 * 10 + 9, seqlens, 12, 64, -1, 1, BF16, 1 / 8, device)
     c.chunk = CHUNKED_PREFILL_CHUNK
     return c
+
+
+# --------------------------------------------------------------------------
+# relative-position bias and prefill against the paged cache
+# --------------------------------------------------------------------------
+def rel_bias_table(seed: int, num_heads: int, buckets: int = T5_MAX_DISTANCE + 1) -> np.ndarray:
+    """A seeded N(0,1) signed relative-position table [H, 2*buckets - 1]:
+    column buckets-1+d holds the bias of a query d positions after its key."""
+    rng = np.random.default_rng(seed * 131 + 3)
+    return rng.standard_normal((num_heads, 2 * buckets - 1), dtype=np.float32)
+
+
+@dataclasses.dataclass
+class PagedPrefillCase:
+    """Prefill of each sequence's newest query tokens against its keys in the
+    paged cache.  ``cache`` holds the keys/values of all ctx_s positions (token
+    arrays, slot mapping, block tables); the queries are the last Lq_s
+    positions, packed [Tq, H, D] by ``cu_seqlens_q``."""
+    name: str
+    cache: DecodeCase
+    cu_seqlens_q: np.ndarray            # int32 [S+1]
+    q: Optional[np.ndarray]             # storage [Tq, H, D] (None when drawn on device)
+    window: int
+    causal: int
+    scale: float
+    rel_bias: Optional[np.ndarray] = None
+    device_q: object = None
+
+    @property
+    def dtype(self) -> int:
+        return self.cache.dtype
+
+    @property
+    def num_heads(self) -> int:
+        return self.cache.num_heads
+
+    @property
+    def head_dim(self) -> int:
+        return self.cache.head_dim
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.cu_seqlens_q) - 1
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.cu_seqlens_q[-1])
+
+    @property
+    def query_lens(self) -> np.ndarray:
+        return np.diff(self.cu_seqlens_q).astype(np.int64)
+
+    @property
+    def max_query_len(self) -> int:
+        return int(self.query_lens.max()) if self.num_seqs else 0
+
+    def kept_pairs(self) -> int:
+        """(query, key) pairs the mask keeps, summed over sequences."""
+        total = 0
+        for Lq, ctx in zip(self.query_lens, self.cache.context_lens.astype(np.int64)):
+            if Lq == 0 or ctx == 0:
+                continue
+            p = ctx - Lq + np.arange(Lq)
+            lo = np.zeros(Lq, dtype=np.int64)
+            hi = np.full(Lq, ctx, dtype=np.int64)
+            if self.window > 0:
+                lo = np.maximum(lo, p - self.window + 1)
+                if not self.causal:
+                    hi = np.minimum(hi, p + self.window)
+            if self.causal:
+                hi = np.minimum(hi, p + 1)
+            total += int(np.maximum(hi - lo, 0).sum())
+        return total
+
+
+def make_paged_prefill_case(name: str, seed: int, dtype: int, context_lens, query_lens, num_heads: int,
+                            head_dim: int, window: int = -1, causal: int = 1, rel_buckets: int = 0,
+                            scale: Optional[float] = None, pool_blocks: Optional[int] = None,
+                            max_blocks_per_seq: Optional[int] = None, device: Optional[str] = None,
+                            cache: Optional[DecodeCase] = None) -> PagedPrefillCase:
+    """Draw the paged keys (or take ``cache``), then the queries of the last
+    query_lens[s] positions of each sequence, then the bias table."""
+    context_lens = np.asarray(context_lens, dtype=np.int32)
+    query_lens = np.asarray(query_lens, dtype=np.int64)
+    H, D = num_heads, head_dim
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if cache is None:
+        cache = make_decode_case(name, seed, dtype, len(context_lens), H, D, context_lens=context_lens,
+                                 pool_blocks=pool_blocks, window=window, scale=scale, device=device,
+                                 max_blocks_per_seq=max_blocks_per_seq)
+    cu = np.zeros(len(query_lens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(query_lens)
+    Tq = int(cu[-1])
+    q = dq = None
+    if device is None:
+        q = encode(np.random.default_rng(seed * 31 + 5).standard_normal((Tq, H, D), dtype=np.float32), dtype)
+    else:
+        import torch
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 7919 + 41)
+        tdt = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}[dtype]
+        dq = torch.randn((Tq, H, D), generator=g, device=device, dtype=torch.float32).to(tdt)
+    rel = rel_bias_table(seed, H, rel_buckets) if rel_buckets > 0 else None
+    return PagedPrefillCase(name, cache, cu, q, window, causal, float(scale), rel, dq)
+
+
+def t5_encoder_prefill_workload(device: Optional[str] = None, num_seqs: int = 256,
+                                enc_len: int = 512) -> PrefillCase:
+    """T5-large-shaped encoder self-attention: 256 sequences x 512 tokens
+    (the encoder length of the cross-attention decode workload), 16 heads x
+    64, bf16, bidirectional, T5 relative-position bias [16, 257] (distance
+    capped at 128 either way), scale 1/8."""
+    c = make_prefill_case("t5-encoder-prefill", 1004 * 10 + 21, np.full(num_seqs, enc_len), 16, 64, -1, 0, BF16,
+                          1 / 8, device)
+    c.rel_bias = rel_bias_table(1004 * 10 + 21, 16)
+    return c
+
+
+def t5_paged_prefill_workload(device: Optional[str] = None, num_seqs: Optional[int] = None):
+    """A prompt chunk of each sequence of the T5-large-shaped decode workload
+    through its block tables: the last Lq_s = min(ctx_s, U[1,256]) positions
+    query (a) the decoder self-attention cache (contexts U[1,2048], causal,
+    the T5 bias table's non-negative half) and (b) the encoder cross-attention
+    cache (encoder length 512, no bias, no mask).  Returns (self, cross)."""
+    sc = decode_workload(3, device=device, num_seqs=num_seqs)
+    cc = cross_workload(device=device, num_seqs=num_seqs)
+    rng = np.random.default_rng(1004 * 10 + 22)
+    ql = np.minimum(sc.context_lens, rng.integers(1, 257, size=sc.num_seqs)).astype(np.int64)
+    self_case = make_paged_prefill_case("t5-large-paged-prefill-self", 1004 * 10 + 22, BF16, sc.context_lens, ql,
+                                        16, 64, -1, 1, T5_MAX_DISTANCE + 1, 1 / 8, device=device, cache=sc)
+    cross_case = make_paged_prefill_case("t5-large-paged-prefill-cross", 1004 * 10 + 23, BF16, cc.context_lens,
+                                         ql, 16, 64, -1, 0, 0, 1 / 8, device=device, cache=cc)
+    # the cross-attention queries are the same prompt tokens
+    cross_case.q, cross_case.device_q = self_case.q, self_case.device_q
+    return self_case, cross_case

@@ -32,6 +32,13 @@ MUTANTS = {
     "t5_distance_off_by_one": ("int d = (ctx - 1) - j;", "int d = ctx - j;"),
     "chunk_boundary_shifted": ("if (chunk > 0 && r / chunk != c / chunk) return 0;",
                                "if (chunk > 0 && (r + 1) / chunk != (c + 1) / chunk) return 0;"),
+    "rel_bias_sign_flipped": ("rel_term(c->rel_bias, c->num_buckets, h, r - col)",
+                              "rel_term(c->rel_bias, c->num_buckets, h, col - r)"),
+    "rel_bias_clamp_off_by_one": ("if (d > cap) d = cap;", "if (d > cap - 1) d = cap - 1;"),
+    "paged_prefill_position_offset_dropped": ("const int pos = ctx - Lq + (int)(i - c->cu_seqlens_q[b]);",
+                                              "const int pos = (int)(i - c->cu_seqlens_q[b]);"),
+    "paged_prefill_bias_distance_reversed": ("rel_term(c->rel_bias, c->num_buckets, h, pos - col)",
+                                             "rel_term(c->rel_bias, c->num_buckets, h, col - pos)"),
 }
 
 
@@ -49,6 +56,12 @@ def _pin_suite():
     yield lambda: pins.test_reshape_and_cache_round_trip_and_skip(pins.F16)
     yield lambda: pins.test_t5_table_decode_equals_materialised_bias(-1, 129)
     yield pins.test_chunked_matches_bruteforce
+    yield pins.test_rel_bias_one_hot_selects_previous_key
+    yield pins.test_paged_rel_bias_one_hot_selects_key_before_the_query_position
+    yield pins.test_rel_bias_saturates_at_the_last_column
+    for causal in (0, 1):
+        yield lambda causal=causal: pins.test_paged_prefill_matches_bruteforce(7, causal, 129, pins.BF16)
+        yield lambda causal=causal: pins.test_biased_prefill_matches_bruteforce(9, causal, 5)
 
 
 def _build_mutant(name, tmpdir):
@@ -69,7 +82,7 @@ def test_pins_catch_planted_mistake(name, monkeypatch):
         so = _build_mutant(name, d)
         mut = ctypes.CDLL(so)
         for fn in ("oracle_paged_decode", "oracle_paged_decode_t5", "oracle_prefill", "oracle_prefill_chunked",
-                   "oracle_reshape_and_cache", "oracle_widen"):
+                   "oracle_prefill_biased", "oracle_paged_prefill", "oracle_reshape_and_cache", "oracle_widen"):
             getattr(mut, fn).argtypes = getattr(real, fn).argtypes
             getattr(mut, fn).restype = getattr(real, fn).restype
         monkeypatch.setattr(oracle, "_lib", mut)

@@ -509,3 +509,219 @@ def test_chunked_matches_bruteforce():
         ref[a:e] = np.einsum("hij,jhd->ihd", w, v[a:e])
     got = oracle.prefill_chunked(case.q, case.k, case.v, cu, C, 0, case.scale, BF16)
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# relative-position bias in prefill; prefill against the paged cache
+# ---------------------------------------------------------------------------
+def _rel_cols(rel, d):
+    """Columns of the signed table for distances d (any shape), saturated."""
+    cap = (rel.shape[1] - 1) // 2
+    return cap + np.clip(d, -cap, cap)
+
+
+def _softmax_rows(lg, keep, V):
+    """Masked softmax over the last axis of lg [H, n, m]; rows that keep no key
+    give zeros.  V: [m, H, D] -> [n, H, D]."""
+    lg = np.where(keep[None], lg, -np.inf)
+    m = lg.max(axis=2, keepdims=True)
+    m = np.where(np.isfinite(m), m, 0.0)
+    w = np.where(keep[None], np.exp(lg - m), 0.0)
+    tot = w.sum(axis=2, keepdims=True)
+    w = np.divide(w, tot, out=np.zeros_like(w), where=tot > 0)
+    return np.einsum("hij,jhd->ihd", w, V)
+
+
+def brute_prefill_biased(case):
+    q = synth.decode_to_f32(case.q, case.dtype).astype(np.float64)
+    k = synth.decode_to_f32(case.k, case.dtype).astype(np.float64)
+    v = synth.decode_to_f32(case.v, case.dtype).astype(np.float64)
+    rel = case.rel_bias.astype(np.float64)
+    out = np.zeros_like(q)
+    cu = case.cu_seqlens
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        if e == a:
+            continue
+        r = np.arange(e - a)[:, None]; c = np.arange(e - a)[None, :]
+        keep = np.ones((e - a, e - a), dtype=bool)
+        if case.causal:
+            keep &= c <= r
+        if case.window > 0:
+            keep &= np.abs(r - c) < case.window
+        lg = (np.einsum("ihd,jhd->hij", q[a:e], k[a:e]) + rel[:, _rel_cols(rel, r - c)]) * case.scale
+        out[a:e] = _softmax_rows(lg, keep, v[a:e])
+    return out
+
+
+def brute_paged_prefill(pc):
+    """From the token arrays (no block table): the last Lq positions of each
+    sequence against its ctx contiguous keys."""
+    c = pc.cache
+    q = synth.decode_to_f32(pc.q, pc.dtype).astype(np.float64)
+    K = synth.decode_to_f32(c.key, pc.dtype).astype(np.float64)
+    V = synth.decode_to_f32(c.value, pc.dtype).astype(np.float64)
+    out = np.zeros_like(q)
+    for s in range(pc.num_seqs):
+        a, e = int(pc.cu_seqlens_q[s]), int(pc.cu_seqlens_q[s + 1])
+        ctx = int(c.context_lens[s])
+        if e == a or ctx == 0:
+            continue
+        t0 = int(c.tok_offsets[s])
+        p = ctx - (e - a) + np.arange(e - a)[:, None]
+        col = np.arange(ctx)[None, :]
+        keep = np.ones((e - a, ctx), dtype=bool)
+        if pc.causal:
+            keep &= col <= p
+        if pc.window > 0:
+            keep &= np.abs(p - col) < pc.window
+        lg = np.einsum("ihd,jhd->hij", q[a:e], K[t0:t0 + ctx])
+        if pc.rel_bias is not None:
+            rel = pc.rel_bias.astype(np.float64)
+            lg = lg + rel[:, _rel_cols(rel, p - col)]
+        out[a:e] = _softmax_rows(lg * pc.scale, keep, V[t0:t0 + ctx])
+    return out
+
+
+def run_oracle_paged_prefill(pc, **kw):
+    kc, vc = fill_cache_numpy(pc.cache)
+    return oracle.paged_prefill(pc.q, kc, vc, pc.cache.block_tables, pc.cu_seqlens_q, pc.cache.context_lens,
+                                pc.window, pc.causal, pc.scale, pc.cache.block_size, pc.dtype, rel_bias=pc.rel_bias,
+                                **kw)
+
+
+def biased_case(seqlens, window, causal, buckets=5, dtype=BF16, seed=23):
+    case = synth.make_prefill_case("pin", seed, seqlens, 2, 64, window, causal, dtype)
+    case.rel_bias = synth.rel_bias_table(seed, 2, buckets)
+    return case
+
+
+def run_oracle_prefill_biased(case, **kw):
+    return oracle.prefill_biased(case.q, case.k, case.v, case.cu_seqlens, case.window, case.causal, case.scale,
+                                 case.dtype, case.rel_bias, **kw)
+
+
+PAGED_CTX = (1, 15, 16, 17, 40, 100, 130)
+PAGED_QL = (1, 15, 5, 17, 3, 60, 130)
+
+
+def paged_case(window=-1, causal=1, buckets=0, dtype=BF16, ctx=PAGED_CTX, ql=PAGED_QL, seed=29):
+    return synth.make_paged_prefill_case("pin", seed, dtype, ctx, ql, 2, 64, window, causal, buckets,
+                                         pool_blocks=40)
+
+
+@pytest.mark.parametrize("window", [-1, 1, 9, 200])
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("buckets", [1, 5, 129])
+def test_biased_prefill_matches_bruteforce(window, causal, buckets):
+    case = biased_case([1, 7, 70, 130], window, causal, buckets)
+    np.testing.assert_allclose(run_oracle_prefill_biased(case), brute_prefill_biased(case), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [-1, 1, 7, 300])
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("buckets", [0, 129])
+@pytest.mark.parametrize("dtype", [BF16, F32])
+def test_paged_prefill_matches_bruteforce(window, causal, buckets, dtype):
+    pc = paged_case(window, causal, buckets, dtype)
+    np.testing.assert_allclose(run_oracle_paged_prefill(pc), brute_paged_prefill(pc), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [-1, 3])
+def test_paged_prefill_more_queries_than_keys_and_empty_context(window):
+    """Without the causal mask a sequence may have more query rows than keys
+    (early rows sit at negative positions) or no keys at all (zero rows)."""
+    pc = paged_case(window, 0, 4, ctx=(5, 0, 30), ql=(9, 3, 4))
+    got = run_oracle_paged_prefill(pc)
+    np.testing.assert_allclose(got, brute_paged_prefill(pc), rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(got[9:12], 0.0)
+
+
+def test_rel_bias_one_hot_selects_previous_key():
+    """A huge bias at distance +1 only: every query r >= 1 returns v_{r-1}
+    exactly (a sign slip would return v_{r+1})."""
+    case = biased_case([12, 30], -1, 0, buckets=4, dtype=F32)
+    case.rel_bias[:] = 0
+    case.rel_bias[:, 3 + 1] = 1e4
+    case.scale = 1.0
+    got = run_oracle_prefill_biased(case)
+    v = synth.decode_to_f32(case.v, F32).astype(np.float64)
+    for a, e in zip(case.cu_seqlens[:-1], case.cu_seqlens[1:]):
+        np.testing.assert_array_equal(got[a + 1:e], v[a:e - 1])
+
+
+def test_paged_rel_bias_one_hot_selects_key_before_the_query_position():
+    """Paged and causal: with the huge bias at distance +1, query row r of a
+    sequence (position ctx - Lq + r) returns the value at position ctx - Lq + r - 1."""
+    pc = paged_case(-1, 1, 4, F32, ctx=(20, 37, 16), ql=(5, 37, 1))
+    pc.rel_bias[:] = 0
+    pc.rel_bias[:, 3 + 1] = 1e4
+    pc.scale = 1.0
+    got = run_oracle_paged_prefill(pc)
+    V = synth.decode_to_f32(pc.cache.value, F32).astype(np.float64)
+    for s in range(pc.num_seqs):
+        a, e = int(pc.cu_seqlens_q[s]), int(pc.cu_seqlens_q[s + 1])
+        ctx, t0 = int(pc.cache.context_lens[s]), int(pc.cache.tok_offsets[s])
+        for r in range(e - a):
+            p = ctx - (e - a) + r
+            if p >= 1:
+                np.testing.assert_array_equal(got[a + r], V[t0 + p - 1])
+
+
+def test_rel_bias_saturates_at_the_last_column():
+    """Zero query, bias b only in the saturated column (distance >= cap):
+    the weights take two values, split exactly at distance cap."""
+    B, cap, b = 4, 3, 1.5
+    case = biased_case([20], -1, 0, buckets=B, dtype=F32)
+    case.q[:] = 0
+    case.rel_bias[:] = 0
+    case.rel_bias[:, 2 * cap] = b
+    got = run_oracle_prefill_biased(case)
+    v = synth.decode_to_f32(case.v, F32).astype(np.float64)
+    for r in range(20):
+        wts = np.where(r - np.arange(20) >= cap, math.exp(b * case.scale), 1.0)
+        ref = np.einsum("j,jhd->hd", wts, v[:20]) / wts.sum()
+        np.testing.assert_allclose(got[r], ref, rtol=1e-13, atol=1e-13)
+
+
+def test_rel_bias_constant_shift_leaves_output():
+    case = biased_case([9, 50], 7, 0, buckets=6)
+    case.rel_bias = (np.round(case.rel_bias * 1024) / 1024).astype(np.float32)   # + 3 stays exact in f32
+    a = run_oracle_prefill_biased(case)
+    case.rel_bias = case.rel_bias + np.float32(3.0)
+    np.testing.assert_allclose(run_oracle_prefill_biased(case), a, rtol=0, atol=1e-12)
+
+
+def test_paged_prefill_of_whole_sequences_equals_packed_causal_prefill():
+    """Querying every position (Lq = ctx) through the block table is the
+    causal biased prefill over the contiguous tokens."""
+    ctx = (1, 16, 17, 90)
+    pc = paged_case(-1, 1, 7, ctx=ctx, ql=ctx)
+    got = run_oracle_paged_prefill(pc)
+    packed = synth.make_prefill_case("pin", 1, list(ctx), 2, 64, -1, 1, BF16, pc.scale)
+    packed.q, packed.k, packed.v, packed.rel_bias = pc.q, pc.cache.key, pc.cache.value, pc.rel_bias
+    np.testing.assert_allclose(got, run_oracle_prefill_biased(packed), rtol=0, atol=1e-13)
+
+
+def test_noncausal_paged_prefill_rows_are_paged_decodes():
+    """Without mask or bias, every query row is a decode over all ctx keys of
+    its sequence (a decoder prompt's cross-attention)."""
+    pc = paged_case(-1, 0, 0)
+    got = run_oracle_paged_prefill(pc)
+    seq = np.repeat(np.arange(pc.num_seqs), pc.query_lens)
+    kc, vc = fill_cache_numpy(pc.cache)
+    ref = oracle.paged_decode(pc.q, kc, vc, pc.cache.block_tables[seq], pc.cache.context_lens[seq], None, -1,
+                              pc.scale, 16, pc.dtype)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13)
+
+
+def test_causal_paged_prefill_last_rows_are_t5_decodes():
+    """The last query row of each sequence is the decode at position ctx-1
+    with the table's non-negative half as the T5 decode table."""
+    pc = paged_case(-1, 1, 129)
+    last = (pc.cu_seqlens_q[1:] - 1).astype(np.int64)
+    got = run_oracle_paged_prefill(pc, rows=last)
+    kc, vc = fill_cache_numpy(pc.cache)
+    ref = oracle.paged_decode_t5(pc.q[last], kc, vc, pc.cache.block_tables, pc.cache.context_lens,
+                                 np.ascontiguousarray(pc.rel_bias[:, 128:]), -1, pc.scale, 16, pc.dtype)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13)
