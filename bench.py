@@ -21,6 +21,13 @@ batch of seeded synthetic input, already resident in HBM:
         three layers: full, window 64, window 64 (bidirectional).
   chunked-prefill    the same sequences, one chunked-local layer (chunks of
         1024 positions, causal within the chunk).
+  t5-encoder-prefill T5-large-shaped encoder self-attention: 256 x 512 tokens,
+        16 heads x 64 bf16, bidirectional, T5 relative-position bias from a
+        [16, 257] table computed in the kernel.
+  t5-paged-prefill   a prompt chunk (the last min(ctx, U[1,256]) positions) of
+        every sequence of the t5-large-decode batch through the block tables:
+        its K/V written by reshape_and_cache, then causal + T5 bias over the
+        self-attention cache, and unmasked over the encoder cache.
 
 metric/unit: decode workloads report algorithmic KV+bias bytes per second
 (GB/s); the prefill workload reports TFLOP/s (4*D per kept (query, key) pair
@@ -487,29 +494,105 @@ def prefill_flops(case) -> int:
     return 4 * case.head_dim * case.num_heads * case.visible_pairs()
 
 
+PREFILL_WORKLOADS = ("encoder-prefill", "chunked-prefill", "t5-encoder-prefill", "t5-paged-prefill")
+
+
+class PrefillLaunch:
+    """One prefill call of a step: its device inputs, output and FLOPs.
+    ``host_inputs`` are the tensors a step copies from the host for e2e."""
+
+    def __init__(self, name, case, fn, out, flops, host_inputs, pre=None):
+        self.name, self.case, self.fn, self.out, self.flops = name, case, fn, out, flops
+        self.host_inputs = host_inputs
+        self.pre = pre               # work the step does before the call (reshape_and_cache of new K/V)
+
+    def __call__(self):
+        if self.pre is not None:
+            self.pre()
+        self.fn()
+
+
+def build_prefill_launches(args, pka, device):
+    import torch
+    w = args.workload
+    launches = []
+    if w in ("encoder-prefill", "chunked-prefill", "t5-encoder-prefill"):
+        if w == "chunked-prefill":
+            layers = [synth.chunked_prefill_workload(device=device)]
+        elif w == "t5-encoder-prefill":
+            layers = [synth.t5_encoder_prefill_workload(device=device)]
+        else:
+            layers = [synth.prefill_workload(l, device=device) for l in range(3)]
+        cu = torch.from_numpy(layers[0].cu_seqlens).to(device)
+        for c in layers:
+            q, k, v = c.device_qkv
+            out = torch.empty_like(q)
+            if c.rel_bias is not None:
+                rel = torch.from_numpy(c.rel_bias).to(device)
+                fn = (lambda c=c, q=q, k=k, v=v, out=out, rel=rel:
+                      pka.prefill_biased(out, q, k, v, cu, c.max_seqlen, rel, c.window, c.causal, c.scale))
+            elif c.chunk > 0:
+                fn = (lambda c=c, q=q, k=k, v=v, out=out:
+                      pka.chunked_prefill(out, q, k, v, cu, c.max_seqlen, c.chunk, c.causal, c.scale))
+            else:
+                fn = (lambda c=c, q=q, k=k, v=v, out=out:
+                      pka.swa_prefill(out, q, k, v, cu, c.max_seqlen, c.window, c.causal, c.scale))
+            launches.append(PrefillLaunch(c.name, c, fn, out, prefill_flops(c), [q, k, v, cu]))
+        return launches
+    # t5-paged-prefill: a prompt chunk of every sequence of the T5-large decode
+    # batch against the self-attention cache (its K/V written first) and the
+    # encoder cross-attention cache
+    self_c, cross_c = synth.t5_paged_prefill_workload(device=device)
+    q = self_c.device_q
+    cuq = torch.from_numpy(self_c.cu_seqlens_q).to(device)
+    for pc in (self_c, cross_c):
+        c = pc.cache
+        H, D = c.num_heads, c.head_dim
+        kc = torch.zeros((c.num_blocks, H, 16, D), dtype=torch.bfloat16, device=device)
+        vc = torch.zeros_like(kc)
+        key, value = c.device_kv
+        pka.reshape_and_cache(key, value, kc, vc, torch.from_numpy(c.slot_mapping).to(device))
+        bt = torch.from_numpy(np.ascontiguousarray(c.block_tables)).to(device)
+        cl = torch.from_numpy(c.context_lens).to(device)
+        rel = torch.from_numpy(pc.rel_bias).to(device) if pc.rel_bias is not None else None
+        out = torch.empty_like(q)
+        ins = [q, bt, cl, cuq] + ([rel] if rel is not None else [])
+        pre = None
+        if pc.causal:
+            # the chunk's own K/V rows: the last Lq positions of each sequence
+            qpos = np.concatenate([c.tok_offsets[s] + c.context_lens[s] - np.arange(l, 0, -1)
+                                   for s, l in enumerate(pc.query_lens)]).astype(np.int64)
+            idx = torch.from_numpy(qpos).to(device)
+            new_k, new_v = key[idx].contiguous(), value[idx].contiguous()
+            slots = torch.from_numpy(c.slot_mapping[qpos]).to(device)
+            pre = (lambda new_k=new_k, new_v=new_v, kc=kc, vc=vc, slots=slots:
+                   pka.reshape_and_cache(new_k, new_v, kc, vc, slots))
+            ins += [new_k, new_v, slots]
+        fn = (lambda pc=pc, out=out, kc=kc, vc=vc, bt=bt, cl=cl, rel=rel:
+              pka.paged_prefill(out, q, kc, vc, bt, cuq, cl, pc.max_query_len, pc.window, pc.causal, rel, pc.scale))
+        launches.append(PrefillLaunch(pc.name, pc, fn, out, 4 * D * H * pc.kept_pairs(), ins, pre))
+        del key, value
+        c.device_kv = None
+    torch.cuda.empty_cache()
+    return launches
+
+
 def run_prefill(args, rank, world, local, peaks):
     import torch
     import paged_kv_attention_23_gb300 as pka
     pka.load()
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    if args.workload == "chunked-prefill":
-        layers = [synth.chunked_prefill_workload(device=device)]
-    else:
-        layers = [synth.prefill_workload(l, device=device) for l in range(3)]
-    flops = [prefill_flops(c) for c in layers]
-    cu = torch.from_numpy(layers[0].cu_seqlens).to(device)
-    outs = [torch.empty_like(c.device_qkv[0]) for c in layers]
+    launches = build_prefill_launches(args, pka, device)
+    flops = [l.flops for l in launches]
 
     def step(events=None, k=0):
-        for j, c in enumerate(layers):
-            q, kk, v = c.device_qkv
+        for j, l in enumerate(launches):
+            if l.pre is not None:
+                l.pre()
             if events is not None:
                 events[j][0][k].record()
-            if c.chunk > 0:
-                pka.chunked_prefill(outs[j], q, kk, v, cu, c.max_seqlen, c.chunk, c.causal, c.scale)
-            else:
-                pka.swa_prefill(outs[j], q, kk, v, cu, c.max_seqlen, c.window, c.causal, c.scale)
+            l.fn()
             if events is not None:
                 events[j][1][k].record()
 
@@ -531,53 +614,72 @@ def run_prefill(args, rank, world, local, peaks):
     torch.cuda.synchronize(); barrier(world)
     clk = clocks.stop()
     ms_step = max_over_ranks(t0.elapsed_time(t1), world) / K
-    launch_ms = per_launch_ms(lambda ev: [step(ev, k) for k in range(K)], len(layers), K)
+    launch_ms = per_launch_ms(lambda ev: [step(ev, k) for k in range(K)], len(launches), K)
     value = sum(flops) * world / (ms_step * 1e-3) / 1e12
-    ach = flops[0] / (launch_ms[0] * 1e-3) / 1e12
+    jd = int(np.argmax(flops))
+    ach = flops[jd] / (launch_ms[jd] * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
-    qkv_bytes = [4 * c.num_tokens * c.num_heads * c.head_dim * 2 for c in layers]
+    cases = [l.case for l in launches]
+    packed = args.workload != "t5-paged-prefill"
+    qkv_bytes = [4 * c.num_tokens * c.num_heads * c.head_dim * 2 for c in cases]
+    kname = {"t5-paged-prefill": "paged_prefill (self-attention, causal + T5 bias)",
+             "t5-encoder-prefill": "prefill_biased (T5 encoder layer)"}.get(args.workload,
+                                                                         "swa_prefill (full-attention layer)")
     roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
             "frac": round(ach / peak, 4), "traffic": recorded_traffic("swa_prefill.cu", args.workload),
-            "kernel": "swa_prefill (full-attention layer)", "alg_flops_per_launch": flops[0],
-            "launch_ms": round(launch_ms[0], 4), "peak_src": peaks["src"] + " bf16_tflops (burst)"}
-    extra = {"layer_ms": [round(x, 4) for x in launch_ms],
-             "layer_TFLOPs": [round(f / (m * 1e-3) / 1e12, 2) for f, m in zip(flops, launch_ms)],
-             "window_layer_GBps": [round(b / (m * 1e-3) / 1e9, 1) for b, m in zip(qkv_bytes[1:], launch_ms[1:])],
-             "window_layer_hbm_frac": [round(b / (m * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
-                                       for b, m in zip(qkv_bytes[1:], launch_ms[1:])],
+            "kernel": kname, "alg_flops_per_launch": flops[jd],
+            "launch_ms": round(launch_ms[jd], 4), "peak_src": peaks["src"] + " bf16_tflops (burst)"}
+    extra = {"launch_ms": [round(x, 4) for x in launch_ms],
+             "launch_TFLOPs": [round(f / (m * 1e-3) / 1e12, 2) for f, m in zip(flops, launch_ms)],
              "flops_per_step": sum(flops)}
-    e2e = prefill_e2e(args, layers, pka, cu, outs, sum(flops), world) if not args.no_e2e else None
-    cfg = {"workload": args.workload, "num_seqs": layers[0].num_seqs, "num_tokens": layers[0].num_tokens,
-           "num_heads": 12, "head_dim": 64, "windows": [c.window for c in layers],
-           "chunks": [c.chunk for c in layers], "causal": layers[0].causal,
-           "l2": f"q/k/v {qkv_bytes[0] * 3 / 4 / 2**20:.0f} MiB per layer > L2", "parallelism": f"replicas x{world}"}
+    if args.workload == "encoder-prefill":
+        extra["window_layer_GBps"] = [round(b / (m * 1e-3) / 1e9, 1) for b, m in zip(qkv_bytes[1:], launch_ms[1:])]
+        extra["window_layer_hbm_frac"] = [round(b / (m * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+                                          for b, m in zip(qkv_bytes[1:], launch_ms[1:])]
+    e2e = prefill_e2e(args, launches, sum(flops), world) if not args.no_e2e else None
+    c0 = cases[0]
+    cfg = {"workload": args.workload, "num_seqs": c0.num_seqs, "num_tokens": c0.num_tokens,
+           "num_heads": c0.num_heads, "head_dim": c0.head_dim, "windows": [c.window for c in cases],
+           "causal": [c.causal for c in cases], "parallelism": f"replicas x{world}"}
+    if packed:
+        cfg["chunks"] = [getattr(c, "chunk", 0) for c in cases]
+        cfg["l2"] = f"q/k/v {qkv_bytes[0] * 3 / 4 / 2**20:.0f} MiB per layer > L2"
+        cfg["bias"] = ["T5 relative-position table [H, 257] in kernel" if c.rel_bias is not None else None
+                       for c in cases]
+    else:
+        cfg["context_lens"] = ["U[1,2048] (self)", "512 (cross)"]
+        cfg["query_lens"] = "min(ctx, U[1,256])"
+        cfg["bias"] = ["T5 table, non-negative half (self)", None]
+        cfg["l2"] = "self + cross caches 1.6 GB > L2"
     return {"value": value, "unit": "TFLOP/s", "ms_per_step": ms_step, "dtype": "bf16", "config": cfg,
-            "roofline": roof, "e2e": e2e, "clocks": clk, "gpu_launches": len(layers) * K, "extra": extra,
-            "cases": layers}
+            "roofline": roof, "e2e": e2e, "clocks": clk,
+            "gpu_launches": K * sum(1 + (l.pre is not None) for l in launches), "extra": extra, "cases": cases,
+            "launches": launches}
 
 
-def prefill_e2e(args, layers, pka, cu, outs, flops, world):
+def prefill_e2e(args, launches, flops, world):
+    """The same step through the public API from pinned host buffers: each
+    call's inputs copied host->device, the call, its output read back."""
     import torch
     hosts = []
-    h2d = cu.numel() * 4
-    for c in layers:
+    h2d = 0
+    for l in launches:
         hs = []
-        for t in c.device_qkv:
+        for t in l.host_inputs:
             h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
             h.copy_(t)
-            hs.append(h)
+            hs.append((h, t))
             h2d += t.numel() * t.element_size()
         hosts.append(hs)
-    hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    hout = [torch.empty(l.out.shape, dtype=l.out.dtype, pin_memory=True) for l in launches]
+    d2h = sum(l.out.numel() * l.out.element_size() for l in launches)
 
     def step():
-        for c, hs, o, ho in zip(layers, hosts, outs, hout):
-            for h, d in zip(hs, c.device_qkv):
+        for l, hs, ho in zip(launches, hosts, hout):
+            for h, d in hs:
                 d.copy_(h, non_blocking=True)
-            q, k, v = c.device_qkv
-            pka.swa_prefill(o, q, k, v, cu, c.max_seqlen, c.window, c.causal, c.scale)
-            ho.copy_(o, non_blocking=True)
+            l()
+            ho.copy_(l.out, non_blocking=True)
 
     for _ in range(args.warmup):
         step()
@@ -653,57 +755,96 @@ def oracle_decode_sample(cases, budget_s: float, seed: int = 0):
     return total_b, total_s, threads, desc
 
 
-def oracle_prefill_sample(layers, budget_s: float, seed: int = 0):
+def oracle_prefill_sample(cases, budget_s: float, seed: int = 0):
+    """Time the oracle on seeded random query rows (all heads) of each case
+    until about budget_s seconds of CPU work; returns (flops, s, threads, desc)."""
     import oracle
     oracle.build()
     rng = np.random.default_rng(seed)
     threads = oracle.default_threads()
-    host = [[_host_storage(t, BF16) for t in c.device_qkv] if c.device_qkv is not None else [c.q, c.k, c.v]
-            for c in layers]
+    host = []
+    for c in cases:
+        if isinstance(c, synth.PagedPrefillCase):
+            cc = c.cache
+            kc = np.zeros((cc.num_blocks, cc.num_heads, 16, cc.head_dim), dtype=cc.key.dtype)
+            vc = np.zeros_like(kc)
+            oracle.reshape_and_cache(kc, vc, cc.key, cc.value, cc.slot_mapping, 16)
+            host.append((c.q, kc, vc))
+        elif c.device_qkv is not None:
+            host.append(tuple(_host_storage(t, BF16) for t in c.device_qkv))
+        else:
+            host.append((c.q, c.k, c.v))
     flops = 0
     secs = 0.0
     nrows = 0
     t_start = time.time()
     while time.time() - t_start < budget_s:
-        for c, (q, k, v) in zip(layers, host):
-            rows = np.sort(rng.choice(c.num_tokens, size=64, replace=False)).astype(np.int64)
+        for c, (q, k, v) in zip(cases, host):
+            rows = np.sort(rng.choice(c.num_tokens, size=min(64, c.num_tokens), replace=False)).astype(np.int64)
             t = time.time()
-            if c.chunk > 0:
+            if isinstance(c, synth.PagedPrefillCase):
+                oracle.paged_prefill(q, k, v, c.cache.block_tables, c.cu_seqlens_q, c.cache.context_lens, c.window,
+                                     c.causal, c.scale, 16, BF16, rel_bias=c.rel_bias, rows=rows, nthreads=threads)
+            elif c.chunk > 0:
                 oracle.prefill_chunked(q, k, v, c.cu_seqlens, c.chunk, c.causal, c.scale, BF16, rows=rows,
                                        nthreads=threads)
+            elif c.rel_bias is not None:
+                oracle.prefill_biased(q, k, v, c.cu_seqlens, c.window, c.causal, c.scale, BF16, c.rel_bias, rows=rows,
+                                      nthreads=threads)
             else:
                 oracle.prefill(q, k, v, c.cu_seqlens, c.window, c.causal, c.scale, BF16, rows=rows,
                                nthreads=threads)
             secs += time.time() - t
             flops += 4 * c.head_dim * c.num_heads * _kept_keys(c, rows)
             nrows += len(rows)
-    desc = f"{nrows} query rows drawn at random over the {len(layers)} layer(s) (all heads), fp64 oracle, {secs:.1f} s"
+    desc = (f"{nrows} query rows drawn at random over {len(cases)} call(s) of {cases[0].name} (all heads), "
+            f"fp64 oracle, {secs:.1f} s")
     return flops, secs, threads, desc
 
 
 def _kept_keys(c, rows):
-    cu = c.cu_seqlens
+    """Keys the mask keeps, summed over the listed query rows."""
+    paged = isinstance(c, synth.PagedPrefillCase)
+    cu = c.cu_seqlens_q if paged else c.cu_seqlens
     tot = 0
     for i in rows:
         b = int(np.searchsorted(cu, i, side="right") - 1)
         L = int(cu[b + 1] - cu[b]); r = int(i - cu[b])
-        if c.chunk > 0:
-            lo = r // c.chunk * c.chunk
-            hi = min(L - 1, lo + c.chunk - 1)
+        Lk = int(c.cache.context_lens[b]) if paged else L
+        p = Lk - L + r
+        chunk = 0 if paged else c.chunk
+        if chunk > 0:
+            lo = p // chunk * chunk
+            hi = min(Lk - 1, lo + chunk - 1)
         elif c.window > 0:
-            lo, hi = max(0, r - c.window + 1), min(L - 1, r + c.window - 1)
+            lo, hi = max(0, p - c.window + 1), min(Lk - 1, p + c.window - 1)
         else:
-            lo, hi = 0, L - 1
+            lo, hi = 0, Lk - 1
         if c.causal:
-            hi = min(hi, r)
-        tot += hi - lo + 1
+            hi = min(hi, p)
+        tot += max(0, hi - lo + 1)
     return tot
+
+
+def host_prefill_cases(workload, small=False):
+    """Host-drawn cases of a prefill workload for the oracle (small: fewer
+    sequences of the same shape for the large T5 workloads)."""
+    if workload == "chunked-prefill":
+        return [synth.chunked_prefill_workload()]
+    if workload == "t5-encoder-prefill":
+        return [synth.t5_encoder_prefill_workload(num_seqs=32 if small else 256)]
+    if workload == "t5-paged-prefill":
+        return list(synth.t5_paged_prefill_workload(num_seqs=32))
+    return [synth.prefill_workload(l) for l in range(3)]
 
 
 def cpu_baseline(res, args):
     budget = args.cpu_seconds
-    if args.workload in ("encoder-prefill", "chunked-prefill"):
-        f, s, th, desc = oracle_prefill_sample(res["cases"], budget)
+    if args.workload in PREFILL_WORKLOADS:
+        cases = host_prefill_cases(args.workload, small=True) if args.workload == "t5-paged-prefill" else res["cases"]
+        f, s, th, desc = oracle_prefill_sample(cases, budget)
+        if args.workload == "t5-paged-prefill":
+            desc += " (32 sequences of the same shapes, drawn on the host)"
         return {"value": round(f / s / 1e12, 6), "unit": "TFLOP/s", "cores": th, "kind": "oracle", "sample": desc}
     b, s, th, desc = oracle_decode_sample(res["cases"], budget)
     return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": th, "kind": "oracle", "sample": desc}
@@ -714,9 +855,8 @@ def run_reference(args, rank, world):
     bounded sample per step."""
     if rank != 0:
         return None
-    if args.workload in ("encoder-prefill", "chunked-prefill"):
-        layers = ([synth.chunked_prefill_workload()] if args.workload == "chunked-prefill"
-                  else [synth.prefill_workload(l) for l in range(3)])
+    if args.workload in PREFILL_WORKLOADS:
+        layers = host_prefill_cases(args.workload, small=True)
         per = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
         oracle_prefill_sample(layers, 0.5)
         f, s, th, desc = oracle_prefill_sample(layers, per * args.steps)
@@ -749,7 +889,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
     ap.add_argument("--workload", default="t5-small-decode",
-                    choices=sorted(DECODE_WORKLOADS) + ["encoder-prefill", "chunked-prefill"])
+                    choices=sorted(DECODE_WORKLOADS) + list(PREFILL_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--separate-launches", action="store_true",
                     help="t5-large-decode: one decode launch per attention type instead of one fused launch")
@@ -771,7 +911,7 @@ def main():
             print(json.dumps(line), flush=True)
         return
     peaks = measured_peaks()
-    if args.workload in ("encoder-prefill", "chunked-prefill"):
+    if args.workload in PREFILL_WORKLOADS:
         res = run_prefill(args, rank, world, local, peaks)
     else:
         res = run_decode(args, rank, world, local, peaks)

@@ -314,6 +314,68 @@ PKA_API pka_status pka_chunked_prefill(void *out, const void *q, const void *k, 
                                        int num_heads, int head_dim, int chunk, int causal, float scale,
                                        pka_dtype dtype, int32_t *status, void *stream);
 
+/*
+ * pka_prefill_biased — pka_swa_prefill with an additive relative-position
+ * bias in the scores: the T5 bias of an encoder's bidirectional
+ * self-attention ("Add Encoder-decoder model support and T5 Model support":
+ * T5 carries a custom bias in its attention; "PagedAttention: Support custom
+ * attention bias for T5 model (1/2)": softmax((QK^T + A)/sqrt(d_k)) V, the
+ * relative distance capped, larger distances reusing the last value).  With
+ * cap = num_buckets - 1 and d = r - c (query position minus key position):
+ *   A[h, r, c] = rel_bias[h, cap + clamp(d, -cap, cap)]
+ *   out[i,h,:] = sum_c softmax(scale * (q[i,h,:] . k[c,h,:] + A[h,r,c]))_c v[c,h,:]
+ * over the keys pka_swa_prefill's mask keeps.  A causal layer only reads the
+ * table's non-negative half, columns cap .. 2 cap, which is the decode-side
+ * table of pka_paged_attn_decode_t5bias.
+ *   rel_bias   f32 [num_heads, 2 * num_buckets - 1], 4-byte aligned, not NULL
+ *   num_buckets >= 1
+ * Every other argument and error as for pka_swa_prefill.
+ */
+PKA_API pka_status pka_prefill_biased(void *out, const void *q, const void *k, const void *v,
+                                      const int32_t *cu_seqlens, int num_seqs, int num_tokens, int max_seqlen,
+                                      int num_heads, int head_dim, int window, int causal, const float *rel_bias,
+                                      int num_buckets, float scale, pka_dtype dtype, int32_t *status, void *stream);
+
+/*
+ * pka_paged_prefill — prefill of each sequence's newest tokens against its
+ * keys in the paged cache ("Add Encoder-decoder model support and T5 Model
+ * support": prompt and generated tokens keep separate KV blocks, and the
+ * prefill kernels as well as the decode kernels read cross-attention keys
+ * through their own block table).  Sequence s has Lq_s = cu_seqlens_q[s+1] -
+ * cu_seqlens_q[s] query rows and ctx_s = context_lens[s] keys, key j at
+ *   k_cache[block_tables[s, j / 16], h, j % 16, :]   (v_cache likewise).
+ * Query row r of s sits at key position p = ctx_s - Lq_s + r (the queries are
+ * the last Lq_s positions, whose K/V reshape_and_cache has already written).
+ * The keys c in [0, ctx_s) kept are pka_swa_prefill's with r replaced by p
+ * (causal: c <= p; window: |p - c| < window, causal 0 <= p - c < window); the
+ * optional bias is pka_prefill_biased's with d = p - c.  A row that keeps no
+ * key (ctx_s == 0, or rows at p < 0 when Lq_s > ctx_s) is written as zeros.
+ * With causal = 0, window -1 and no bias every query attends to all ctx_s
+ * keys: a decoder prompt's cross-attention to the encoder.
+ *
+ *   out, q        [num_tokens, num_heads, 64] bf16, rows packed by cu_seqlens_q
+ *   k_cache, v_cache [num_blocks, num_heads, 16, 64] bf16, 16-byte aligned
+ *   block_tables  int32 [num_seqs, max_blocks_per_seq]; entries of blocks
+ *                 with no kept key (before every row's window, past ctx_s)
+ *                 are never read
+ *   context_lens  int32 [num_seqs], each in [0, max_blocks_per_seq * 16]
+ *                 (PKA_DEVCHK_CONTEXT_LEN and clamped otherwise)
+ *   max_query_len upper bound on every Lq_s
+ *   rel_bias      NULL or f32 [num_heads, 2 * num_buckets - 1]
+ *   block_size    16
+ *   status        int32 device word or NULL (PKA_DEVCHK_CU_SEQLENS,
+ *                 PKA_DEVCHK_CONTEXT_LEN, PKA_DEVCHK_BLOCK_ID — the entry is
+ *                 replaced by block 0 — and PKA_DEVCHK_TIMEOUT)
+ * Cache rows past ctx_s in the last block may hold any bits (NaN included).
+ * Accumulation is f32; P is rounded to bf16 before the P.V product.
+ */
+PKA_API pka_status pka_paged_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *block_tables, const int32_t *cu_seqlens_q,
+                                     const int32_t *context_lens, int num_seqs, int num_tokens, int max_query_len,
+                                     int num_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                                     int num_blocks, int window, int causal, const float *rel_bias, int num_buckets,
+                                     float scale, pka_dtype dtype, int32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

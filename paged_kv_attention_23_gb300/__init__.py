@@ -13,7 +13,8 @@ import os
 import threading
 
 __all__ = ["PkaError", "load", "build", "lib_path", "reshape_and_cache", "paged_attn_decode",
-           "paged_attn_decode_t5bias", "paged_attn_decode_multi", "chunked_prefill",
+           "paged_attn_decode_t5bias", "paged_attn_decode_multi", "chunked_prefill", "prefill_biased",
+           "paged_prefill",
            "paged_attn_decode_workspace_size", "swa_prefill", "DecodeWorkspace", "DTYPE_CODE",
            "DEVCHK_BLOCK_ID", "DEVCHK_CONTEXT_LEN", "DEVCHK_SLOT", "DEVCHK_TIMEOUT", "DEVCHK_CU_SEQLENS",
            "EXPORTED_SYMBOLS"]
@@ -27,7 +28,8 @@ DEVCHK_BLOCK_ID, DEVCHK_CONTEXT_LEN, DEVCHK_SLOT, DEVCHK_TIMEOUT, DEVCHK_CU_SEQL
 EXPORTED_SYMBOLS = ("pka_status_string", "pka_version", "pka_reshape_and_cache",
                     "pka_paged_attn_decode_workspace_size", "pka_paged_attn_decode",
                     "pka_paged_attn_decode_noalloc", "pka_paged_attn_decode_t5bias",
-                    "pka_paged_attn_decode_multi", "pka_swa_prefill", "pka_chunked_prefill")
+                    "pka_paged_attn_decode_multi", "pka_swa_prefill", "pka_chunked_prefill", "pka_prefill_biased",
+                    "pka_paged_prefill")
 
 
 class DecodeProblem(ctypes.Structure):
@@ -85,6 +87,10 @@ def load():
         lib.pka_paged_attn_decode_multi.restype = I
         lib.pka_swa_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P]
         lib.pka_swa_prefill.restype = I
+        lib.pka_prefill_biased.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, I, F, I, P, P]
+        lib.pka_prefill_biased.restype = I
+        lib.pka_paged_prefill.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P, I, F, I, P, P]
+        lib.pka_paged_prefill.restype = I
         lib.pka_chunked_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P]
         lib.pka_chunked_prefill.restype = I
         _lib = lib
@@ -328,4 +334,60 @@ def chunked_prefill(out, q, k, v, cu_seqlens, max_seqlen, chunk, causal=1, scale
            lib.pka_chunked_prefill(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
                                    T, int(max_seqlen), H, D, int(chunk), int(causal), float(scale), _dtype_code(q),
                                    _ptr(status), _stream(stream)))
+    return out
+
+
+def prefill_biased(out, q, k, v, cu_seqlens, max_seqlen, rel_bias, window=-1, causal=0, scale=None, status=None,
+                   stream=None):
+    """``swa_prefill`` with the relative-position bias rel_bias [H, 2B-1]:
+    A[h, r, c] = rel_bias[h, B-1 + clamp(r - c, -(B-1), B-1)] inside the scores."""
+    torch = _torch()
+    for n, t in (("out", out), ("q", q), ("k", k), ("v", v)):
+        _need(t, n, ndim=3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(rel_bias, "rel_bias", torch.float32, 2)
+    T, H, D = q.shape
+    if rel_bias.shape[0] != H or rel_bias.shape[1] % 2 != 1:
+        raise ValueError("rel_bias must be [num_heads, 2 * num_buckets - 1]")
+    if scale is None:
+        scale = D ** -0.5
+    lib = load()
+    _check("pka_prefill_biased",
+           lib.pka_prefill_biased(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T,
+                                  int(max_seqlen), H, D, int(window), int(causal), _ptr(rel_bias),
+                                  (rel_bias.shape[1] + 1) // 2, float(scale), _dtype_code(q), _ptr(status),
+                                  _stream(stream)))
+    return out
+
+
+def paged_prefill(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, context_lens, max_query_len, window=-1,
+                  causal=1, rel_bias=None, scale=None, status=None, stream=None):
+    """Prefill of each sequence's last Lq tokens (q/out [T, H, 64], packed by
+    cu_seqlens_q) against its context_lens[s] keys in the paged caches
+    [num_blocks, H, 16, 64] through block_tables; query row r sits at key
+    position ctx - Lq + r.  Optional relative-position bias as in
+    ``prefill_biased``."""
+    torch = _torch()
+    _need(out, "out", ndim=3); _need(q, "q", ndim=3)
+    _need(k_cache, "k_cache", ndim=4); _need(v_cache, "v_cache", ndim=4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    nb_buckets = 0
+    if rel_bias is not None:
+        _need(rel_bias, "rel_bias", torch.float32, 2)
+        if rel_bias.shape[1] % 2 != 1:
+            raise ValueError("rel_bias must be [num_heads, 2 * num_buckets - 1]")
+        nb_buckets = (rel_bias.shape[1] + 1) // 2
+    T, H, D = q.shape
+    nb, _, bs, _ = k_cache.shape
+    if scale is None:
+        scale = D ** -0.5
+    lib = load()
+    _check("pka_paged_prefill",
+           lib.pka_paged_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                 _ptr(cu_seqlens_q), _ptr(context_lens), cu_seqlens_q.numel() - 1, T,
+                                 int(max_query_len), H, D, bs, block_tables.shape[1], nb, int(window), int(causal),
+                                 _ptr(rel_bias), nb_buckets, float(scale), _dtype_code(q), _ptr(status),
+                                 _stream(stream)))
     return out

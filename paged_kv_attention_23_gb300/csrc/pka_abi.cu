@@ -68,6 +68,48 @@ pka_status prepare_decode(const pka_decode_problem &p, int block_size, int num_h
     return PKA_OK;
 }
 
+// Checks shared by every prefill entry point; on PKA_OK fills the packed-key
+// launch arguments (a.num_tokens == 0: nothing to launch).
+pka_status prepare_prefill(void *out, const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                           int num_seqs, int num_tokens, int max_seqlen, int num_heads, int head_dim, int window,
+                           int causal, float scale, pka_dtype dtype, int32_t *status, pka::PrefillArgs &a)
+{
+    if (num_seqs < 0 || num_tokens < 0 || max_seqlen < 0 || num_heads < 1 || !std::isfinite(scale) ||
+        (causal != 0 && causal != 1) || !dtype_ok(dtype))
+        return PKA_ERR_INVALID_ARG;
+    if (window != -1 && window < 1) return PKA_ERR_INVALID_ARG;
+    if (dtype != PKA_BF16) return PKA_ERR_UNSUPPORTED;
+    if (head_dim != 64) return PKA_ERR_UNSUPPORTED;
+    a.num_tokens = 0;
+    if (num_seqs == 0 || num_tokens == 0) return PKA_OK;
+    if (!out || !q || !k || !v || !cu_seqlens) return PKA_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(cu_seqlens, 4) ||
+        !aligned(status, 4))
+        return PKA_ERR_INVALID_ARG;
+    a.out = out;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.cu_seqlens = cu_seqlens;
+    a.context_lens = nullptr;
+    a.block_tables = nullptr;
+    a.rel_bias = nullptr;
+    a.num_buckets = 0;
+    a.status = status;
+    a.scale = scale;
+    a.num_seqs = num_seqs;
+    a.num_tokens = num_tokens;
+    a.max_seqlen = max_seqlen;
+    a.num_heads = num_heads;
+    a.head_dim = head_dim;
+    a.window = window;
+    a.causal = causal;
+    a.chunk = 0;
+    a.mbps = 0;
+    a.num_blocks = 0;
+    return PKA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -187,33 +229,10 @@ pka_status pka_swa_prefill(void *out, const void *q, const void *k, const void *
                            int num_seqs, int num_tokens, int max_seqlen, int num_heads, int head_dim, int window,
                            int causal, float scale, pka_dtype dtype, int32_t *status, void *stream)
 {
-    if (num_seqs < 0 || num_tokens < 0 || max_seqlen < 0 || num_heads < 1 || !std::isfinite(scale) ||
-        (causal != 0 && causal != 1) || !dtype_ok(dtype))
-        return PKA_ERR_INVALID_ARG;
-    if (window != -1 && window < 1) return PKA_ERR_INVALID_ARG;
-    if (dtype != PKA_BF16) return PKA_ERR_UNSUPPORTED;
-    if (head_dim != 64) return PKA_ERR_UNSUPPORTED;
-    if (num_seqs == 0 || num_tokens == 0) return PKA_OK;
-    if (!out || !q || !k || !v || !cu_seqlens) return PKA_ERR_INVALID_ARG;
-    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(cu_seqlens, 4) ||
-        !aligned(status, 4))
-        return PKA_ERR_INVALID_ARG;
     pka::PrefillArgs a;
-    a.out = out;
-    a.q = q;
-    a.k = k;
-    a.v = v;
-    a.cu_seqlens = cu_seqlens;
-    a.status = status;
-    a.scale = scale;
-    a.num_seqs = num_seqs;
-    a.num_tokens = num_tokens;
-    a.max_seqlen = max_seqlen;
-    a.num_heads = num_heads;
-    a.head_dim = head_dim;
-    a.window = window;
-    a.causal = causal;
-    a.chunk = 0;
+    const pka_status st = prepare_prefill(out, q, k, v, cu_seqlens, num_seqs, num_tokens, max_seqlen, num_heads,
+                                          head_dim, window, causal, scale, dtype, status, a);
+    if (st != PKA_OK || a.num_tokens == 0) return st;
     return from_cuda(pka::launch_swa_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -222,33 +241,52 @@ pka_status pka_chunked_prefill(void *out, const void *q, const void *k, const vo
                                int causal, float scale, pka_dtype dtype, int32_t *status, void *stream)
 {
     if (chunk < 1) return PKA_ERR_INVALID_ARG;
-    // every other argument is checked as for the sliding-window prefill
-    if (num_seqs < 0 || num_tokens < 0 || max_seqlen < 0 || num_heads < 1 || !std::isfinite(scale) ||
-        (causal != 0 && causal != 1) || !dtype_ok(dtype))
-        return PKA_ERR_INVALID_ARG;
-    if (dtype != PKA_BF16) return PKA_ERR_UNSUPPORTED;
-    if (head_dim != 64) return PKA_ERR_UNSUPPORTED;
-    if (num_seqs == 0 || num_tokens == 0) return PKA_OK;
-    if (!out || !q || !k || !v || !cu_seqlens) return PKA_ERR_INVALID_ARG;
-    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(cu_seqlens, 4) ||
-        !aligned(status, 4))
-        return PKA_ERR_INVALID_ARG;
     pka::PrefillArgs a;
-    a.out = out;
-    a.q = q;
-    a.k = k;
-    a.v = v;
-    a.cu_seqlens = cu_seqlens;
-    a.status = status;
-    a.scale = scale;
-    a.num_seqs = num_seqs;
-    a.num_tokens = num_tokens;
-    a.max_seqlen = max_seqlen;
-    a.num_heads = num_heads;
-    a.head_dim = head_dim;
-    a.window = -1;
-    a.causal = causal;
+    const pka_status st = prepare_prefill(out, q, k, v, cu_seqlens, num_seqs, num_tokens, max_seqlen, num_heads,
+                                          head_dim, -1, causal, scale, dtype, status, a);
+    if (st != PKA_OK || a.num_tokens == 0) return st;
     a.chunk = chunk;
+    return from_cuda(pka::launch_swa_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
+pka_status pka_prefill_biased(void *out, const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                              int num_seqs, int num_tokens, int max_seqlen, int num_heads, int head_dim, int window,
+                              int causal, const float *rel_bias, int num_buckets, float scale, pka_dtype dtype,
+                              int32_t *status, void *stream)
+{
+    if (!rel_bias || num_buckets < 1 || !aligned(rel_bias, 4)) return PKA_ERR_INVALID_ARG;
+    pka::PrefillArgs a;
+    const pka_status st = prepare_prefill(out, q, k, v, cu_seqlens, num_seqs, num_tokens, max_seqlen, num_heads,
+                                          head_dim, window, causal, scale, dtype, status, a);
+    if (st != PKA_OK || a.num_tokens == 0) return st;
+    a.rel_bias = rel_bias;
+    a.num_buckets = num_buckets;
+    return from_cuda(pka::launch_swa_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
+pka_status pka_paged_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_tables, const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                             int num_seqs, int num_tokens, int max_query_len, int num_heads, int head_dim,
+                             int block_size, int max_blocks_per_seq, int num_blocks, int window, int causal,
+                             const float *rel_bias, int num_buckets, float scale, pka_dtype dtype, int32_t *status,
+                             void *stream)
+{
+    if (rel_bias && (num_buckets < 1 || !aligned(rel_bias, 4))) return PKA_ERR_INVALID_ARG;
+    if (max_blocks_per_seq < 1 || num_blocks < 1) return PKA_ERR_INVALID_ARG;
+    pka::PrefillArgs a;
+    const pka_status st = prepare_prefill(out, q, k_cache, v_cache, cu_seqlens_q, num_seqs, num_tokens, max_query_len,
+                                          num_heads, head_dim, window, causal, scale, dtype, status, a);
+    if (st != PKA_OK) return st;
+    if (block_size != 16) return PKA_ERR_UNSUPPORTED;
+    if (a.num_tokens == 0) return PKA_OK;
+    if (!block_tables || !context_lens || !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PKA_ERR_INVALID_ARG;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.mbps = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.rel_bias = rel_bias;
+    a.num_buckets = rel_bias ? num_buckets : 0;
     return from_cuda(pka::launch_swa_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -53,12 +53,18 @@ cudaError_t launch_paged_decode_multi(const DecodeArgs *a, const DecodePlan *pla
 // ---- sliding-window prefill ----------------------------------------------------
 struct PrefillArgs {
     void *out;
-    const void *q, *k, *v;
-    const int32_t *cu_seqlens;
+    const void *q;
+    const void *k, *v;                 // packed [T, H, 64], or the paged caches [num_blocks, H, 16, 64]
+    const int32_t *cu_seqlens;         // query rows (packed: key rows too)
+    const int32_t *context_lens;       // paged only: keys per sequence
+    const int32_t *block_tables;       // paged only: [num_seqs, mbps]; NULL selects packed keys
+    const float *rel_bias;             // [H, 2 * num_buckets - 1] or NULL
+    int num_buckets;
     int32_t *status;
     float scale;
     int num_seqs, num_tokens, max_seqlen, num_heads, head_dim, window, causal;
-    int chunk;   // > 0: chunked local attention (window must be -1)
+    int chunk;   // > 0: chunked local attention (window must be -1; packed only)
+    int mbps, num_blocks;              // paged only
 };
 
 cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream);

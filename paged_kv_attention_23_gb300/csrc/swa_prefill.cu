@@ -66,7 +66,9 @@ constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NS, B_SF = 2 + 2 * NS, 
               B_OF = B_PF + 2, B_OE = B_OF + 2, NBAR = B_OE + 2;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, abort flag
 constexpr uint32_t OFF_SCHED = (OFF_MISC + 16 + 127) / 128 * 128;
-constexpr uint32_t SMEM_BYTES = OFF_SCHED + (4 * MAX_SEQS + 1) * 4 + 1024;   // + alignment slack
+constexpr uint32_t SMEM_BYTES = OFF_SCHED + (6 * MAX_SEQS + 1) * 4 + 1024;   // + alignment slack
+constexpr int CBS = 16;                   // paged cache block: 16 key rows of one head
+constexpr uint32_t CBLK_BYTES = CBS * HD * 2;                                  // 2 KB per block and head
 
 // TMEM columns: S of query tile w at 128 w, O of query tile w at 256 + 64 w
 constexpr uint32_t TMEM_COLS = 512;
@@ -77,23 +79,30 @@ constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(BM, HD, false, true);   // O +=
 
 struct Params {
     __nv_bfloat16 *out;
-    const int32_t *cu_seqlens;
+    const int32_t *cu_seqlens;       // query rows (packed keys too)
+    const int32_t *context_lens;     // paged: keys of each sequence
+    const int32_t *block_tables;     // paged: [num_seqs, mbps] cache blocks
+    const float *rel_bias;           // [H, 2 * num_buckets - 1] relative-position bias, or NULL
     int32_t *status;
     float scale_log2;
     int num_seqs, num_tokens, H, window, causal, chunk;
+    int mbps, num_blocks, num_buckets;
 };
 
 // One work item: two query tiles [r0, r0+128) and [r0+128, r0+256) of a
 // (sequence, head) and the key tiles c_lo + 128 j, j < nkv, covering both.
 // Query tile w multiplies key tiles jb[w] .. je[w] (empty when jb > je).
+// Query row r sits at key position r + qoff (qoff = Lk - L: the queries are
+// the sequence's last L positions); keys at k_end and beyond are not needed.
 struct Item {
-    int s0, L, h, r0, c_lo, nkv;
+    int s0, L, Lk, qoff, seq, h, r0, c_lo, nkv, k_end;
     int jb[2], je[2];
 };
 
 struct Sched {
-    const int *cum, *start, *len;
+    const int *cum, *start, *len, *lenk, *seqid;
     int nseq, H, window, causal, chunk;
+    bool paged;
     __device__ __forceinline__ Item get(int t) const
     {
         int lo = 0, hi = nseq;                         // cum[lo] <= t < cum[hi]
@@ -104,27 +113,39 @@ struct Sched {
         Item I;
         I.s0 = start[lo];
         I.L = len[lo];
+        I.Lk = paged ? lenk[lo] : I.L;
+        I.seq = seqid[lo];
+        I.qoff = I.Lk - I.L;
         const int np = (I.L + 2 * BM - 1) / (2 * BM);
         const int r = t - cum[lo];
         I.h = r / np;                                  // pairs of one head are neighbours: shared K/V in L2
         I.r0 = (r - I.h * np) * 2 * BM;
-        int c_lo = 0, c_hi = -1;
+        int c_lo = 0x7fffffff, c_hi = -1;
         int lo_w[2], hi_w[2];
         for (int w = 0; w < 2; ++w) {
+            lo_w[w] = 0; hi_w[w] = -1;
             const int a = I.r0 + w * BM;
-            if (a >= I.L) { lo_w[w] = 0; hi_w[w] = -1; continue; }
-            const int b = min(a + BM, I.L) - 1;
-            int kl = 0, kh = I.L - 1;
-            if (chunk > 0) { kl = a / chunk * chunk; kh = min(I.L - 1, b / chunk * chunk + chunk - 1); }
-            else if (window > 0) { kl = max(0, a - window + 1); kh = min(I.L - 1, b + window - 1); }
-            if (causal) kh = min(kh, b);
+            if (a >= I.L) continue;
+            const int pa = a + I.qoff, pb = min(a + BM, I.L) - 1 + I.qoff;   // key positions of the tile's rows
+            int kl = 0, kh = I.Lk - 1;
+            if (chunk > 0) { kl = pa / chunk * chunk; kh = min(I.Lk - 1, pb / chunk * chunk + chunk - 1); }
+            else if (window > 0) { kl = max(0, pa - window + 1); kh = min(I.Lk - 1, pb + window - 1); }
+            if (causal) kh = min(kh, pb);
+            if (kh < kl) continue;                     // no key for any row of this tile
             lo_w[w] = kl;
             hi_w[w] = kh;
-            if (w == 0) c_lo = kl;
+            c_lo = min(c_lo, kl);
             c_hi = max(c_hi, kh);
         }
+        if (c_hi < 0) {                                // neither tile has a key
+            I.c_lo = 0; I.nkv = 0; I.k_end = 0;
+            I.jb[0] = I.jb[1] = 1; I.je[0] = I.je[1] = 0;
+            return I;
+        }
+        if (paged) c_lo = c_lo / CBS * CBS;            // paged key tiles are whole cache blocks
         I.c_lo = c_lo;
         I.nkv = (c_hi - c_lo) / BN + 1;
+        I.k_end = c_hi + 1;
         for (int w = 0; w < 2; ++w) {
             if (hi_w[w] < lo_w[w]) { I.jb[w] = 1; I.je[w] = 0; continue; }
             I.jb[w] = (lo_w[w] - c_lo) / BN;
@@ -197,6 +218,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     return true;
 }
 
+// PAGED: keys come from the paged cache [num_blocks, H, 16, 64] through the
+// block tables (tm_k / tm_v are 4-D maps with one cache block per box);
+// otherwise from the packed [T, H, 64] keys of the same rows as the queries.
+// BIAS: the relative-position bias is added to the scores.
+template <bool PAGED, bool BIAS>
 __global__ void __launch_bounds__(NTHREADS, 1)
 swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const Params P)
@@ -214,6 +240,8 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     int *start = cum + MAX_SEQS + 1;
     int *len = start + MAX_SEQS;
     int *rank_tmp = len + MAX_SEQS;
+    int *lenk = rank_tmp + MAX_SEQS;
+    int *seqid = lenk + MAX_SEQS;
 
     // ---- schedule: sequences by decreasing length (longest work first) -------
     const int S = P.num_seqs;
@@ -224,6 +252,10 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             a = 0; b = 0;
         }
         rank_tmp[s] = b - a;
+        if (PAGED) {
+            const int c = P.context_lens[s];
+            if (c < 0 || c > P.mbps * CBS) flag_status(P.status, PKA_DEVCHK_CONTEXT_LEN);
+        }
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NBAR; ++i) {
@@ -249,6 +281,8 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const int a = P.cu_seqlens[s];
         start[rk] = a < 0 ? 0 : a;
         len[rk] = Ls;
+        seqid[rk] = s;
+        if (PAGED) lenk[rk] = min(max(P.context_lens[s], 0), P.mbps * CBS);
     }
     __syncthreads();
     if (warp == 0) {
@@ -267,7 +301,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         if (lane == 31) cum[S] = incl;
     }
     __syncthreads();
-    const Sched sched{cum, start, len, S, P.H, P.window, P.causal, P.chunk};
+    const Sched sched{cum, start, len, lenk, seqid, S, P.H, P.window, P.causal, P.chunk, PAGED};
     const int total_items = cum[S];
     const uint32_t tmem = *tmem_base_sm;
 
@@ -288,10 +322,34 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             for (int j = 0; j < I.nkv; ++j, ++g) {
                 const uint32_t st = g % NS;
                 if (!wait_or_abort(BAR(B_KVE + st), ((g / NS) & 1) ^ 1, abort_flag, P.status)) { ok = false; break; }
-                const int row = I.s0 + I.c_lo + j * BN;
-                mbar_arrive_expect_tx(BAR(B_KVF + st), 2 * TILE_BYTES);
-                tc::tma_load_3d(sb + OFF_KV + st * 2 * TILE_BYTES, &tm_k, 0, I.h, row, BAR(B_KVF + st));
-                tc::tma_load_3d(sb + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES, &tm_v, 0, I.h, row, BAR(B_KVF + st));
+                const uint32_t dk = sb + OFF_KV + st * 2 * TILE_BYTES, dv = dk + TILE_BYTES;
+                if constexpr (PAGED) {
+                    // the tile's cache blocks below k_end, one 16-row box each; a
+                    // 2 KB box keeps the 1024-byte swizzle atoms of a contiguous tile
+                    const int c0 = I.c_lo + j * BN;
+                    const int nblk = min(BN / CBS, (I.k_end - c0 + CBS - 1) / CBS);
+                    const int32_t *bt = P.block_tables + (size_t)I.seq * P.mbps + c0 / CBS;
+                    int phys[BN / CBS];
+#pragma unroll
+                    for (int b = 0; b < BN / CBS; ++b) phys[b] = b < nblk ? __ldg(bt + b) : 0;
+                    mbar_arrive_expect_tx(BAR(B_KVF + st), 2u * nblk * CBLK_BYTES);
+#pragma unroll
+                    for (int b = 0; b < BN / CBS; ++b) {
+                        if (b >= nblk) break;
+                        int pb = phys[b];
+                        if ((unsigned)pb >= (unsigned)P.num_blocks) {
+                            flag_status(P.status, PKA_DEVCHK_BLOCK_ID);
+                            pb = 0;
+                        }
+                        tc::tma_load_4d(dk + b * CBLK_BYTES, &tm_k, 0, 0, I.h, pb, BAR(B_KVF + st));
+                        tc::tma_load_4d(dv + b * CBLK_BYTES, &tm_v, 0, 0, I.h, pb, BAR(B_KVF + st));
+                    }
+                } else {
+                    const int row = I.s0 + I.c_lo + j * BN;
+                    mbar_arrive_expect_tx(BAR(B_KVF + st), 2 * TILE_BYTES);
+                    tc::tma_load_3d(dk, &tm_k, 0, I.h, row, BAR(B_KVF + st));
+                    tc::tma_load_3d(dv, &tm_v, 0, I.h, row, BAR(B_KVF + st));
+                }
             }
             if (!ok) break;
         }
@@ -344,7 +402,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 tc::commit(BAR(B_KVE + st));
                 return true;
             };
-            bool ok = issue_qk(0);
+            bool ok = I.nkv == 0 || issue_qk(0);
             for (int j = 0; j < I.nkv && ok; ++j) {
                 if (j + 1 < I.nkv && !issue_qk(j + 1)) ok = false;
                 if (ok && !issue_pv(j)) ok = false;
@@ -362,15 +420,32 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const uint32_t tS = tmem + lane_addr + COL_S + w * BN;
         const uint32_t tO = tmem + lane_addr + COL_O + w * HD;
         const uint32_t pbase = sb + OFF_P + w * P_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
-        uint32_t cs = 0, co = 0;
+        uint32_t cs = 0, co = 0, g = 0;
         for (int t = blockIdx.x; t < total_items && !*abort_flag; t += gridDim.x) {
             const Item I = sched.get(t);
-            if (I.jb[w] > I.je[w]) continue;           // this query tile lies past the sequence
-            const int rr = I.r0 + w * BM + row;        // query position within its sequence
-            int lo = 0, hi = I.L;                      // keys [lo, hi) kept for this row
-            if (P.chunk > 0) { lo = rr / P.chunk * P.chunk; hi = min(hi, lo + P.chunk); }
-            else if (P.window > 0) { lo = max(lo, rr - P.window + 1); hi = min(hi, rr + P.window); }
-            if (P.causal) hi = min(hi, rr + 1);
+            const uint32_t g_item = g;                 // K/V stages of this item start at g_item
+            g += I.nkv;
+            const int rr = I.r0 + w * BM + row;        // query row within its sequence
+            if (I.jb[w] > I.je[w]) {
+                // past the sequence, or (paged) no key for any row of the tile: zero rows
+                if (PAGED && rr < I.L) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(P.out + ((size_t)(I.s0 + rr) * P.H + I.h) * HD);
+#pragma unroll
+                    for (int c = 0; c < HD / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                continue;
+            }
+            const int pos = rr + I.qoff;               // the row's key position
+            int lo = 0, hi = I.Lk;                     // keys [lo, hi) kept for this row
+            if (P.chunk > 0) { lo = pos / P.chunk * P.chunk; hi = min(hi, lo + P.chunk); }
+            else if (P.window > 0) { lo = max(lo, pos - P.window + 1); hi = min(hi, pos + P.window); }
+            if (P.causal) hi = min(hi, pos + 1);
+            const float *rel = nullptr;                // rel[d]: bias of a key d positions before the row
+            int cap = 0;
+            if constexpr (BIAS) {
+                cap = P.num_buckets - 1;
+                rel = P.rel_bias + (size_t)I.h * (2 * cap + 1) + cap;
+            }
             float m = -INFINITY, l = 0.f;
             bool ok = true;
             for (int j = I.jb[w]; j <= I.je[w]; ++j, ++cs) {
@@ -381,8 +456,33 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 tc::tmem_ld64(tS + 64, x + 64);
                 tc::fence_before_sync();
                 mbar_arrive(BAR(B_SE + w));            // S columns free: QK of the next key tile may start
-                // mask to the kept key range; tile max of the raw scores
                 const int c0 = I.c_lo + j * BN;
+                if constexpr (PAGED) {
+                    // V rows at k_end and beyond hold unread blocks or cache rows
+                    // past the context (any bits): zero them so that P = 0 there
+                    // contributes exactly nothing to P V
+                    if (row >= I.k_end - c0) {
+                        const uint32_t vrow = sb + OFF_KV + ((g_item + j) % NS) * 2 * TILE_BYTES + TILE_BYTES + row * 128;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + c * 16), "r"(0)
+                                         : "memory");
+                    }
+                }
+                // the relative-position bias: one value for the whole tile when
+                // every key of it lies beyond the table's reach, else per key
+                float boff = 0.f;
+                if constexpr (BIAS) {
+                    const int dhi = pos - c0, dlo = dhi - (BN - 1);
+                    if (dlo >= cap) boff = __ldg(rel + cap);
+                    else if (dhi <= -cap) boff = __ldg(rel - cap);
+                    else {
+#pragma unroll
+                        for (int i = 0; i < BN; ++i) x[i] += __ldg(rel + min(max(dhi - i, -cap), cap));
+                    }
+                    boff *= P.scale_log2;
+                }
+                // mask to the kept key range; tile max of the raw scores
                 const int ilo = lo - c0, ihi = hi - c0;
                 const bool masked = ilo > 0 || ihi < BN;
                 if (masked) {
@@ -397,7 +497,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     for (int i = 1; i < 32; i += 2) a = tc::max3(a, x[k * 32 + i], x[k * 32 + i + 1]);
                     mx[k] = fmaxf(a, x[k * 32 + 31]);
                 }
-                const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * P.scale_log2;
+                const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * P.scale_log2 + boff;
                 // raise the running max only when it grows by more than 2^8
                 const bool raise = mt > m + RESCALE_LOG2;
                 const float m_old = m;
@@ -409,7 +509,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 }
                 if (raise) l *= ex2(m_old - m);
                 // P = 2^(scale * s - m) as bf16 into the swizzled buffer; row sum in f32
-                const float mneg = m == -INFINITY ? 0.f : -m;
+                const float mneg = (m == -INFINITY ? 0.f : -m) + boff;
                 l += write_p_row(x, P.scale_log2, mneg, pbase, row);
                 if (j > I.jb[w] && __any_sync(kFull, raise)) {
                     // the running max rose: bring this row's O to the new max (in TMEM)
@@ -491,21 +591,62 @@ bool make_map(CUtensorMap *m, const void *base, int T, int H)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [num_blocks, H, 16, 64] bf16 paged cache -> boxes of one block (16 rows x
+// 64 dims) of one head, 128-byte swizzle
+bool make_paged_map(CUtensorMap *m, const void *base, int num_blocks, int H)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)HD, (cuuint64_t)CBS, (cuuint64_t)H, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)HD * 2, (cuuint64_t)CBLK_BYTES, (cuuint64_t)H * CBLK_BYTES};
+    const cuuint32_t box[4] = {HD, CBS, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool PAGED, bool BIAS>
+cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, Params P,
+                       const PrefillArgs &a, int sms, cudaStream_t stream)
+{
+    auto kern = swa_prefill_tc_kernel<PAGED, BIAS>;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [&] {
+        attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    if (attr != cudaSuccess) return attr;
+    for (int base = 0; base < a.num_seqs; base += MAX_SEQS) {
+        P.num_seqs = std::min(MAX_SEQS, a.num_seqs - base);
+        P.cu_seqlens = a.cu_seqlens + base;
+        if (PAGED) {
+            P.context_lens = a.context_lens + base;
+            P.block_tables = a.block_tables + (size_t)base * a.mbps;
+        }
+        const long long tiles_upper = (long long)P.num_seqs * ((a.max_seqlen + 2 * BM - 1) / (2 * BM)) * a.num_heads;
+        const int grid = (int)std::max<long long>(1, std::min<long long>(sms, tiles_upper));
+        kern<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mq, mk, mv, P);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream)
 {
     if (a.head_dim != HD) return cudaErrorInvalidValue;
+    const bool paged = a.block_tables != nullptr;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, a.q, a.num_tokens, a.num_heads) || !make_map(&mk, a.k, a.num_tokens, a.num_heads) ||
-        !make_map(&mv, a.v, a.num_tokens, a.num_heads))
+    if (!make_map(&mq, a.q, a.num_tokens, a.num_heads)) return cudaErrorInvalidValue;
+    if (paged) {
+        if (!make_paged_map(&mk, a.k, a.num_blocks, a.num_heads) || !make_paged_map(&mv, a.v, a.num_blocks, a.num_heads))
+            return cudaErrorInvalidValue;
+    } else if (!make_map(&mk, a.k, a.num_tokens, a.num_heads) || !make_map(&mv, a.v, a.num_tokens, a.num_heads)) {
         return cudaErrorInvalidValue;
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(swa_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    });
-    if (attr != cudaSuccess) return attr;
+    }
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -518,16 +659,17 @@ cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream)
     P.window = a.window;
     P.causal = a.causal;
     P.chunk = a.chunk;
-    for (int base = 0; base < a.num_seqs; base += MAX_SEQS) {
-        P.num_seqs = std::min(MAX_SEQS, a.num_seqs - base);
-        P.cu_seqlens = a.cu_seqlens + base;
-        const long long tiles_upper = (long long)P.num_seqs * ((a.max_seqlen + 2 * BM - 1) / (2 * BM)) * a.num_heads;
-        const int grid = (int)std::max<long long>(1, std::min<long long>(sms, tiles_upper));
-        swa_prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mq, mk, mv, P);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    P.context_lens = nullptr;
+    P.block_tables = nullptr;
+    P.rel_bias = a.rel_bias;
+    P.num_buckets = a.rel_bias ? a.num_buckets : 0;
+    P.mbps = a.mbps;
+    P.num_blocks = a.num_blocks;
+    const bool bias = a.rel_bias != nullptr;
+    if (paged) return bias ? launch_cfg<true, true>(mq, mk, mv, P, a, sms, stream)
+                           : launch_cfg<true, false>(mq, mk, mv, P, a, sms, stream);
+    return bias ? launch_cfg<false, true>(mq, mk, mv, P, a, sms, stream)
+                : launch_cfg<false, false>(mq, mk, mv, P, a, sms, stream);
 }
 
 }  // namespace pka

@@ -162,3 +162,37 @@ def test_multi_decode_argument_checks_need_no_gpu(lib):
               prob(num_seqs=1, workspace=ws * 2, workspace_bytes=wsb, bias_table=fake * 4, num_buckets=4,
                    **dict(bufs, out=fake * 2)))
     assert f(two, 2, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_UNSUPPORTED                 # two tables
+
+
+def test_biased_and_paged_prefill_argument_checks_need_no_gpu(lib):
+    fake = 4096
+    b = lib.pka_prefill_biased
+    #        out   q     k     v     cu    S  T  Lmax H   D   W   c  rel  B  scale  dt
+    assert b(NULL, NULL, NULL, NULL, NULL, 0, 0, 0, 12, 64, -1, 0, fake, 4, 0.125, 2, NULL, NULL) == pka.PKA_OK
+    assert b(NULL, NULL, NULL, NULL, NULL, 0, 0, 0, 12, 64, -1, 0, NULL, 4, 0.125, 2, NULL, NULL) == \
+        pka.PKA_ERR_INVALID_ARG                                                    # no table
+    assert b(NULL, NULL, NULL, NULL, NULL, 0, 0, 0, 12, 64, -1, 0, fake, 0, 0.125, 2, NULL, NULL) == \
+        pka.PKA_ERR_INVALID_ARG                                                    # no buckets
+    assert b(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, fake, 4, 0.125, 1, NULL, NULL) == \
+        pka.PKA_ERR_UNSUPPORTED                                                    # f16
+    assert b(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, fake, 4, 0.125, 2, NULL, NULL) == \
+        pka.PKA_ERR_INVALID_ARG                                                    # NULL buffers
+    p = lib.pka_paged_prefill
+
+    def paged(**kw):
+        a = dict(out=NULL, q=NULL, kc=NULL, vc=NULL, bt=NULL, cu=NULL, cl=NULL, S=0, T=0, Lq=0, H=16, D=64, bs=16,
+                 mbps=8, nb=32, W=-1, causal=1, rel=NULL, B=0, scale=0.125, dt=2)
+        a.update(kw)
+        return p(a["out"], a["q"], a["kc"], a["vc"], a["bt"], a["cu"], a["cl"], a["S"], a["T"], a["Lq"], a["H"],
+                 a["D"], a["bs"], a["mbps"], a["nb"], a["W"], a["causal"], a["rel"], a["B"], a["scale"], a["dt"],
+                 NULL, NULL)
+
+    assert paged() == pka.PKA_OK
+    assert paged(bs=32) == pka.PKA_ERR_UNSUPPORTED
+    assert paged(D=128) == pka.PKA_ERR_UNSUPPORTED
+    assert paged(mbps=0) == pka.PKA_ERR_INVALID_ARG
+    assert paged(rel=fake, B=0) == pka.PKA_ERR_INVALID_ARG
+    assert paged(W=0) == pka.PKA_ERR_INVALID_ARG
+    bufs = dict(out=fake, q=fake, kc=fake, vc=fake, cu=fake, S=1, T=4, Lq=4)
+    assert paged(**bufs) == pka.PKA_ERR_INVALID_ARG                                 # no block table
+    assert paged(**dict(bufs, bt=fake, cl=fake + 2)) == pka.PKA_ERR_INVALID_ARG     # misaligned lengths

@@ -113,3 +113,166 @@ def test_chunked_prefill_workload_sampled(cuda_lib):
     rows = np.array(rows, dtype=np.int64)
     ref = oracle.prefill_chunked(q, k, v, case.cu_seqlens, case.chunk, case.causal, case.scale, BF16, rows=rows)
     _check(to_f64(got[rows], BF16), ref, "chunked workload")
+
+
+# ---------------------------------------------------------------------------
+# relative-position bias in the scores
+# ---------------------------------------------------------------------------
+def run_gpu_biased(pka, case):
+    import torch
+    if case.device_qkv is not None:
+        q, k, v = case.device_qkv
+    else:
+        q, k, v = (to_dev(a, case.dtype) for a in (case.q, case.k, case.v))
+    out = torch.empty_like(q)
+    cu = torch.from_numpy(case.cu_seqlens).cuda()
+    rel = torch.from_numpy(case.rel_bias).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pka.prefill_biased(out, q, k, v, cu, case.max_seqlen, rel, case.window, case.causal, case.scale, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return out
+
+
+@pytest.mark.parametrize("window", [-1, 1, 64, 300])
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("buckets", [1, 5, 129])
+def test_biased_prefill_small_parity(cuda_lib, window, causal, buckets):
+    lens = [1, 2, 127, 128, 129, 255, 300, 513]
+    case = synth.make_prefill_case("biased", 300 + max(window, 0) + causal + buckets, lens, 3, 64, window, causal,
+                                   BF16, scale=1 / 8)
+    case.rel_bias = synth.rel_bias_table(buckets, 3, buckets) * np.float32(2.0)
+    got = to_f64(run_gpu_biased(cuda_lib, case), BF16)
+    ref = oracle.prefill_biased(case.q, case.k, case.v, case.cu_seqlens, window, causal, case.scale, BF16,
+                                case.rel_bias)
+    _check(got, ref, f"biased W={window} causal={causal} B={buckets}")
+
+
+def test_biased_prefill_t5_encoder_workload_sampled(cuda_lib):
+    """The T5-large-shaped encoder (256 x 512 tokens, 16 heads, bias table
+    [16, 257]) at full size, checked on sampled rows."""
+    case = synth.t5_encoder_prefill_workload(device="cuda")
+    got = run_gpu_biased(cuda_lib, case)
+    q, k, v = (to_host_storage(t, BF16) for t in case.device_qkv)
+    rows = _sample_rows(case, np.random.default_rng(410), per_seq=8)
+    ref = oracle.prefill_biased(q, k, v, case.cu_seqlens, -1, 0, case.scale, BF16, case.rel_bias, rows=rows)
+    _check(to_f64(got[rows], BF16), ref, "t5 encoder")
+
+
+# ---------------------------------------------------------------------------
+# prefill against the paged cache
+# ---------------------------------------------------------------------------
+class GpuPagedPrefill:
+    """A PagedPrefillCase resident on the GPU: caches filled by the library's
+    reshape_and_cache, queries packed."""
+
+    def __init__(self, pc, pka):
+        import torch
+        from helpers import GpuDecode
+        self.pc = pc
+        self.pka = pka
+        self.cache = GpuDecode(pc.cache, pka)
+        self.q = pc.device_q if pc.device_q is not None else to_dev(pc.q, pc.dtype)
+        self.cu = torch.from_numpy(pc.cu_seqlens_q).cuda()
+        self.rel = torch.from_numpy(pc.rel_bias).cuda() if pc.rel_bias is not None else None
+        self.out = torch.empty_like(self.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def run(self):
+        import torch
+        g, pc = self.cache, self.pc
+        self.pka.paged_prefill(self.out, self.q, g.k_cache, g.v_cache, g.block_tables, self.cu, g.context_lens,
+                               pc.max_query_len, pc.window, pc.causal, self.rel, pc.scale, status=self.status)
+        torch.cuda.synchronize()
+        return self.out
+
+    def host_caches(self):
+        return to_host_storage(self.cache.k_cache, self.pc.dtype), to_host_storage(self.cache.v_cache, self.pc.dtype)
+
+
+def oracle_paged(gp, rows=None, q=None):
+    pc = gp.pc
+    kc, vc = gp.host_caches()
+    return oracle.paged_prefill(pc.q if q is None else q, kc, vc, pc.cache.block_tables, pc.cu_seqlens_q,
+                                pc.cache.context_lens, pc.window, pc.causal, pc.scale, 16, pc.dtype,
+                                rel_bias=pc.rel_bias, rows=rows)
+
+
+PAGED_CTX = (1, 15, 16, 17, 130, 300, 520, 700, 2000)
+PAGED_QL = (1, 15, 5, 17, 130, 256, 257, 40, 600)
+
+
+@pytest.mark.parametrize("window", [-1, 1, 40, 300])
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("buckets", [0, 129])
+def test_paged_prefill_small_parity(cuda_lib, window, causal, buckets):
+    pc = synth.make_paged_prefill_case("paged", 500 + max(window, 0) + causal + buckets, BF16, PAGED_CTX, PAGED_QL,
+                                       3, 64, window, causal, buckets, scale=1 / 8, pool_blocks=400)
+    gp = GpuPagedPrefill(pc, cuda_lib)
+    got = to_f64(gp.run(), BF16)
+    _check(got, oracle_paged(gp), f"paged W={window} causal={causal} B={buckets}")
+    assert int(gp.status.item()) == 0
+
+
+@pytest.mark.parametrize("window", [-1, 3])
+def test_paged_prefill_rows_without_keys_are_zero(cuda_lib, window):
+    """Non-causal: more query rows than keys, and a sequence with no keys."""
+    pc = synth.make_paged_prefill_case("paged-edge", 520 + window, BF16, (5, 0, 30, 200), (9, 3, 4, 300), 2, 64,
+                                       window, 0, 4, scale=1 / 8)
+    gp = GpuPagedPrefill(pc, cuda_lib)
+    gp.out.fill_(7.0)
+    got = to_f64(gp.run(), BF16)
+    ref = oracle_paged(gp)
+    _check(got, ref, f"paged edge W={window}")
+    assert np.all(got[9:12] == 0.0)
+
+
+def test_paged_prefill_ignores_cache_tails_and_evicted_blocks(cuda_lib):
+    """Cache rows past each context hold NaN, and the block-table entries of
+    blocks before every row's window hold an id past the pool (evicted): the
+    result is unchanged and no status bit is set, so neither was used."""
+    import torch
+    W = 50
+    pc = synth.make_paged_prefill_case("paged-evict", 530, BF16, (700, 333, 129), (100, 20, 129), 2, 64, W, 1, 129,
+                                       scale=1 / 8, pool_blocks=120)
+    gp = GpuPagedPrefill(pc, cuda_lib)
+    ref = to_f64(gp.run(), BF16).copy()
+    bt = pc.cache.block_tables.copy()
+    kc, vc = gp.cache.k_cache, gp.cache.v_cache
+    for s in range(pc.num_seqs):
+        ctx, Lq = int(pc.cache.context_lens[s]), int(pc.query_lens[s])
+        last = (ctx - 1) // 16
+        blk = int(bt[s, last])
+        kc[blk, :, ctx % 16 or 16:] = float("nan")
+        vc[blk, :, ctx % 16 or 16:] = float("nan")
+        first_kept = max(0, ctx - Lq - W + 1)             # the earliest key any row keeps
+        bt[s, :first_kept // 16] = 1 << 30
+    gp.cache.block_tables.copy_(torch.from_numpy(bt))
+    got = to_f64(gp.run(), BF16)
+    assert np.isfinite(got).all()
+    assert int(gp.status.item()) == 0
+    assert max_err(got, ref) == 0.0
+
+
+def test_paged_prefill_t5_workload_sampled(cuda_lib):
+    """A prompt chunk of each sequence of the T5-large-shaped decode workload:
+    causal with the T5 bias over the self-attention cache, and unmasked over
+    the encoder cache, checked on sampled rows."""
+    import torch
+    self_c, cross_c = synth.t5_paged_prefill_workload(device="cuda")
+    rng = np.random.default_rng(540)
+    for pc in (self_c, cross_c):
+        gp = GpuPagedPrefill(pc, cuda_lib)
+        got = gp.run()
+        assert int(gp.status.item()) == 0
+        cu = pc.cu_seqlens_q
+        rows = []
+        for b in range(pc.num_seqs):
+            a, e = int(cu[b]), int(cu[b + 1])
+            pick = {a, e - 1} | set((a + rng.choice(e - a, size=min(e - a, 6), replace=False)).tolist())
+            rows += sorted(pick)
+        rows = np.array(rows, dtype=np.int64)
+        ref = oracle_paged(gp, rows=rows, q=to_host_storage(gp.q, BF16))
+        _check(to_f64(got[rows], BF16), ref, pc.name)
+        del gp
+        torch.cuda.empty_cache()
