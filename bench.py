@@ -6,15 +6,17 @@
 Prints ONE JSON line (rank 0).  A step is one pass of the hot path over one
 batch of seeded synthetic input, already resident in HBM:
 
-  t5-small-decode (default)  reshape_and_cache of each sequence's new token,
-        then biased paged decode: 64 seqs x 8 heads x 64, bf16, contexts
-        U[1,512], T5 bias [64,8,512] materialised from an [8,129] table.
+  t5-small-decode (default)  each sequence's new token appended to the cache
+        and the biased paged decode, in one launch: 64 seqs x 8 heads x 64,
+        bf16, contexts U[1,512], T5 bias [64,8,512] materialised from an
+        [8,129] table.
   tiny-decode        4 x 2 x 64 fp32, contexts U[1,64], Gaussian bias.
   t5-large-decode    decoder self-attention (256 x 16 x 64 bf16, contexts
         U[1,2048], T5 bias padded to 2048) + encoder cross-attention (own block
-        table, encoder length 512, no bias), both after their reshape_and_cache;
-        the two attention calls go out as one fused launch
-        (--separate-launches: one each).
+        table, encoder length 512, no bias), in one launch that also appends
+        the decoder's new token (the encoder cache is static).
+  --separate-launches: reshape_and_cache of every side's new token, then one
+        decode launch per side (the unfused step).
   long-ctx-decode    512 x 16 x 128 fp16, contexts log-U[16,8192], causal
         window 4096, bias [512,16,8192] N(0,0.25) NaN-padded.
   encoder-prefill    32 packed sequences U[128,8192], 12 heads x 64 bf16,
@@ -270,6 +272,7 @@ class DecodeSide:
         self.table = (torch.from_numpy(case.bias_table).to(device) if getattr(case, "bias_table", None) is not None
                       else None)
         self.use_table = False
+        self.append = True            # the step appends the newest token (not for the static encoder cache)
         self.out = torch.empty((case.num_seqs, H, D), dtype=tdt, device=device)
         self.ws = torch.zeros(pka.paged_attn_decode_workspace_size(case.num_seqs, H, D, case.max_context_len,
                                                                    case.window), dtype=torch.uint8, device=device)
@@ -296,6 +299,8 @@ class DecodeSide:
         c = self.case
         pr = dict(out=self.out, q=self.q, k_cache=self.kc, v_cache=self.vc, block_tables=self.bt, context_lens=self.cl,
                   sliding_window=c.window, scale=c.scale, max_context_len=c.max_context_len, workspace=self.ws)
+        if self.append:
+            pr["key_new"], pr["value_new"] = self.new_k, self.new_v
         if bias_on and self.use_table and self.table is not None:
             pr["bias_table"] = self.table
         elif bias_on and self.bias is not None:
@@ -314,8 +319,12 @@ class DecodeSide:
 
 
 def decode_all(pka, sides, fused, bias_on=True, events=None, k=0):
-    """The step's attention calls: one fused launch over all sides, or one
-    launch per side; events[j] brackets launch j."""
+    """The step: fused, one launch that appends each appending side's newest
+    token and decodes all sides; else reshape_and_cache of every side's new
+    token, then one decode launch per side.  events[j] brackets decode launch j."""
+    if not fused:
+        for s in sides:
+            s.reshape(pka)
     if fused:
         if events is not None:
             events[0][0][k].record()
@@ -329,6 +338,11 @@ def decode_all(pka, sides, fused, bias_on=True, events=None, k=0):
         s.decode(pka, bias_on and s.bias is not None)
         if events is not None:
             events[j][1][k].record()
+
+
+def rot_sides_cross(rot):
+    """The cross-attention side of every rotated copy (the second side)."""
+    return [sides[1] for sides in rot]
 
 
 def build_decode_sides(workload, device, on_device_draw, num_seqs=None):
@@ -363,12 +377,13 @@ def run_decode(args, rank, world, local, peaks):
     rot = [sides] + [[s.clone() for s in sides] for _ in range(copies - 1)]
     torch.cuda.synchronize()
 
-    fused = len(sides) > 1 and not args.separate_launches
+    fused = not args.separate_launches
     nlaunch = 1 if fused else len(sides)
+    if len(sides) > 1:
+        for s in rot_sides_cross(rot):
+            s.append = False
 
     def step(i, bias_on=True, events=None):
-        for s in rot[i % copies]:
-            s.reshape(pka)
         decode_all(pka, rot[i % copies], fused, bias_on, events, i)
 
     clocks = ClockSampler(gpu_id(local))
@@ -434,10 +449,11 @@ def run_decode(args, rank, world, local, peaks):
                     if c.bias is not None else None for c in cases],
            "l2": f"inputs rotated over {copies} copies ({per_copy * copies / 2**20:.0f} MiB > L2)"
            if copies > 1 else f"inputs {per_copy / 2**20:.0f} MiB > L2", "parallelism": f"replicas x{world}",
-           "attention_launches": "one fused launch (self + cross)" if fused else "one per attention type"}
+           "launches_per_step": ("one: append of the newest token + decode" + (" of self and cross" if len(sides) > 1 else ""))
+           if fused else "reshape_and_cache per side, then one decode per side"}
     return {"value": value, "unit": "GB/s", "ms_per_step": ms_step, "dtype": synth.DTYPE_NAMES[cases[0].dtype],
             "config": cfg, "roofline": roof, "e2e": e2e, "clocks": clk,
-            "gpu_launches": K * (len(sides) + nlaunch), "extra": extra, "cases": cases}
+            "gpu_launches": K * (1 if fused else 2 * len(sides)), "extra": extra, "cases": cases}
 
 
 def decode_e2e(args, sides, pka, step_bytes, world, fused=False):
@@ -447,7 +463,8 @@ def decode_e2e(args, sides, pka, step_bytes, world, fused=False):
     host_in = []
     h2d = 0
     for s in sides:
-        names = ["q", "new_k", "new_v", "slots", "bt", "cl"]
+        names = (["q", "new_k", "new_v", "bt", "cl"] if s.append else ["q", "bt", "cl"]) if fused else \
+            ["q", "new_k", "new_v", "slots", "bt", "cl"]
         if s.use_table and s.table is not None:
             names.append("table")
         elif s.bias is not None:
@@ -467,7 +484,6 @@ def decode_e2e(args, sides, pka, step_bytes, world, fused=False):
         for s, pairs in zip(sides, host_in):
             for h, d in pairs:
                 d.copy_(h, non_blocking=True)
-            s.reshape(pka)
         decode_all(pka, sides, fused)
         for s, o in zip(sides, outs):
             o.copy_(s.out, non_blocking=True)
@@ -892,7 +908,7 @@ def main():
                     choices=sorted(DECODE_WORKLOADS) + list(PREFILL_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--separate-launches", action="store_true",
-                    help="t5-large-decode: one decode launch per attention type instead of one fused launch")
+                    help="decode workloads: reshape_and_cache launches, then one decode launch per attention type")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)

@@ -205,6 +205,22 @@ PKA_API pka_status pka_paged_attn_decode_t5bias(void *out, const void *q, const 
  *                 pka_paged_attn_decode; the problems' workspaces must not
  *                 overlap.  PKA_ERR_WORKSPACE if any is missing or short.
  *   status        one int32 device word or NULL for all problems
+ *   key_new, value_new  optional, 16-byte aligned: the K and V rows of each
+ *                 sequence's newest token, position ctx_s - 1, fused append.
+ *                 The launch first writes them to the cache at
+ *                   k_cache[block_tables[s, (ctx_s-1) / 16], h, (ctx_s-1) % 16, :]
+ *                 (v_cache likewise) — what pka_reshape_and_cache does with
+ *                 that slot — and attends with them, so one launch does the
+ *                 scatter and the decode of a step ("Add Encoder-decoder model
+ *                 support and T5 Model support": KV caching of the new token
+ *                 precedes its attention).  Results and cache contents are
+ *                 bit-identical to pka_reshape_and_cache followed by the
+ *                 decode.  The caches of such a problem are written (the
+ *                 const qualifier notwithstanding); the block holding
+ *                 position ctx_s - 1 must belong to sequence s alone, and no
+ *                 other problem of the launch may read it.  ctx_s == 0
+ *                 appends nothing.  A block id out of range sets
+ *                 PKA_DEVCHK_BLOCK_ID and skips the write.
  * Problems with num_seqs == 0 are skipped.  The problems' out arrays must
  * not overlap (PKA_ERR_INVALID_ARG).  Errors are those of the single-problem calls, checked per
  * problem before anything is enqueued.
@@ -228,6 +244,8 @@ typedef struct {
     int max_context_len;
     void *workspace;
     size_t workspace_bytes;
+    const void *key_new;         /* or NULL: [num_seqs, num_heads, head_dim] of dtype */
+    const void *value_new;       /* NULL exactly when key_new is */
 } pka_decode_problem;
 
 PKA_API pka_status pka_paged_attn_decode_multi(const pka_decode_problem *problems, int num_problems,

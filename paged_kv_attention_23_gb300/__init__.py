@@ -40,7 +40,8 @@ class DecodeProblem(ctypes.Structure):
                 ("sliding_window", ctypes.c_int), ("scale", ctypes.c_float), ("num_seqs", ctypes.c_int),
                 ("max_blocks_per_seq", ctypes.c_int), ("bias_row_stride", ctypes.c_int),
                 ("num_blocks", ctypes.c_int), ("max_context_len", ctypes.c_int),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("key_new", ctypes.c_void_p), ("value_new", ctypes.c_void_p)]
 
 _lib = None
 _lock = threading.Lock()
@@ -252,8 +253,11 @@ def paged_attn_decode_multi(problems, status=None, stream=None):
     step's self- and cross-attention).  ``problems`` is a sequence of dicts
     with the keyword arguments of ``paged_attn_decode`` — out, q, k_cache,
     v_cache, block_tables, context_lens and optionally attn_bias or
-    bias_table, sliding_window, scale, max_context_len, workspace.  All share
-    num_heads, head_dim, block size and dtype; each gets its own workspace."""
+    bias_table, sliding_window, scale, max_context_len, workspace — plus
+    optionally key_new / value_new [S, H, D]: the newest token's K/V, written
+    to the cache at position ctx-1 and attended in the same launch.  All
+    share num_heads, head_dim, block size and dtype; each gets its own
+    workspace."""
     torch = _torch()
     lib = load()
     arr = (DecodeProblem * max(1, len(problems)))()
@@ -291,9 +295,12 @@ def paged_attn_decode_multi(problems, status=None, stream=None):
             dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
             ws = _default_ws.setdefault((dev, "multi", i), DecodeWorkspace(q.device)).get(need)
         keep.append(ws)
+        kn, vn = pr.get("key_new"), pr.get("value_new")
+        if kn is not None or vn is not None:
+            _need(kn, "key_new", q.dtype, 3); _need(vn, "value_new", q.dtype, 3)
         arr[i] = DecodeProblem(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(cl), _ptr(bias), _ptr(table),
                                table.shape[1] if table is not None else 0, w, float(scale), S, mbps, stride, nb,
-                               int(mcl), _ptr(ws), ws.numel() * ws.element_size())
+                               int(mcl), _ptr(ws), ws.numel() * ws.element_size(), _ptr(kn), _ptr(vn))
     if not problems:
         raise ValueError("paged_attn_decode_multi needs at least one problem")
     _check("pka_paged_attn_decode_multi",

@@ -79,6 +79,7 @@ struct Prob {
     const int32_t *block_tables, *context_lens;
     const float *bias;
     const float *bias_table;     // [H, num_buckets] T5 relative-position table, or NULL
+    const unsigned char *k_new, *v_new;   // [S, H, D] newest token's K/V (position ctx-1), or NULL
     unsigned *counters;
     float2 *ws_ml;
     float *ws_acc;
@@ -318,6 +319,20 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
         const Unit cu = unit_of(u, cum, ctxs, P);
         const Prob &CP = P.pr[cu.prob];
         const bool has_bias = CP.bias != nullptr, has_table = CP.bias_table != nullptr;
+        // append: the sequence's newest token (position ctx-1) lies in the last
+        // block of its last partition; its K/V row comes from k_new / v_new,
+        // replaces the cache row in the staged block and is written to the cache
+        const bool append = CP.k_new != nullptr && cu.p == cu.npart - 1 && cu.nb > 0;
+        uint4 kn = make_uint4(0u, 0u, 0u, 0u), vn = kn;
+        int app_phys = -1;
+        if (append) {
+            const size_t rowoff = ((size_t)cu.gs * P.H + cu.h) * R::ROW;
+            if (lane < R::NC) {
+                kn = __ldg(reinterpret_cast<const uint4 *>(CP.k_new + rowoff) + lane);
+                vn = __ldg(reinterpret_cast<const uint4 *>(CP.v_new + rowoff) + lane);
+            }
+            app_phys = __ldg(CP.block_tables + (size_t)cu.gs * CP.mbps + (cu.ctx - 1) / BS);
+        }
         m_run = -INFINITY;
         l_run = 0.f;
 #pragma unroll
@@ -330,6 +345,23 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
             if (!mbar_wait_bounded(smem_u32(&bars[stage]), (consumed / NSTAGE) & 1)) {
                 if (lane == 0) flag_status(P.status, PKA_DEVCHK_TIMEOUT);
                 return;
+            }
+            if (append && cb == cu.nb - 1) {
+                const int r = (cu.ctx - 1) % BS;
+                if (lane < R::NC) {
+                    unsigned char *row = stages + stage * R::STAGE + r * R::ROW;
+                    reinterpret_cast<uint4 *>(row + R::K_OFF)[lane] = kn;
+                    reinterpret_cast<uint4 *>(row + R::V_OFF)[lane] = vn;
+                    if ((unsigned)app_phys < (unsigned)CP.num_blocks) {
+                        const size_t off = (((size_t)app_phys * P.H + cu.h) * BS + r) * R::ROW;
+                        reinterpret_cast<uint4 *>(const_cast<unsigned char *>(CP.k_cache) + off)[lane] = kn;
+                        reinterpret_cast<uint4 *>(const_cast<unsigned char *>(CP.v_cache) + off)[lane] = vn;
+                    } else if (lane == 0) {
+                        flag_status(P.status, PKA_DEVCHK_BLOCK_ID);
+                    }
+                    fence_proxy_async();         // before a later bulk copy refills this stage
+                }
+                __syncwarp();
             }
             if (cb == 0) DT::load_q(qreg, stp + R::Q_OFF, q_first, q_rot);
             // score of key `key` (both lanes of the pair end with the full sum)
@@ -596,6 +628,8 @@ cudaError_t launch_paged_decode_multi(const DecodeArgs *a, const DecodePlan *siz
         R.bias = a[i].bias;
         R.bias_table = a[i].bias_table;
         R.num_buckets = a[i].num_buckets;
+        R.k_new = static_cast<const unsigned char *>(a[i].k_new);
+        R.v_new = static_cast<const unsigned char *>(a[i].v_new);
         R.counters = reinterpret_cast<unsigned *>(ws);
         R.ws_ml = reinterpret_cast<float2 *>(ws + round_up(shi * 4, 256));
         R.ws_acc = reinterpret_cast<float *>(ws + round_up(shi * 4, 256) + round_up(slots * 8, 256));

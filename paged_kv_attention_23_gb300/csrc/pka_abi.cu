@@ -34,6 +34,8 @@ pka_status prepare_decode(const pka_decode_problem &p, int block_size, int num_h
     if (block_size != 16) return PKA_ERR_UNSUPPORTED;
     if ((long long)p.max_context_len > (long long)p.max_blocks_per_seq * block_size) return PKA_ERR_INVALID_ARG;
     if (p.attn_bias && (p.bias_row_stride < p.max_context_len || p.bias_row_stride < 1)) return PKA_ERR_INVALID_ARG;
+    if ((p.key_new == nullptr) != (p.value_new == nullptr) || !aligned(p.key_new, 16) || !aligned(p.value_new, 16))
+        return PKA_ERR_INVALID_ARG;
     a.num_seqs = 0;
     if (p.num_seqs == 0) return PKA_OK;
     if (!p.out || !p.q || !p.k_cache || !p.v_cache || !p.block_tables || !p.context_lens) return PKA_ERR_INVALID_ARG;
@@ -53,6 +55,8 @@ pka_status prepare_decode(const pka_decode_problem &p, int block_size, int num_h
     a.bias = p.attn_bias;
     a.bias_table = p.bias_table;
     a.num_buckets = p.bias_table ? p.num_buckets : 0;
+    a.k_new = p.key_new;
+    a.v_new = p.value_new;
     a.status = status;
     a.scale = p.scale;
     a.window = p.sliding_window;

@@ -36,6 +36,7 @@ struct DecodeArgs {
     const float *bias;
     const float *bias_table;   // T5 relative-position table [H, num_buckets] or NULL
     int num_buckets;
+    const void *k_new, *v_new; // [S, H, D] newest token's K/V to append at position ctx-1, or NULL
     int32_t *status;
     float scale;
     int window, num_seqs, num_heads, head_dim, max_blocks_per_seq, num_blocks, max_context_len;

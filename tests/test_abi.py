@@ -196,3 +196,15 @@ def test_biased_and_paged_prefill_argument_checks_need_no_gpu(lib):
     bufs = dict(out=fake, q=fake, kc=fake, vc=fake, cu=fake, S=1, T=4, Lq=4)
     assert paged(**bufs) == pka.PKA_ERR_INVALID_ARG                                 # no block table
     assert paged(**dict(bufs, bt=fake, cl=fake + 2)) == pka.PKA_ERR_INVALID_ARG     # misaligned lengths
+
+
+def test_multi_decode_append_needs_both_rows(lib):
+    f = lib.pka_paged_attn_decode_multi
+    P = pka.DecodeProblem
+    fake = 4096
+    bufs = dict(out=fake, q=fake, k_cache=fake, v_cache=fake, block_tables=fake, context_lens=fake, num_seqs=1,
+                sliding_window=-1, scale=0.125, max_blocks_per_seq=4, num_blocks=8, max_context_len=64)
+    one = (P * 1)(P(key_new=fake, **bufs))
+    assert f(one, 1, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG            # value_new missing
+    one = (P * 1)(P(key_new=fake + 8, value_new=fake, **bufs))
+    assert f(one, 1, 16, 2, 64, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG            # misaligned

@@ -389,3 +389,71 @@ def test_multi_rejects_bad_problem_sets(cuda_lib):
     with pytest.raises(ValueError):                                       # different head counts
         c = synth.make_decode_case("multi-e", 75, BF16, 3, 4, 64)
         cuda_lib.paged_attn_decode_multi([ga.problem("none"), GpuDecode(c, cuda_lib).problem("none")])
+
+
+# ---------------------------------------------------------------------------
+# fused append: the newest token's K/V written and attended in one launch
+# ---------------------------------------------------------------------------
+def _append_state(case, pka):
+    """Caches holding every token but each sequence's newest (those rows NaN),
+    and the newest rows as key_new / value_new [S, H, D]."""
+    import torch
+    H, D, bs = case.num_heads, case.head_dim, case.block_size
+    tdt = torch_dtype(case.dtype)
+    key, value = to_dev(case.key, case.dtype), to_dev(case.value, case.dtype)
+    kc = torch.zeros((case.num_blocks, H, bs, D), dtype=tdt, device="cuda")
+    vc = torch.zeros_like(kc)
+    slots = case.slot_mapping.copy()
+    newest = np.where(case.context_lens > 0, case.tok_offsets[1:] - 1, -1)
+    have = newest >= 0
+    slots[newest[have]] = -1
+    pka.reshape_and_cache(key, value, kc, vc, torch.from_numpy(slots).cuda())
+    ns = torch.from_numpy(case.slot_mapping[newest[have]]).cuda()
+    kc[ns // bs, :, ns % bs] = float("nan")
+    vc[ns // bs, :, ns % bs] = float("nan")
+    idx = torch.from_numpy(np.where(have, newest, 0).astype(np.int64)).cuda()
+    k_new, v_new = key[idx].contiguous(), value[idx].contiguous()
+    return kc, vc, k_new, v_new
+
+
+@pytest.mark.parametrize("dtype,D,window", [(BF16, 64, -1), (BF16, 64, 40), (F32, 128, 5), (F16, 128, -1)])
+def test_multi_append_equals_scatter_then_decode(cuda_lib, dtype, D, window):
+    """Outputs and cache bytes of the fused append are bit-identical to
+    reshape_and_cache followed by the decode, from caches whose newest rows
+    held NaN; and the decode matches the oracle."""
+    import torch
+    case = synth.make_decode_case("append", 90 + D + max(window, 0), dtype, len(EDGE_CTX), 3, D,
+                                  context_lens=np.array(EDGE_CTX), pool_blocks=160, window=window, bias="gauss",
+                                  scale=0.2)
+    g = GpuDecode(case, cuda_lib)                       # every token scattered by reshape_and_cache
+    ref_out = g.run().clone()
+    kc, vc, k_new, v_new = _append_state(case, cuda_lib)
+    out = torch.empty_like(ref_out)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pr = dict(g.problem("bias"), out=out, k_cache=kc, v_cache=vc, key_new=k_new, value_new=v_new)
+    cuda_lib.paged_attn_decode_multi([pr], status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(out.view(torch.uint8), ref_out.view(torch.uint8))
+    assert torch.equal(kc.view(torch.uint8), g.k_cache.view(torch.uint8))
+    assert torch.equal(vc.view(torch.uint8), g.v_cache.view(torch.uint8))
+    _check(to_f64(out, dtype), oracle_decode(case), dtype, "append")
+
+
+def test_multi_append_self_with_unappended_cross(cuda_lib):
+    """The T5-large-shaped step in one launch: the self-attention problem
+    appends its newest token, the cross-attention problem does not."""
+    import torch
+    sc, cc = synth.decode_workload(3, num_seqs=48), synth.cross_workload(num_seqs=48)
+    gs, gc = GpuDecode(sc, cuda_lib), GpuDecode(cc, cuda_lib)
+    cuda_lib.paged_attn_decode_multi([gs.problem("bias"), gc.problem("none")])   # same plan, scattered caches
+    ref_s, ref_c = gs.out.clone(), gc.out.clone()
+    kc, vc, k_new, v_new = _append_state(sc, cuda_lib)
+    out_s, out_c = torch.empty_like(ref_s), torch.empty_like(ref_c)
+    cuda_lib.paged_attn_decode_multi([dict(gs.problem("bias"), out=out_s, k_cache=kc, v_cache=vc, key_new=k_new,
+                                           value_new=v_new), dict(gc.problem("none"), out=out_c)])
+    torch.cuda.synchronize()
+    assert torch.equal(out_s.view(torch.int16), ref_s.view(torch.int16))
+    assert torch.equal(out_c.view(torch.int16), ref_c.view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), gs.k_cache.view(torch.int16))
+    _check(to_f64(out_s, BF16), oracle_decode(sc), BF16, "append self")
