@@ -61,6 +61,7 @@ template <typename T, int D> struct Tr {
     static constexpr int RPI = 32 / NC;              // V rows per warp-wide 16-byte load
     static constexpr int PV_IT = BS / RPI;           // P.V iterations per block
     static constexpr int DPL = D / 32;               // dims per lane in the partition merge
+    static constexpr int MCH = 32 / DPL;             // split-K partials merged per L2 round trip
     // stage layout
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = CHUNK;
@@ -438,38 +439,60 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
         old = __shfl_sync(kFull, old, 0);
         if (old != (unsigned)(cu.npart - 1)) continue;
 
-        // last partition of (s, h): merge, write out, return the slots to zero
+        // last partition of (s, h): merge, write out, return the slots to zero.
+        // Every load of a chunk of up to R::MCH partials is issued before any is
+        // used (one L2 round trip per chunk); lane i holds partial i's (m, l).
         const size_t base = sh * CP.max_parts;
-        float M = -INFINITY;
-        for (int i = lane; i < cu.npart; i += 32) M = fmaxf(M, __ldcg(CP.ws_ml + base + i).x);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-        float L = 0.f;
-        for (int i = lane; i < cu.npart; i += 32) {
-            const float2 ml = __ldcg(CP.ws_ml + base + i);
-            L += ml.y * ex2(ml.x - M);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
+        float M = -INFINITY, L = 0.f;
         float o_acc[R::DPL];
 #pragma unroll
         for (int e = 0; e < R::DPL; ++e) o_acc[e] = 0.f;
-        for (int i = 0; i < cu.npart; ++i) {
-            const float w = ex2(__ldcg(CP.ws_ml + base + i).x - M);
-            float *src = CP.ws_acc + (base + i) * D + lane * R::DPL;
-            if constexpr (R::DPL == 4) {
-                const float4 a4 = __ldcg(reinterpret_cast<const float4 *>(src));
-                o_acc[0] = fmaf(w, a4.x, o_acc[0]); o_acc[1] = fmaf(w, a4.y, o_acc[1]);
-                o_acc[2] = fmaf(w, a4.z, o_acc[2]); o_acc[3] = fmaf(w, a4.w, o_acc[3]);
-                __stcg(reinterpret_cast<float4 *>(src), make_float4(0.f, 0.f, 0.f, 0.f));
-            } else {
-                const float2 a2 = __ldcg(reinterpret_cast<const float2 *>(src));
-                o_acc[0] = fmaf(w, a2.x, o_acc[0]); o_acc[1] = fmaf(w, a2.y, o_acc[1]);
-                __stcg(reinterpret_cast<float2 *>(src), make_float2(0.f, 0.f));
+        for (int c0 = 0; c0 < cu.npart; c0 += R::MCH) {
+            const int n = min(R::MCH, cu.npart - c0);
+            float2 ml = make_float2(-INFINITY, 0.f);
+            if (lane < n) ml = __ldcg(CP.ws_ml + base + c0 + lane);
+            float a[R::MCH][R::DPL];
+#pragma unroll
+            for (int i = 0; i < R::MCH; ++i) {
+                const float *src = CP.ws_acc + (base + c0 + i) * D + lane * R::DPL;
+                if constexpr (R::DPL == 4) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (i < n) v = __ldcg(reinterpret_cast<const float4 *>(src));
+                    a[i][0] = v.x; a[i][1] = v.y; a[i][2] = v.z; a[i][3] = v.w;
+                } else {
+                    float2 v = make_float2(0.f, 0.f);
+                    if (i < n) v = __ldcg(reinterpret_cast<const float2 *>(src));
+                    a[i][0] = v.x; a[i][1] = v.y;
+                }
             }
+            float mc = ml.x;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(kFull, mc, o));
+            const float Mn = fmaxf(M, mc);
+            const float corr = M == -INFINITY ? 0.f : ex2(M - Mn);
+            const float w = (lane < n && Mn != -INFINITY) ? ex2(ml.x - Mn) : 0.f;
+            float lc = ml.y * w;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lc += __shfl_xor_sync(kFull, lc, o);
+            L = L * corr + lc;
+#pragma unroll
+            for (int e = 0; e < R::DPL; ++e) o_acc[e] *= corr;
+#pragma unroll
+            for (int i = 0; i < R::MCH; ++i) {
+                const float wi = __shfl_sync(kFull, w, i);
+#pragma unroll
+                for (int e = 0; e < R::DPL; ++e) o_acc[e] = fmaf(wi, a[i][e], o_acc[e]);
+            }
+            M = Mn;
+#pragma unroll
+            for (int i = 0; i < R::MCH; ++i) {
+                if (i >= n) break;
+                float *dst0 = CP.ws_acc + (base + c0 + i) * D + lane * R::DPL;
+                if constexpr (R::DPL == 4) __stcg(reinterpret_cast<float4 *>(dst0), make_float4(0.f, 0.f, 0.f, 0.f));
+                else __stcg(reinterpret_cast<float2 *>(dst0), make_float2(0.f, 0.f));
+            }
+            if (lane < n) __stcg(CP.ws_ml + base + c0 + lane, make_float2(0.f, 0.f));
         }
-        __syncwarp();
-        for (int i = lane; i < cu.npart; i += 32) __stcg(CP.ws_ml + base + i, make_float2(0.f, 0.f));
         const float inv = L > 0.f ? 1.f / L : 0.f;
         T *dst = reinterpret_cast<T *>(static_cast<unsigned char *>(CP.out) + sh * R::ROW) + lane * R::DPL;
 #pragma unroll
