@@ -21,15 +21,15 @@
 //   warp 1      TMEM owner; with warp 10, one MMA-issuing thread per query
 //               tile (each blocks only on its own tile's barriers): per key
 //               tile, S = Q K^T (4 x 128x128x16) into that tile's S columns,
-//               then O += P V (8 x 128x64x16, V read MN-major) into its O
-//               columns.  QK of key tile j+1 is issued before PV of j, so
+//               then O += P V (8 x 128x64x16, P read from TMEM, V MN-major
+//               from shared memory) into its O columns.  QK of key tile j+1 is issued before PV of j, so
 //               scores are ready when the softmax finishes tile j.
 //   warps 2..5  softmax of query tile 0, warps 6..9 of query tile 1 (the two
 //               groups ping-pong on the tensor core): one thread per row
 //               loads its S row, frees the S columns at once, masks, takes
 //               the max (3-input max), and writes P = 2^(scale*s - m) as bf16
-//               into swizzled shared memory; the scale is folded into the
-//               exponent's FMA.  O stays in TMEM: the running max is raised
+//               pairs into the tile's P columns of TMEM (tcgen05.st); the
+//               scale is folded into the exponent's FMA.  O stays in TMEM: the running max is raised
 //               only when a row's max grows by more than 2^8, and only then
 //               is that row of O rescaled in TMEM (rows never see P > 256).
 // Every wait is bounded: on a timeout the CTA records PKA_DEVCHK_TIMEOUT,
@@ -56,11 +56,9 @@ constexpr int NTHREADS = 352;  // producer, MMA (tile 0), 2 x 4 softmax warps, M
 constexpr float RESCALE_LOG2 = 8.f;
 
 constexpr uint32_t TILE_BYTES = BM * HD * 2;             // 16 KB: one Q, K or V tile
-constexpr uint32_t P_BYTES = BM * BN * 2;                // 32 KB: P as two 64-key blocks
 constexpr uint32_t OFF_Q = 0;                             // 2 query tiles
 constexpr uint32_t OFF_KV = 2 * TILE_BYTES;               // NS x (K, V)
-constexpr uint32_t OFF_P = OFF_KV + NS * 2 * TILE_BYTES;  // 2 x P (one per query tile)
-constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr uint32_t OFF_BAR = OFF_KV + NS * 2 * TILE_BYTES;
 // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], s_empty[2], p_full[2], o_full[2], o_empty[2]
 constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NS, B_SF = 2 + 2 * NS, B_SE = B_SF + 2, B_PF = B_SE + 2,
               B_OF = B_PF + 2, B_OE = B_OF + 2, NBAR = B_OE + 2;
@@ -70,9 +68,10 @@ constexpr uint32_t SMEM_BYTES = OFF_SCHED + (6 * MAX_SEQS + 1) * 4 + 1024;   // 
 constexpr int CBS = 16;                   // paged cache block: 16 key rows of one head
 constexpr uint32_t CBLK_BYTES = CBS * HD * 2;                                  // 2 KB per block and head
 
-// TMEM columns: S of query tile w at 128 w, O of query tile w at 256 + 64 w
+// TMEM columns of query tile w: S (f32) at 128 w, O (f32) at 256 + 64 w, P
+// (bf16 pairs) at 384 + 64 w: the 512 columns exactly
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0, COL_O = 256;
+constexpr uint32_t COL_S = 0, COL_O = 256, COL_P = 384;
 
 constexpr uint32_t IDESC_QK = tc::idesc_bf16_f32(BM, BN, false, false);  // S = Q K^T, both K-major
 constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(BM, HD, false, true);   // O += P V, V is MN-major
@@ -176,27 +175,25 @@ __device__ __forceinline__ void add2(float &a0, float &a1, float y0, float y1)
         : "f"(y0), "f"(y1));
 }
 
-// P = 2^(scale * s - m) for one tile row as bf16 into the swizzled P buffer;
-// returns the f32 row sum.
-__device__ __forceinline__ float write_p_row(const float *x, float scale_log2, float mneg, uint32_t pbase, int row)
+// P = 2^(scale * s - m) for one tile row as bf16 pairs into the row's TMEM
+// lane (64 columns, key 2c in the low half of column c); returns the f32 row sum.
+__device__ __forceinline__ float write_p_tmem(const float *x, float scale_log2, float mneg, uint32_t tP)
 {
     float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int c = 0; c < BN / 8; ++c) {
-        uint32_t wv[4];
+    for (int hlf = 0; hlf < 2; ++hlf) {
+        uint32_t pk[BN / 4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int c = 0; c < BN / 4; ++c) {
+            const int i = hlf * (BN / 2) + 2 * c;
             float a0, a1;
-            fma2(x[c * 8 + 2 * e], x[c * 8 + 2 * e + 1], scale_log2, mneg, a0, a1);
+            fma2(x[i], x[i + 1], scale_log2, mneg, a0, a1);
             const float p0 = ex2(a0), p1 = ex2(a1);
-            add2(ls[(e & 1) * 2], ls[(e & 1) * 2 + 1], p0, p1);
+            add2(ls[(c & 1) * 2], ls[(c & 1) * 2 + 1], p0, p1);
             __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
-            wv[e] = *reinterpret_cast<uint32_t *>(&hb);
+            pk[c] = *reinterpret_cast<uint32_t *>(&hb);
         }
-        const uint32_t addr = pbase + (c >> 3) * (P_BYTES / 2) + (((c & 7) ^ (row & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(wv[0]), "r"(wv[1]), "r"(wv[2]),
-                     "r"(wv[3])
-                     : "memory");
+        tc::tmem_st32(tP + hlf * (BN / 4), pk);
     }
     return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
@@ -392,12 +389,11 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 if (!wait_or_abort(BAR(B_PF + w), c & 1, abort_flag, P.status)) return false;
                 if (j == I.jb[w] && !wait_or_abort(BAR(B_OE + w), (co & 1) ^ 1, abort_flag, P.status)) return false;
                 tc::fence_after_sync();
-                const uint32_t pa = sb + OFF_P + w * P_BYTES;
                 const uint32_t va = sb + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    tc::mma_bf16(tmem + COL_O + w * HD, tc::sw128_desc(pa + (kk >> 2) * (P_BYTES / 2) + (kk & 3) * 32),
-                                 tc::sw128_desc(va + kk * 2048), IDESC_PV, kk > 0 || j > I.jb[w]);
+                    tc::mma_bf16_ta(tmem + COL_O + w * HD, tmem + COL_P + w * (BN / 2) + kk * 8,
+                                    tc::sw128_desc(va + kk * 2048), IDESC_PV, kk > 0 || j > I.jb[w]);
                 tc::commit(BAR(B_OF + w));
                 tc::commit(BAR(B_KVE + st));
                 return true;
@@ -419,7 +415,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_addr + COL_S + w * BN;
         const uint32_t tO = tmem + lane_addr + COL_O + w * HD;
-        const uint32_t pbase = sb + OFF_P + w * P_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
+        const uint32_t tP = tmem + lane_addr + COL_P + w * (BN / 2);
         uint32_t cs = 0, co = 0, g = 0;
         for (int t = blockIdx.x; t < total_items && !*abort_flag; t += gridDim.x) {
             const Item I = sched.get(t);
@@ -510,7 +506,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 if (raise) l *= ex2(m_old - m);
                 // P = 2^(scale * s - m) as bf16 into the swizzled buffer; row sum in f32
                 const float mneg = (m == -INFINITY ? 0.f : -m) + boff;
-                l += write_p_row(x, P.scale_log2, mneg, pbase, row);
+                l += write_p_tmem(x, P.scale_log2, mneg, tP);
                 if (j > I.jb[w] && __any_sync(kFull, raise)) {
                     // the running max rose: bring this row's O to the new max (in TMEM)
                     const float c = raise ? ex2(m_old - m) : 1.f;
@@ -520,8 +516,8 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     for (int i = 0; i < HD; ++i) o[i] *= c;
                     tc::tmem_st64(tO, o);
                 }
-                fence_proxy_async();                   // P is read by the tensor cores (async proxy)
-                tc::fence_before_sync();               // orders the O rescale before the next P V
+                if constexpr (PAGED) fence_proxy_async();   // zeroed V rows are read by the tensor cores
+                tc::fence_before_sync();               // orders P and the O rescale before the next P V
                 mbar_arrive(BAR(B_PF + w));
             }
             if (!ok) break;
