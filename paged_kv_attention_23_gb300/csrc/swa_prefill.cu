@@ -176,16 +176,17 @@ __device__ __forceinline__ void add2(float &a0, float &a1, float y0, float y1)
 }
 
 // P = 2^(scale * s - m) for one tile row as bf16 pairs into the row's TMEM
-// lane (64 columns, key 2c in the low half of column c); returns the f32 row sum.
+// lane (64 columns, key 2c in the low half of column c), 16 columns per store
+// (fewer live registers than one wide store); returns the f32 row sum.
 __device__ __forceinline__ float write_p_tmem(const float *x, float scale_log2, float mneg, uint32_t tP)
 {
     float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int hlf = 0; hlf < 2; ++hlf) {
-        uint32_t pk[BN / 4];
+    for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pk[BN / 8];
 #pragma unroll
-        for (int c = 0; c < BN / 4; ++c) {
-            const int i = hlf * (BN / 2) + 2 * c;
+        for (int c = 0; c < BN / 8; ++c) {
+            const int i = q4 * (BN / 4) + 2 * c;
             float a0, a1;
             fma2(x[i], x[i + 1], scale_log2, mneg, a0, a1);
             const float p0 = ex2(a0), p1 = ex2(a1);
@@ -193,7 +194,7 @@ __device__ __forceinline__ float write_p_tmem(const float *x, float scale_log2, 
             __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
             pk[c] = *reinterpret_cast<uint32_t *>(&hb);
         }
-        tc::tmem_st32(tP + hlf * (BN / 4), pk);
+        tc::tmem_st16(tP + q4 * (BN / 8), pk);
     }
     return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
