@@ -26,16 +26,26 @@
 //    Loads run up to NSTAGE blocks ahead of the math and across unit
 //    boundaries; block-table entries of the next unit are fetched one unit
 //    ahead.  Block-table entries and blocks outside the window are never read.
-//  * Math per block: 4 lanes per key compute q.k from 16-byte shared loads
-//    (chunk order rotated per key parity: no bank conflicts), online softmax
-//    in the log2 domain (ex2.approx), P.V with one 16-byte V load per lane per
-//    row group; f32 everywhere.
+//  * Math per block: 2 lanes per key compute q.k from 16-byte shared loads
+//    with mixed-precision FMA (bf16 / f16 operands, f32 accumulate; chunk
+//    order rotated per key: no bank conflicts), online softmax in the log2
+//    domain (ex2.approx), P.V with one 16-byte V load per lane per row group.
+//  * Bias: a materialised A (streamed with the keys), or the T5 table read
+//    from shared memory at column min(ctx-1-j, buckets-1), or none.
 //  * A unit that is its (s, h)'s only partition writes `out` directly.  Else
 //    it writes (m, l, acc) to the workspace and bumps a per-(s, h) counter with
 //    atomicInc(npart - 1), which wraps to zero: the last partition to arrive
-//    merges all partials, writes `out` and zeroes the slots it read.  A call
-//    therefore leaves the whole workspace zero, ready for the next call of any
-//    shape.
+//    merges all partials (every load of a chunk of partials issued at once),
+//    writes `out` and zeroes the slots it read.  A call therefore leaves the
+//    whole workspace zero, ready for the next call of any shape.
+//  * A launch may carry two problems (a decode step's self- and
+//    cross-attention, each with its own tables, caches and workspace); the
+//    unit list runs over the concatenated sequences.
+//  * Fused append: a problem may bring its newest token's K/V (position
+//    ctx-1).  The unit that covers the last block patches that row into the
+//    staged block once the bulk copy has landed and stores it to the cache
+//    slot, so one launch does the KV caching and the attention of a step.
+
 #include <algorithm>
 #include <cmath>
 #include <mutex>

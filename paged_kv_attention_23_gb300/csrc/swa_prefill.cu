@@ -12,6 +12,15 @@
 // Only key tiles that intersect the band are visited ("visit only
 // intra-window blocks", same page).
 //
+// Two template switches widen it ("Add Encoder-decoder model support and T5
+// Model support": T5's custom attention bias; prefill kernels that read
+// cross-attention keys through their block table):
+//   BIAS   adds rel[h, cap + clamp(d, -cap, cap)] to q.k before the scale,
+//          d = query position - key position (the T5 relative-position bias).
+//   PAGED  reads K/V from the paged cache [num_blocks, H, 16, 64] through the
+//          block table, for each sequence's last Lq queries: query row r sits
+//          at key position ctx - Lq + r, and the masks and the bias use it.
+//
 // Work item = two consecutive 128-row query tiles of one (sequence, head)
 // sharing one stream of 128-key K/V tiles (for W = 64: three key tiles per
 // 256 rows, each query tile multiplying only the two it needs).  One
@@ -65,6 +74,7 @@ constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NS, B_SF = 2 + 2 * NS, 
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, abort flag
 constexpr uint32_t OFF_SCHED = (OFF_MISC + 16 + 127) / 128 * 128;
 constexpr uint32_t SMEM_BYTES = OFF_SCHED + (6 * MAX_SEQS + 1) * 4 + 1024;   // + alignment slack
+static_assert(SMEM_BYTES <= 227u * 1024u, "dynamic shared memory per CTA");
 constexpr int CBS = 16;                   // paged cache block: 16 key rows of one head
 constexpr uint32_t CBLK_BYTES = CBS * HD * 2;                                  // 2 KB per block and head
 
