@@ -411,6 +411,17 @@ def run_decode(args, rank, world, local, peaks):
     clk = clocks.stop()
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
     ms_step = total_ms / K
+    # warm-L2 reference (labelled, not the metric): the same steps on one input copy
+    warm_ms = None
+    if copies > 1:
+        wgraph = capture_graph(lambda: [step(0) for _ in range(K)])
+        wgraph.replay()
+        torch.cuda.synchronize(); barrier(world)
+        t0.record()
+        wgraph.replay()
+        t1.record()
+        torch.cuda.synchronize(); barrier(world)
+        warm_ms = max_over_ranks(t0.elapsed_time(t1), world) / K
     # per-launch durations: the same K steps eagerly, queued behind a GPU-side
     # sleep so the host is ahead and events see kernel time, not launch gaps
     launch_ms = per_launch_ms(lambda ev: [step(k, True, ev) for k in range(K)], nlaunch, K)
@@ -448,6 +459,8 @@ def run_decode(args, rank, world, local, peaks):
                                  if off_ms else None),
         "bias_off_seqs_per_s": round(seqs / (off_ms * 1e-3), 1) if off_ms else None,
         "alg_bytes_per_step": step_bytes,
+        "warm_l2_GBps": round(step_bytes * world / (warm_ms * 1e-3) / 1e9, 1) if warm_ms else None,
+        "warm_l2_ms_per_step": round(warm_ms, 5) if warm_ms else None,
     }
     cfg = {"workload": args.workload, "num_seqs": [c.num_seqs for c in cases], "num_heads": cases[0].num_heads,
            "head_dim": cases[0].head_dim, "block_size": 16,
