@@ -33,7 +33,7 @@
  *    one (block, head) is one contiguous block_size * head_dim run.
  *  - Supported now: head_dim in {64, 128}; block_size 16; num_kv_heads ==
  *    num_heads.  Decode: f32, f16, bf16 (q, caches and out share one dtype;
- *    the bias is always f32).  Prefill: bf16, head_dim 64.
+ *    the bias is always f32).  Prefill: bf16 or f16, head_dim 64.
  */
 #ifndef PKA_H
 #define PKA_H
@@ -300,7 +300,8 @@ PKA_API pka_status pka_paged_attn_decode_noalloc(void *out, const void *q, const
  *   out[i,h,:] = sum_c softmax(scale * q[i,h,:] . k[c,h,:])_c v[c,h,:]
  * Only key tiles that intersect the mask are visited.
  *
- *   out, q, k, v  [num_tokens, num_heads, head_dim] bf16, contiguous
+ *   out, q, k, v  [num_tokens, num_heads, head_dim] of dtype (PKA_BF16 or
+ *                 PKA_F16; head_dim 64), contiguous
  *   cu_seqlens    int32 [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0,
  *                 cu_seqlens[num_seqs] = num_tokens
  *   max_seqlen    upper bound on every sequence length (a longer sequence
@@ -310,7 +311,8 @@ PKA_API pka_status pka_paged_attn_decode_noalloc(void *out, const void *q, const
  *   causal        0 or 1
  *   status        int32 device word or NULL (PKA_DEVCHK_CU_SEQLENS,
  *                 PKA_DEVCHK_TIMEOUT)
- * Accumulation is f32; P is rounded to bf16 before the P.V product.
+ * Accumulation is f32; P is rounded to the operand type (bf16 or f16) before
+ * the P.V product, whose operands must share one type.
  */
 PKA_API pka_status pka_swa_prefill(void *out, const void *q, const void *k, const void *v,
                            const int32_t *cu_seqlens, int num_seqs, int num_tokens, int max_seqlen,
@@ -371,8 +373,9 @@ PKA_API pka_status pka_prefill_biased(void *out, const void *q, const void *k, c
  * With causal = 0, window -1 and no bias every query attends to all ctx_s
  * keys: a decoder prompt's cross-attention to the encoder.
  *
- *   out, q        [num_tokens, num_heads, 64] bf16, rows packed by cu_seqlens_q
- *   k_cache, v_cache [num_blocks, num_heads, 16, 64] bf16, 16-byte aligned
+ *   out, q        [num_tokens, num_heads, 64] of dtype (PKA_BF16 or PKA_F16),
+ *                 rows packed by cu_seqlens_q
+ *   k_cache, v_cache [num_blocks, num_heads, 16, 64] of dtype, 16-byte aligned
  *   block_tables  int32 [num_seqs, max_blocks_per_seq]; entries of blocks
  *                 with no kept key (before every row's window, past ctx_s)
  *                 are never read
@@ -385,7 +388,7 @@ PKA_API pka_status pka_prefill_biased(void *out, const void *q, const void *k, c
  *                 PKA_DEVCHK_CONTEXT_LEN, PKA_DEVCHK_BLOCK_ID — the entry is
  *                 replaced by block 0 — and PKA_DEVCHK_TIMEOUT)
  * Cache rows past ctx_s in the last block may hold any bits (NaN included).
- * Accumulation is f32; P is rounded to bf16 before the P.V product.
+ * Accumulation is f32; P is rounded to the operand type before the P.V product.
  */
 PKA_API pka_status pka_paged_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
                                      const int32_t *block_tables, const int32_t *cu_seqlens_q,

@@ -82,9 +82,10 @@ pka_status prepare_prefill(void *out, const void *q, const void *k, const void *
         (causal != 0 && causal != 1) || !dtype_ok(dtype))
         return PKA_ERR_INVALID_ARG;
     if (window != -1 && window < 1) return PKA_ERR_INVALID_ARG;
-    if (dtype != PKA_BF16) return PKA_ERR_UNSUPPORTED;
+    if (dtype != PKA_BF16 && dtype != PKA_F16) return PKA_ERR_UNSUPPORTED;
     if (head_dim != 64) return PKA_ERR_UNSUPPORTED;
     a.num_tokens = 0;
+    a.dtype = dtype;
     if (num_seqs == 0 || num_tokens == 0) return PKA_OK;
     if (!out || !q || !k || !v || !cu_seqlens) return PKA_ERR_INVALID_ARG;
     if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(cu_seqlens, 4) ||

@@ -66,6 +66,7 @@ struct PrefillArgs {
     int num_seqs, num_tokens, max_seqlen, num_heads, head_dim, window, causal;
     int chunk;   // > 0: chunked local attention (window must be -1; packed only)
     int mbps, num_blocks;              // paged only
+    pka_dtype dtype;                   // PKA_BF16 or PKA_F16
 };
 
 cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream);

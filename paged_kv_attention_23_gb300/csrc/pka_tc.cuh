@@ -41,14 +41,14 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
            (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor, kind::f16 with bf16 A and B, f32 accumulator:
-// D format f32 (1) at bits [4,6), A format bf16 (1) at [7,10), B format bf16
-// (1) at [10,13), A major at bit 15, B major at bit 16 (0 = K-major,
-// 1 = MN-major), N >> 3 at [17,23), M >> 4 at [24,29).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major)
+// Instruction descriptor, kind::f16 with 16-bit A and B of one type, f32
+// accumulator: D format f32 (1) at bits [4,6), A format at [7,10) and B format
+// at [10,13) (f16 = 0, bf16 = 1), A major at bit 15, B major at bit 16 (0 =
+// K-major, 1 = MN-major), N >> 3 at [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_16_f32(int M, int N, bool a_mn_major, bool b_mn_major, bool bf16)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ---- MMA ---------------------------------------------------------------------------

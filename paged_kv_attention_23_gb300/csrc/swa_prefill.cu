@@ -48,6 +48,7 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "pka_device.cuh"
 #include "pka_launch.h"
@@ -83,11 +84,13 @@ constexpr uint32_t CBLK_BYTES = CBS * HD * 2;                                  /
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_O = 256, COL_P = 384;
 
-constexpr uint32_t IDESC_QK = tc::idesc_bf16_f32(BM, BN, false, false);  // S = Q K^T, both K-major
-constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(BM, HD, false, true);   // O += P V, V is MN-major
+// S = Q K^T (both K-major) and O += P V (V MN-major), for bf16 or f16 operands
+template <typename T> __host__ __device__ constexpr bool is_bf16() { return std::is_same<T, __nv_bfloat16>::value; }
+template <typename T> __host__ __device__ constexpr uint32_t idesc_qk() { return tc::idesc_16_f32(BM, BN, false, false, is_bf16<T>()); }
+template <typename T> __host__ __device__ constexpr uint32_t idesc_pv() { return tc::idesc_16_f32(BM, HD, false, true, is_bf16<T>()); }
 
 struct Params {
-    __nv_bfloat16 *out;
+    void *out;                       // [T, H, 64] of the operand type
     const int32_t *cu_seqlens;       // query rows (packed keys too)
     const int32_t *context_lens;     // paged: keys of each sequence
     const int32_t *block_tables;     // paged: [num_seqs, mbps] cache blocks
@@ -188,6 +191,7 @@ __device__ __forceinline__ void add2(float &a0, float &a1, float y0, float y1)
 // P = 2^(scale * s - m) for one tile row as bf16 pairs into the row's TMEM
 // lane (64 columns, key 2c in the low half of column c), 16 columns per store
 // (fewer live registers than one wide store); returns the f32 row sum.
+template <typename T>
 __device__ __forceinline__ float write_p_tmem(const float *x, float scale_log2, float mneg, uint32_t tP)
 {
     float ls[4] = {0.f, 0.f, 0.f, 0.f};
@@ -201,8 +205,13 @@ __device__ __forceinline__ float write_p_tmem(const float *x, float scale_log2, 
             fma2(x[i], x[i + 1], scale_log2, mneg, a0, a1);
             const float p0 = ex2(a0), p1 = ex2(a1);
             add2(ls[(c & 1) * 2], ls[(c & 1) * 2 + 1], p0, p1);
-            __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
-            pk[c] = *reinterpret_cast<uint32_t *>(&hb);
+            if constexpr (is_bf16<T>()) {
+                __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
+                pk[c] = *reinterpret_cast<uint32_t *>(&hb);
+            } else {
+                __half2 hh = __floats2half2_rn(p0, p1);
+                pk[c] = *reinterpret_cast<uint32_t *>(&hh);
+            }
         }
         tc::tmem_st16(tP + q4 * (BN / 8), pk);
     }
@@ -230,7 +239,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 // block tables (tm_k / tm_v are 4-D maps with one cache block per box);
 // otherwise from the packed [T, H, 64] keys of the same rows as the queries.
 // BIAS: the relative-position bias is added to the scores.
-template <bool PAGED, bool BIAS>
+template <typename T, bool PAGED, bool BIAS>
 __global__ void __launch_bounds__(NTHREADS, 1)
 swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const Params P)
@@ -384,7 +393,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk)
                     tc::mma_bf16(tmem + COL_S + w * BN, tc::sw128_desc(qa + kk * 32), tc::sw128_desc(ka + kk * 32),
-                                 IDESC_QK, kk > 0);
+                                 idesc_qk<T>(), kk > 0);
                 tc::commit(BAR(B_SF + w));
                 if (j == I.je[w]) tc::commit(BAR(B_QE));         // last read of Q_w in this item
                 return true;
@@ -404,7 +413,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     tc::mma_bf16_ta(tmem + COL_O + w * HD, tmem + COL_P + w * (BN / 2) + kk * 8,
-                                    tc::sw128_desc(va + kk * 2048), IDESC_PV, kk > 0 || j > I.jb[w]);
+                                    tc::sw128_desc(va + kk * 2048), idesc_pv<T>(), kk > 0 || j > I.jb[w]);
                 tc::commit(BAR(B_OF + w));
                 tc::commit(BAR(B_KVE + st));
                 return true;
@@ -436,7 +445,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             if (I.jb[w] > I.je[w]) {
                 // past the sequence, or (paged) no key for any row of the tile: zero rows
                 if (PAGED && rr < I.L) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(P.out + ((size_t)(I.s0 + rr) * P.H + I.h) * HD);
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) + ((size_t)(I.s0 + rr) * P.H + I.h) * HD);
 #pragma unroll
                     for (int c = 0; c < HD / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -517,7 +526,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 if (raise) l *= ex2(m_old - m);
                 // P = 2^(scale * s - m) as bf16 into the swizzled buffer; row sum in f32
                 const float mneg = (m == -INFINITY ? 0.f : -m) + boff;
-                l += write_p_tmem(x, P.scale_log2, mneg, tP);
+                l += write_p_tmem<T>(x, P.scale_log2, mneg, tP);
                 if (j > I.jb[w] && __any_sync(kFull, raise)) {
                     // the running max rose: bring this row's O to the new max (in TMEM)
                     const float c = raise ? ex2(m_old - m) : 1.f;
@@ -542,13 +551,13 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             ++co;
             if (rr < I.L) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                uint4 *dst = reinterpret_cast<uint4 *>(P.out + ((size_t)(I.s0 + rr) * P.H + I.h) * HD);
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) + ((size_t)(I.s0 + rr) * P.H + I.h) * HD);
 #pragma unroll
                 for (int c = 0; c < HD / 8; ++c) {
                     float v[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) v[e] = o[c * 8 + e] * inv;
-                    dst[c] = Vec<__nv_bfloat16>::from_f32(v);
+                    dst[c] = Vec<T>::from_f32(v);
                 }
             }
         }
@@ -585,7 +594,7 @@ EncodeTiledFn encode_fn()
 }
 
 // [T, H, 64] bf16 rows -> boxes of 128 tokens x 64 dims of one head, 128-byte swizzle
-bool make_map(CUtensorMap *m, const void *base, int T, int H)
+bool make_map(CUtensorMap *m, const void *base, int T, int H, CUtensorMapDataType dt)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
@@ -593,14 +602,14 @@ bool make_map(CUtensorMap *m, const void *base, int T, int H)
     const cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)H * HD * 2};
     const cuuint32_t box[3] = {HD, 1, BM};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+    return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // [num_blocks, H, 16, 64] bf16 paged cache -> boxes of one block (16 rows x
 // 64 dims) of one head, 128-byte swizzle
-bool make_paged_map(CUtensorMap *m, const void *base, int num_blocks, int H)
+bool make_paged_map(CUtensorMap *m, const void *base, int num_blocks, int H, CUtensorMapDataType dt)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
@@ -608,16 +617,16 @@ bool make_paged_map(CUtensorMap *m, const void *base, int num_blocks, int H)
     const cuuint64_t strides[3] = {(cuuint64_t)HD * 2, (cuuint64_t)CBLK_BYTES, (cuuint64_t)H * CBLK_BYTES};
     const cuuint32_t box[4] = {HD, CBS, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+    return enc(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool PAGED, bool BIAS>
+template <typename T, bool PAGED, bool BIAS>
 cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, Params P,
                        const PrefillArgs &a, int sms, cudaStream_t stream)
 {
-    auto kern = swa_prefill_tc_kernel<PAGED, BIAS>;
+    auto kern = swa_prefill_tc_kernel<T, PAGED, BIAS>;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [&] {
@@ -640,25 +649,38 @@ cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
     return cudaSuccess;
 }
 
+template <typename T>
+cudaError_t dispatch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const Params &P,
+                     const PrefillArgs &a, int sms, bool paged, bool bias, cudaStream_t stream)
+{
+    if (paged) return bias ? launch_cfg<T, true, true>(mq, mk, mv, P, a, sms, stream)
+                           : launch_cfg<T, true, false>(mq, mk, mv, P, a, sms, stream);
+    return bias ? launch_cfg<T, false, true>(mq, mk, mv, P, a, sms, stream)
+                : launch_cfg<T, false, false>(mq, mk, mv, P, a, sms, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream)
 {
     if (a.head_dim != HD) return cudaErrorInvalidValue;
     const bool paged = a.block_tables != nullptr;
+    const CUtensorMapDataType dt =
+        a.dtype == PKA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, a.q, a.num_tokens, a.num_heads)) return cudaErrorInvalidValue;
+    if (!make_map(&mq, a.q, a.num_tokens, a.num_heads, dt)) return cudaErrorInvalidValue;
     if (paged) {
-        if (!make_paged_map(&mk, a.k, a.num_blocks, a.num_heads) || !make_paged_map(&mv, a.v, a.num_blocks, a.num_heads))
+        if (!make_paged_map(&mk, a.k, a.num_blocks, a.num_heads, dt) ||
+            !make_paged_map(&mv, a.v, a.num_blocks, a.num_heads, dt))
             return cudaErrorInvalidValue;
-    } else if (!make_map(&mk, a.k, a.num_tokens, a.num_heads) || !make_map(&mv, a.v, a.num_tokens, a.num_heads)) {
+    } else if (!make_map(&mk, a.k, a.num_tokens, a.num_heads, dt) || !make_map(&mv, a.v, a.num_tokens, a.num_heads, dt)) {
         return cudaErrorInvalidValue;
     }
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     Params P;
-    P.out = static_cast<__nv_bfloat16 *>(a.out);
+    P.out = a.out;
     P.status = a.status;
     P.scale_log2 = a.scale * 1.4426950408889634f;
     P.num_tokens = a.num_tokens;
@@ -673,10 +695,8 @@ cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream)
     P.mbps = a.mbps;
     P.num_blocks = a.num_blocks;
     const bool bias = a.rel_bias != nullptr;
-    if (paged) return bias ? launch_cfg<true, true>(mq, mk, mv, P, a, sms, stream)
-                           : launch_cfg<true, false>(mq, mk, mv, P, a, sms, stream);
-    return bias ? launch_cfg<false, true>(mq, mk, mv, P, a, sms, stream)
-                : launch_cfg<false, false>(mq, mk, mv, P, a, sms, stream);
+    return a.dtype == PKA_F16 ? dispatch<__half>(mq, mk, mv, P, a, sms, paged, bias, stream)
+                              : dispatch<__nv_bfloat16>(mq, mk, mv, P, a, sms, paged, bias, stream);
 }
 
 }  // namespace pka

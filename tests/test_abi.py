@@ -92,6 +92,7 @@ def test_reshape_and_prefill_argument_checks_need_no_gpu(lib):
     assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, 0, 0, 0.125, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
     assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 2, 0.125, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
     assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, 0.125, 0, NULL, NULL) == pka.PKA_ERR_UNSUPPORTED
+    assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, 0.125, 1, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
     assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, 0.125, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
 
 
@@ -173,8 +174,10 @@ def test_biased_and_paged_prefill_argument_checks_need_no_gpu(lib):
         pka.PKA_ERR_INVALID_ARG                                                    # no table
     assert b(NULL, NULL, NULL, NULL, NULL, 0, 0, 0, 12, 64, -1, 0, fake, 0, 0.125, 2, NULL, NULL) == \
         pka.PKA_ERR_INVALID_ARG                                                    # no buckets
+    assert b(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, fake, 4, 0.125, 0, NULL, NULL) == \
+        pka.PKA_ERR_UNSUPPORTED                                                    # f32
     assert b(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, fake, 4, 0.125, 1, NULL, NULL) == \
-        pka.PKA_ERR_UNSUPPORTED                                                    # f16
+        pka.PKA_ERR_INVALID_ARG                                                    # f16 accepted; NULL buffers
     assert b(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, fake, 4, 0.125, 2, NULL, NULL) == \
         pka.PKA_ERR_INVALID_ARG                                                    # NULL buffers
     p = lib.pka_paged_prefill

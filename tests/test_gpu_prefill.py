@@ -5,7 +5,7 @@ import pytest
 import oracle
 import synth
 from helpers import TOL, max_err, to_dev, to_f64, to_host_storage
-from synth import BF16
+from synth import BF16, F16
 
 pytestmark = pytest.mark.gpu
 
@@ -25,10 +25,10 @@ def run_gpu_prefill(pka, case):
     return out
 
 
-def _check(got, ref, what):
+def _check(got, ref, what, dtype=BF16):
     assert np.isfinite(got).all(), what
     err = max_err(got, ref)
-    assert err <= TOL[BF16], f"{what}: max abs err {err:.3g}"
+    assert err <= TOL[dtype], f"{what}: max abs err {err:.3g}"
 
 
 @pytest.mark.parametrize("window", [-1, 1, 2, 63, 64, 65, 128, 300])
@@ -276,3 +276,42 @@ def test_paged_prefill_t5_workload_sampled(cuda_lib):
         _check(to_f64(got[rows], BF16), ref, pc.name)
         del gp
         torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# f16 operands (same kernel, f16 MMA and f16 P)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("window", [-1, 1, 64, 300])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_prefill_f16_small_parity(cuda_lib, window, causal):
+    lens = [1, 2, 127, 128, 129, 255, 300, 513]
+    case = synth.make_prefill_case("small-f16", 600 + max(window, 0) + causal, lens, 3, 64, window, causal, F16,
+                                   scale=1 / 8)
+    got = to_f64(run_gpu_prefill(cuda_lib, case), F16)
+    ref = oracle.prefill(case.q, case.k, case.v, case.cu_seqlens, window, causal, case.scale, F16)
+    _check(got, ref, f"f16 W={window} causal={causal}", F16)
+
+
+def test_prefill_f16_biased_and_paged_parity(cuda_lib):
+    case = synth.make_prefill_case("biased-f16", 610, [1, 130, 300, 513], 2, 64, 40, 0, F16, scale=1 / 8)
+    case.rel_bias = synth.rel_bias_table(610, 2, 129)
+    got = to_f64(run_gpu_biased(cuda_lib, case), F16)
+    ref = oracle.prefill_biased(case.q, case.k, case.v, case.cu_seqlens, 40, 0, case.scale, F16, case.rel_bias)
+    _check(got, ref, "f16 biased", F16)
+    pc = synth.make_paged_prefill_case("paged-f16", 611, F16, PAGED_CTX, PAGED_QL, 2, 64, -1, 1, 129, scale=1 / 8,
+                                       pool_blocks=400)
+    gp = GpuPagedPrefill(pc, cuda_lib)
+    _check(to_f64(gp.run(), F16), oracle_paged(gp), "f16 paged", F16)
+    assert int(gp.status.item()) == 0
+
+
+def test_prefill_f16_large_logits_stay_finite(cuda_lib):
+    """Scores far beyond the f16 range (|q.k| up to ~1e5 before the scale): P
+    and the accumulator are f32 and P <= 256, so the f16 outputs stay finite
+    (the encoder-decoder page's T5 fp16 overflow report)."""
+    case = synth.make_prefill_case("f16-big", 612, [200, 77], 2, 64, -1, 0, F16, scale=1.0)
+    case.q = synth.encode(synth.decode_to_f32(case.q, F16) * np.float32(40.0), F16)
+    case.k = synth.encode(synth.decode_to_f32(case.k, F16) * np.float32(40.0), F16)
+    got = to_f64(run_gpu_prefill(cuda_lib, case), F16)
+    ref = oracle.prefill(case.q, case.k, case.v, case.cu_seqlens, -1, 0, 1.0, F16)
+    _check(got, ref, "f16 large logits", F16)
