@@ -440,20 +440,62 @@ def test_multi_append_equals_scatter_then_decode(cuda_lib, dtype, D, window):
     _check(to_f64(out, dtype), oracle_decode(case), dtype, "append")
 
 
-def test_multi_append_self_with_unappended_cross(cuda_lib):
+@pytest.mark.parametrize("self_mode", ["bias", "t5"])
+def test_multi_append_self_with_unappended_cross(cuda_lib, self_mode):
     """The T5-large-shaped step in one launch: the self-attention problem
-    appends its newest token, the cross-attention problem does not."""
+    (materialised or in-kernel T5 bias) appends its newest token, the
+    cross-attention problem does not."""
     import torch
     sc, cc = synth.decode_workload(3, num_seqs=48), synth.cross_workload(num_seqs=48)
     gs, gc = GpuDecode(sc, cuda_lib), GpuDecode(cc, cuda_lib)
-    cuda_lib.paged_attn_decode_multi([gs.problem("bias"), gc.problem("none")])   # same plan, scattered caches
+    cuda_lib.paged_attn_decode_multi([gs.problem(self_mode), gc.problem("none")])   # same plan, scattered caches
     ref_s, ref_c = gs.out.clone(), gc.out.clone()
     kc, vc, k_new, v_new = _append_state(sc, cuda_lib)
     out_s, out_c = torch.empty_like(ref_s), torch.empty_like(ref_c)
-    cuda_lib.paged_attn_decode_multi([dict(gs.problem("bias"), out=out_s, k_cache=kc, v_cache=vc, key_new=k_new,
-                                           value_new=v_new), dict(gc.problem("none"), out=out_c)])
+    cuda_lib.paged_attn_decode_multi([dict(gs.problem(self_mode), out=out_s, k_cache=kc, v_cache=vc,
+                                           key_new=k_new, value_new=v_new), dict(gc.problem("none"), out=out_c)])
     torch.cuda.synchronize()
     assert torch.equal(out_s.view(torch.int16), ref_s.view(torch.int16))
     assert torch.equal(out_c.view(torch.int16), ref_c.view(torch.int16))
     assert torch.equal(kc.view(torch.int16), gs.k_cache.view(torch.int16))
-    _check(to_f64(out_s, BF16), oracle_decode(sc), BF16, "append self")
+    ref = oracle_decode_t5(sc) if self_mode == "t5" else oracle_decode(sc)
+    _check(to_f64(out_s, BF16), ref, BF16, "append self")
+
+
+def test_multi_append_across_the_launch_split(cuda_lib):
+    """1300 appending sequences over two problems take two launches; every
+    sequence's newest row is written and attended exactly once."""
+    import torch
+    a = synth.make_decode_case("app-a", 95, F16, 700, 2, 64, ctx_range=(0, 70), bias="gauss", bias_stride=80,
+                               window=23, scale=0.3)
+    b = synth.make_decode_case("app-b", 96, F16, 600, 2, 64, ctx_range=(1, 200), pool_blocks=5000,
+                               max_blocks_per_seq=16, scale=0.05)
+    ga, gb = GpuDecode(a, cuda_lib), GpuDecode(b, cuda_lib)
+    cuda_lib.paged_attn_decode_multi([ga.problem("bias"), gb.problem("none")])
+    ref_a, ref_b = ga.out.clone(), gb.out.clone()
+    ka, va, kna, vna = _append_state(a, cuda_lib)
+    kb, vb, knb, vnb = _append_state(b, cuda_lib)
+    oa, ob = torch.empty_like(ref_a), torch.empty_like(ref_b)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cuda_lib.paged_attn_decode_multi([dict(ga.problem("bias"), out=oa, k_cache=ka, v_cache=va, key_new=kna,
+                                           value_new=vna),
+                                      dict(gb.problem("none"), out=ob, k_cache=kb, v_cache=vb, key_new=knb,
+                                           value_new=vnb)], status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(oa.view(torch.int16), ref_a.view(torch.int16))
+    assert torch.equal(ob.view(torch.int16), ref_b.view(torch.int16))
+    assert torch.equal(ka.view(torch.int16), ga.k_cache.view(torch.int16))
+    assert torch.equal(vb.view(torch.int16), gb.v_cache.view(torch.int16))
+
+
+def test_multi_materialised_bias_then_table(cuda_lib):
+    """Problem 0 with a materialised bias, problem 1 with the T5 table: the
+    launch caches the second problem's table."""
+    a = synth.decode_workload(2)
+    b = synth.make_decode_case("tab1", 97, BF16, 20, 8, 64, ctx_range=(1, 400))
+    b.bias_table = np.random.default_rng(97).standard_normal((8, 33)).astype(np.float32)
+    ga, gb = GpuDecode(a, cuda_lib), GpuDecode(b, cuda_lib)
+    cuda_lib.paged_attn_decode_multi([ga.problem("bias"), gb.problem("t5")])
+    _check(to_f64(ga.out, BF16), oracle_decode(a), BF16, "materialised problem 0")
+    _check(to_f64(gb.out, BF16), oracle_decode_t5(b), BF16, "table problem 1")
