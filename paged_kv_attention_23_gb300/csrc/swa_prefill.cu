@@ -68,10 +68,11 @@ constexpr float RESCALE_LOG2 = 8.f;
 constexpr uint32_t TILE_BYTES = BM * HD * 2;             // 16 KB: one Q, K or V tile
 constexpr uint32_t OFF_Q = 0;                             // 2 query tiles
 constexpr uint32_t OFF_KV = 2 * TILE_BYTES;               // NS x (K, V)
-constexpr uint32_t OFF_BAR = OFF_KV + NS * 2 * TILE_BYTES;
+constexpr uint32_t OFF_OST = OFF_KV + NS * 2 * TILE_BYTES;  // 2 output staging tiles (one per query tile)
+constexpr uint32_t OFF_BAR = OFF_OST + 2 * TILE_BYTES;
 // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], s_empty[2], p_full[2], o_full[2], o_empty[2]
 constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NS, B_SF = 2 + 2 * NS, B_SE = B_SF + 2, B_PF = B_SE + 2,
-              B_OF = B_PF + 2, B_OE = B_OF + 2, NBAR = B_OE + 2;
+              B_OF = B_PF + 2, B_OE = B_OF + 2, B_EW = B_OE + 2, B_ER = B_EW + 2, NBAR = B_ER + 2;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, abort flag
 constexpr uint32_t OFF_SCHED = (OFF_MISC + 16 + 127) / 128 * 128;
 constexpr uint32_t SMEM_BYTES = OFF_SCHED + (6 * MAX_SEQS + 1) * 4 + 1024;   // + alignment slack
@@ -242,7 +243,8 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 template <typename T, bool PAGED, bool BIAS>
 __global__ void __launch_bounds__(NTHREADS, 1)
 swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const Params P)
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                      const Params P)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled tiles
@@ -277,7 +279,8 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     if (threadIdx.x == 0) {
         for (int i = 0; i < NBAR; ++i) {
             const bool by_softmax = (i >= B_SE && i < B_SE + 2) || (i >= B_PF && i < B_PF + 2) ||
-                                    (i >= B_OE && i < B_OE + 2);
+                                    (i >= B_OE && i < B_OE + 2) || (i >= B_EW && i < B_EW + 2) ||
+                                    (i >= B_ER && i < B_ER + 2);
             const bool by_both_mma = i == B_QE || (i >= B_KVE && i < B_KVE + NS);
             mbar_init(BAR(i), by_softmax ? 128 : by_both_mma ? 2 : 1);
         }
@@ -327,6 +330,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         tc::prefetch_tensormap(&tm_q);
         tc::prefetch_tensormap(&tm_k);
         tc::prefetch_tensormap(&tm_v);
+        tc::prefetch_tensormap(&tm_o);
         uint32_t g = 0, wq = 0;
         for (int t = blockIdx.x; t < total_items && !*abort_flag; t += gridDim.x, ++wq) {
             const Item I = sched.get(t);
@@ -436,7 +440,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const uint32_t tS = tmem + lane_addr + COL_S + w * BN;
         const uint32_t tO = tmem + lane_addr + COL_O + w * HD;
         const uint32_t tP = tmem + lane_addr + COL_P + w * (BN / 2);
-        uint32_t cs = 0, co = 0, g = 0;
+        uint32_t cs = 0, co = 0, g = 0, ep = 0;
         for (int t = blockIdx.x; t < total_items && !*abort_flag; t += gridDim.x) {
             const Item I = sched.get(t);
             const uint32_t g_item = g;                 // K/V stages of this item start at g_item
@@ -549,8 +553,38 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             tc::fence_before_sync();
             mbar_arrive(BAR(B_OE + w));
             ++co;
-            if (rr < I.L) {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int tile0 = I.r0 + w * BM;            // the tile's first row within its sequence
+            if (!BIAS && tile0 + BM <= I.L) {
+                // a whole tile: rows into the 128-byte-swizzled staging tile, then one
+                // TMA store, so the softmax threads issue no strided global stores
+                // (the bias instances keep plain stores: their per-key table loads
+                // and the extra live registers of this path cost more than it saves).
+                // The group's previous store has finished reading the staging tile:
+                if (row == 0) tc::bulk_wait_read_all();
+                mbar_arrive(BAR(B_EW + w));
+                if (!wait_or_abort(BAR(B_EW + w), ep & 1, abort_flag, P.status)) break;
+                const uint32_t srow = sb + OFF_OST + w * TILE_BYTES + row * 128;
+#pragma unroll
+                for (int c = 0; c < HD / 8; ++c) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = o[c * 8 + e] * inv;
+                    const uint4 u = Vec<T>::from_f32(v);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(srow + ((c ^ (row & 7)) << 4)),
+                                 "r"(u.x), "r"(u.y), "r"(u.z), "r"(u.w)
+                                 : "memory");
+                }
+                fence_proxy_async();                   // the rows are read by the TMA engine
+                mbar_arrive(BAR(B_ER + w));
+                if (row == 0) {
+                    if (!wait_or_abort(BAR(B_ER + w), ep & 1, abort_flag, P.status)) break;
+                    tc::tma_store_3d(&tm_o, 0, I.h, I.s0 + tile0, sb + OFF_OST + w * TILE_BYTES);
+                    tc::bulk_commit_group();
+                }
+                ++ep;
+            } else if (rr < I.L) {
+                // plain stores of the rows inside the sequence (its last, partial tile)
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) + ((size_t)(I.s0 + rr) * P.H + I.h) * HD);
 #pragma unroll
                 for (int c = 0; c < HD / 8; ++c) {
@@ -562,6 +596,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             }
         }
         (void)co;
+        if (!BIAS && row == 0) tc::bulk_wait_all();   // the staging tiles stay valid until the stores are done
     }
 
     // ---- teardown: every role is done with TMEM --------------------------------
@@ -623,8 +658,8 @@ bool make_paged_map(CUtensorMap *m, const void *base, int num_blocks, int H, CUt
 }
 
 template <typename T, bool PAGED, bool BIAS>
-cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, Params P,
-                       const PrefillArgs &a, int sms, cudaStream_t stream)
+cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+                       Params P, const PrefillArgs &a, int sms, cudaStream_t stream)
 {
     auto kern = swa_prefill_tc_kernel<T, PAGED, BIAS>;
     static std::once_flag once;
@@ -642,7 +677,7 @@ cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
         }
         const long long tiles_upper = (long long)P.num_seqs * ((a.max_seqlen + 2 * BM - 1) / (2 * BM)) * a.num_heads;
         const int grid = (int)std::max<long long>(1, std::min<long long>(sms, tiles_upper));
-        kern<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mq, mk, mv, P);
+        kern<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mo, P);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -650,13 +685,13 @@ cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
 }
 
 template <typename T>
-cudaError_t dispatch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const Params &P,
-                     const PrefillArgs &a, int sms, bool paged, bool bias, cudaStream_t stream)
+cudaError_t dispatch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+                     const Params &P, const PrefillArgs &a, int sms, bool paged, bool bias, cudaStream_t stream)
 {
-    if (paged) return bias ? launch_cfg<T, true, true>(mq, mk, mv, P, a, sms, stream)
-                           : launch_cfg<T, true, false>(mq, mk, mv, P, a, sms, stream);
-    return bias ? launch_cfg<T, false, true>(mq, mk, mv, P, a, sms, stream)
-                : launch_cfg<T, false, false>(mq, mk, mv, P, a, sms, stream);
+    if (paged) return bias ? launch_cfg<T, true, true>(mq, mk, mv, mo, P, a, sms, stream)
+                           : launch_cfg<T, true, false>(mq, mk, mv, mo, P, a, sms, stream);
+    return bias ? launch_cfg<T, false, true>(mq, mk, mv, mo, P, a, sms, stream)
+                : launch_cfg<T, false, false>(mq, mk, mv, mo, P, a, sms, stream);
 }
 
 }  // namespace
@@ -667,8 +702,9 @@ cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream)
     const bool paged = a.block_tables != nullptr;
     const CUtensorMapDataType dt =
         a.dtype == PKA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, a.q, a.num_tokens, a.num_heads, dt)) return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, a.q, a.num_tokens, a.num_heads, dt) || !make_map(&mo, a.out, a.num_tokens, a.num_heads, dt))
+        return cudaErrorInvalidValue;
     if (paged) {
         if (!make_paged_map(&mk, a.k, a.num_blocks, a.num_heads, dt) ||
             !make_paged_map(&mv, a.v, a.num_blocks, a.num_heads, dt))
@@ -695,8 +731,8 @@ cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream)
     P.mbps = a.mbps;
     P.num_blocks = a.num_blocks;
     const bool bias = a.rel_bias != nullptr;
-    return a.dtype == PKA_F16 ? dispatch<__half>(mq, mk, mv, P, a, sms, paged, bias, stream)
-                              : dispatch<__nv_bfloat16>(mq, mk, mv, P, a, sms, paged, bias, stream);
+    return a.dtype == PKA_F16 ? dispatch<__half>(mq, mk, mv, mo, P, a, sms, paged, bias, stream)
+                              : dispatch<__nv_bfloat16>(mq, mk, mv, mo, P, a, sms, paged, bias, stream);
 }
 
 }  // namespace pka
