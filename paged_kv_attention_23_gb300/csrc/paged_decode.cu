@@ -116,24 +116,47 @@ struct Unit {
 
 __device__ __forceinline__ int prob_of(int s, const Params &P) { return (P.nprob > 1 && s >= P.pr[0].num_seqs) ? 1 : 0; }
 
-// Unit u -> (s, h, p) by binary search in the per-sequence prefix sums.
-__device__ __forceinline__ Unit unit_of(int u, const int *cum, const int *ctxs, const Params &P)
+// The sequence s of unit u: cum[s] <= u < cum[s + 1].  Called by a whole
+// warp with the same u: lane i tests the i-th of 32 evenly spaced candidates,
+// so 1024 sequences take two shared-memory rounds.
+__device__ __forceinline__ int seq_of_warp(int u, const int *cum, int num_seqs)
 {
-    int lo = 0, hi = P.num_seqs;                      // cum[lo] <= u < cum[hi]
+    int lo = 0, n = num_seqs;                         // cum[lo] <= u < cum[lo + n]
+    while (n > 1) {
+        const int step = (n + 31) >> 5;
+        const int idx = lo + (int)(threadIdx.x & 31) * step;
+        const unsigned m = __ballot_sync(kFull, idx < lo + n && cum[idx] <= u);
+        const int nlo = lo + (__popc(m) - 1) * step;   // candidates at or below u form a prefix
+        n = min(step, lo + n - nlo);
+        lo = nlo;
+    }
+    return lo;
+}
+
+// The same for one thread on its own (binary search).
+__device__ __forceinline__ int seq_of_lane(int u, const int *cum, int num_seqs)
+{
+    int lo = 0, hi = num_seqs;                        // cum[lo] <= u < cum[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (cum[mid] <= u) lo = mid; else hi = mid;
     }
+    return lo;
+}
+
+// Unit u of sequence s -> (h, p) and its block range.
+__device__ __forceinline__ Unit unit_in_seq(int u, int s, const int *cum, const int *ctxs, const Params &P)
+{
     Unit U;
-    U.s = lo;
-    U.prob = prob_of(lo, P);
+    U.s = s;
+    U.prob = prob_of(s, P);
     const Prob &R = P.pr[U.prob];
-    U.gs = R.seq_base + lo - (U.prob ? P.pr[0].num_seqs : 0);
-    U.npart = (cum[lo + 1] - cum[lo]) / P.H;
-    const int r = u - cum[lo];
+    U.gs = R.seq_base + s - (U.prob ? P.pr[0].num_seqs : 0);
+    U.npart = (cum[s + 1] - cum[s]) / P.H;
+    const int r = u - cum[s];
     U.h = r / U.npart;
     U.p = r - U.h * U.npart;
-    U.ctx = ctxs[lo];
+    U.ctx = ctxs[s];
     U.start = (R.window > 0 && U.ctx > R.window) ? U.ctx - R.window : 0;
     if (U.ctx == 0) {
         U.b0 = 0; U.nb = 0;
@@ -143,6 +166,11 @@ __device__ __forceinline__ Unit unit_of(int u, const int *cum, const int *ctxs, 
         U.nb = min(R.part_blocks, last + 1 - U.b0);
     }
     return U;
+}
+
+__device__ __forceinline__ Unit unit_of(int u, const int *cum, const int *ctxs, const Params &P)
+{
+    return unit_in_seq(u, seq_of_warp(u, cum, P.num_seqs), cum, ctxs, P);
 }
 
 __device__ __forceinline__ int load_bt(const Unit &U, const Params &P, int lane)
@@ -258,6 +286,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
     // ---- producer state (issue side) ---------------------------------------
     int pk = 0;                                        // unit ordinal of the issue side
     Unit pu = unit_of(gw, cum, ctxs, P);
+    const Unit first_unit = pu;                       // the consumer's first unit
     int pbt = load_bt(pu, P, lane);
     bool p_next_ok = gw + nwt < total_units;
     Unit pn = pu;
@@ -327,7 +356,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
     for (int ck = 0;; ++ck) {
         const int u = gw + ck * nwt;
         if (u >= total_units) break;
-        const Unit cu = unit_of(u, cum, ctxs, P);
+        const Unit cu = ck == 0 ? first_unit : unit_of(u, cum, ctxs, P);
         const Prob &CP = P.pr[cu.prob];
         const bool has_bias = CP.bias != nullptr, has_table = CP.bias_table != nullptr;
         // append: the sequence's newest token (position ctx-1) lies in the last
