@@ -81,6 +81,32 @@ template <typename T, int D> struct Tr {
     static_assert(NC % 8 == 0 && 32 % NC == 0, "row must be 8, 16 or 32 chunks");
 };
 
+// n / d for any 32-bit unsigned n and a divisor fixed per launch, by one
+// high multiply, a subtract, an add and two shifts (division by invariant
+// integers using multiplication, Granlund and Montgomery 1994): a runtime
+// integer division costs a ~200-cycle dependent chain, which the unit lookup
+// and the partition counts would otherwise pay on every warp's first load.
+struct FastDiv {
+    uint32_t m, s1, s2;
+    __device__ __forceinline__ uint32_t div(uint32_t n) const
+    {
+        const uint32_t t = __umulhi(m, n);
+        return (t + ((n - t) >> s1)) >> s2;
+    }
+};
+
+// d in [1, 2^31): l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1.
+static inline FastDiv make_fastdiv(uint32_t d)
+{
+    int l = 0;
+    while ((1ull << l) < d) ++l;
+    FastDiv f;
+    f.m = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
+    f.s1 = l < 1 ? (uint32_t)l : 1u;
+    f.s2 = l > 1 ? (uint32_t)(l - 1) : 0u;
+    return f;
+}
+
 // One decode problem of a launch: decoder self-attention and encoder
 // cross-attention of a step are two problems with their own block tables.
 constexpr int MAX_PROBLEMS = 2;
@@ -97,6 +123,7 @@ struct Prob {
     float scale_log2;
     int window, seq_base, num_seqs, mbps, num_blocks, max_ctx, part_blocks, max_parts, num_buckets;
     long long bias_stride;
+    FastDiv by_part_blocks;
 };
 
 struct Params {
@@ -104,6 +131,7 @@ struct Params {
     int nprob;
     int num_seqs;                // sequences of this launch over all problems (problem 0's first)
     int H;
+    FastDiv by_H;
     int32_t *status;
 };
 
@@ -133,17 +161,6 @@ __device__ __forceinline__ int seq_of_warp(int u, const int *cum, int num_seqs)
     return lo;
 }
 
-// The same for one thread on its own (binary search).
-__device__ __forceinline__ int seq_of_lane(int u, const int *cum, int num_seqs)
-{
-    int lo = 0, hi = num_seqs;                        // cum[lo] <= u < cum[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (cum[mid] <= u) lo = mid; else hi = mid;
-    }
-    return lo;
-}
-
 // Unit u of sequence s -> (h, p) and its block range.
 __device__ __forceinline__ Unit unit_in_seq(int u, int s, const int *cum, const int *ctxs, const Params &P)
 {
@@ -152,10 +169,10 @@ __device__ __forceinline__ Unit unit_in_seq(int u, int s, const int *cum, const 
     U.prob = prob_of(s, P);
     const Prob &R = P.pr[U.prob];
     U.gs = R.seq_base + s - (U.prob ? P.pr[0].num_seqs : 0);
-    U.npart = (cum[s + 1] - cum[s]) / P.H;
+    U.npart = (int)P.by_H.div((uint32_t)(cum[s + 1] - cum[s]));
     const int r = u - cum[s];
-    U.h = r / U.npart;
-    U.p = r - U.h * U.npart;
+    U.p = (int)P.by_H.div((uint32_t)r);
+    U.h = r - U.p * P.H;
     U.ctx = ctxs[s];
     U.start = (R.window > 0 && U.ctx > R.window) ? U.ctx - R.window : 0;
     if (U.ctx == 0) {
@@ -244,7 +261,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
         if (c > 0) {
             const int start = (R.window > 0 && c > R.window) ? c - R.window : 0;
             const int nblk = (c - 1) / BS - start / BS + 1;
-            npart = min((nblk + R.part_blocks - 1) / R.part_blocks, R.max_parts);
+            npart = min((int)R.by_part_blocks.div((uint32_t)(nblk + R.part_blocks - 1)), R.max_parts);
         }
         cum[s + 1] = npart * P.H;
     }
@@ -702,6 +719,7 @@ cudaError_t launch_paged_decode_multi(const DecodeArgs *a, const DecodePlan *siz
         R.max_ctx = a[i].max_context_len;
         R.part_blocks = plan[i].part_blocks;
         R.max_parts = plan[i].max_parts;
+        R.by_part_blocks = make_fastdiv((uint32_t)plan[i].part_blocks);
         R.bias_stride = a[i].bias_row_stride;
         R.seq_base = 0;
         R.num_seqs = a[i].num_seqs;
@@ -720,6 +738,7 @@ cudaError_t launch_paged_decode_multi(const DecodeArgs *a, const DecodePlan *siz
         P.nprob = 0;
         P.num_seqs = 0;
         P.H = H;
+        P.by_H = make_fastdiv((uint32_t)H);
         P.status = a[0].status;
         for (int i = 0; i < n; ++i) {
             const long long lo = std::max(base, first[i]), hi = std::min(end, first[i] + a[i].num_seqs);
