@@ -229,6 +229,14 @@ def capture_graph(fn):
     return g
 
 
+def queue_ahead():
+    """A GPU-side sleep (~0.5 ms) ahead of a timed region: the host submits the
+    timed graph while it runs, so the region's events bracket device work only,
+    not the host's graph-launch latency."""
+    import torch
+    torch.cuda._sleep(int(1e6))
+
+
 def per_launch_ms(run, nsides, K):
     """Mean device duration of each side's timed launch over K steps: run(ev)
     records ev[side][0][k] / ev[side][1][k] around the launch of step k."""
@@ -404,6 +412,7 @@ def run_decode(args, rank, world, local, peaks):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(); barrier(world)
+    queue_ahead()
     t0.record()
     graph.replay()
     t1.record()
@@ -417,6 +426,7 @@ def run_decode(args, rank, world, local, peaks):
         wgraph = capture_graph(lambda: [step(0) for _ in range(K)])
         wgraph.replay()
         torch.cuda.synchronize(); barrier(world)
+        queue_ahead()
         t0.record()
         wgraph.replay()
         t1.record()
@@ -644,6 +654,7 @@ def run_prefill(args, rank, world, local, peaks):
     graph.replay()
     t0 = torch.cuda.Event(enable_timing=True); t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(); barrier(world)
+    queue_ahead()
     t0.record()
     graph.replay()
     t1.record()
