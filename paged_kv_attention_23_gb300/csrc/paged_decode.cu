@@ -132,6 +132,7 @@ struct Params {
     int num_seqs;                // sequences of this launch over all problems (problem 0's first)
     int H;
     FastDiv by_H;
+    unsigned *queue;             // unit hand-out counter (problem 0's workspace), zero between calls
     int32_t *status;
 };
 
@@ -301,23 +302,61 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
 
 
     // ---- producer state (issue side) ---------------------------------------
+    // A warp takes units gw and gw + nwt; when the launch has more than two
+    // rounds of units the rest are handed out one at a time by an atomic
+    // counter, so warps that stream faster take more of them (a static
+    // round-robin left the slowest warps running alone for the last fifth of
+    // a large launch).  The counter wraps to zero after the launch's
+    // total_units - nwt requests (each warp's last request overshoots once).
+    const bool dyn = total_units > 2 * nwt;
+    unsigned fut = 0;                                  // lane 0: the counter's answer for the next request
+    auto request = [&]() {
+        if (lane == 0) fut = atom_inc_relaxed(P.queue, (unsigned)(total_units - nwt - 1));
+    };
+    if (dyn) request();
+    // The ids of the non-empty units this warp streams, in order: lane i % 32
+    // holds the i-th (the copy side is at most NSTAGE blocks ahead).
+    int ring = 0;
+    uint32_t ring_n = 0;
+    auto ring_push = [&](int id) {
+        if (lane == (int)(ring_n & 31)) ring = id;
+        ++ring_n;
+    };
     int pk = 0;                                        // unit ordinal of the issue side
     Unit pu = unit_of(gw, cum, ctxs, P);
-    const Unit first_unit = pu;                       // the consumer's first unit
+    const Unit first_unit = pu;                       // the consumer's first unit, when not empty
+    if (pu.nb > 0) ring_push(gw);
     int pbt = load_bt(pu, P, lane);
-    bool p_next_ok = gw + nwt < total_units;
+    int pn_id = gw + nwt;
+    bool p_next_ok = pn_id < total_units;
     Unit pn = pu;
     int pnbt = 0;
-    if (p_next_ok) { pn = unit_of(gw + nwt, cum, ctxs, P); pnbt = load_bt(pn, P, lane); }
+    if (p_next_ok) {
+        pn = unit_of(pn_id, cum, ctxs, P);
+        pnbt = load_bt(pn, P, lane);
+        if (pn.nb > 0) ring_push(pn_id);
+    }
     bool p_active = true;
     int pib = 0;
     auto p_advance_unit = [&]() {
+        if (pu.nb == 0 && lane < R::NC)                // a sequence without keys: zero output row
+            reinterpret_cast<uint4 *>(static_cast<unsigned char *>(P.pr[pu.prob].out) +
+                                      ((size_t)pu.gs * P.H + pu.h) * R::ROW)[lane] = make_uint4(0u, 0u, 0u, 0u);
         ++pk;
         if (!p_next_ok) { p_active = false; return; }
         pu = pn; pbt = pnbt; pib = 0;
-        const int nu = gw + (pk + 1) * nwt;
-        p_next_ok = nu < total_units;
-        if (p_next_ok) { pn = unit_of(nu, cum, ctxs, P); pnbt = load_bt(pn, P, lane); }
+        if (dyn && pk + 1 >= 2) {
+            pn_id = 2 * nwt + __shfl_sync(kFull, (int)fut, 0);
+            if (pn_id < total_units) request();
+        } else {
+            pn_id = gw + (pk + 1) * nwt;
+        }
+        p_next_ok = pn_id < total_units;
+        if (p_next_ok) {
+            pn = unit_of(pn_id, cum, ctxs, P);
+            pnbt = load_bt(pn, P, lane);
+            if (pn.nb > 0) ring_push(pn_id);
+        }
     };
     while (p_active && pu.nb == 0) p_advance_unit();
 
@@ -370,10 +409,9 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
         }
     };
 
-    for (int ck = 0;; ++ck) {
-        const int u = gw + ck * nwt;
-        if (u >= total_units) break;
-        const Unit cu = ck == 0 ? first_unit : unit_of(u, cum, ctxs, P);
+    for (uint32_t ck = 0; ck < ring_n; ++ck) {       // ring_n grows as the copy side advances
+        const int u = (ck == 0 && first_unit.nb > 0) ? gw : __shfl_sync(kFull, ring, (int)(ck & 31));
+        const Unit cu = u == gw ? first_unit : unit_of(u, cum, ctxs, P);
         const Prob &CP = P.pr[cu.prob];
         const bool has_bias = CP.bias != nullptr, has_table = CP.bias_table != nullptr;
         // append: the sequence's newest token (position ctx-1) lies in the last
@@ -457,7 +495,6 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
             __syncwarp();
             ++consumed;
         }
-        if (cu.nb == 0) top_up();          // keep the loads streaming past an empty unit
 
         // ---- unit finished: write out or merge partials ------------------------
         float l = l_run;                                // lanes 2k, 2k+1 hold key k's weights
@@ -627,7 +664,7 @@ size_t decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, const D
 {
     const size_t sh = (size_t)num_seqs * num_heads;
     const size_t slots = sh * plan.max_parts;
-    return round_up(sh * 4, 256) + round_up(slots * 8, 256) + round_up(slots * head_dim * 4, 256);
+    return round_up(sh * 4, 256) + round_up(slots * 8, 256) + round_up(slots * head_dim * 4, 256) + 256;
 }
 
 // Streaming warps per CTA of the configuration dispatch_cfg picks.
@@ -689,6 +726,7 @@ cudaError_t launch_paged_decode_multi(const DecodeArgs *a, const DecodePlan *siz
         pb[pick] *= 2;
     }
     Prob pr[MAX_PROBLEMS];
+    unsigned *queue = nullptr;
     for (int i = 0; i < n; ++i) {
         if (pb[i] != plan[i].part_blocks) {
             plan[i].part_blocks = pb[i];
@@ -712,6 +750,9 @@ cudaError_t launch_paged_decode_multi(const DecodeArgs *a, const DecodePlan *siz
         R.counters = reinterpret_cast<unsigned *>(ws);
         R.ws_ml = reinterpret_cast<float2 *>(ws + round_up(shi * 4, 256));
         R.ws_acc = reinterpret_cast<float *>(ws + round_up(shi * 4, 256) + round_up(slots * 8, 256));
+        if (i == 0)
+            queue = reinterpret_cast<unsigned *>(ws + round_up(shi * 4, 256) + round_up(slots * 8, 256) +
+                                                 round_up(slots * a[i].head_dim * 4, 256));
         R.scale_log2 = a[i].scale * 1.4426950408889634f;
         R.window = a[i].window;
         R.mbps = a[i].max_blocks_per_seq;
@@ -739,6 +780,7 @@ cudaError_t launch_paged_decode_multi(const DecodeArgs *a, const DecodePlan *siz
         P.num_seqs = 0;
         P.H = H;
         P.by_H = make_fastdiv((uint32_t)H);
+        P.queue = queue;
         P.status = a[0].status;
         for (int i = 0; i < n; ++i) {
             const long long lo = std::max(base, first[i]), hi = std::min(end, first[i] + a[i].num_seqs);

@@ -222,6 +222,15 @@ template <> __device__ __forceinline__ void fma2_mixed<__half>(uint32_t q, uint3
         : "r"(q), "r"(k));
 }
 
+// Relaxed increment with wrap (atomicInc semantics) at GPU scope: a counter
+// that carries no data, only an index.
+__device__ __forceinline__ unsigned atom_inc_relaxed(unsigned *p, unsigned wrap)
+{
+    unsigned old;
+    asm volatile("atom.relaxed.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(wrap) : "memory");
+    return old;
+}
+
 // Release-acquire increment with wrap (atomicInc semantics) at GPU scope.
 __device__ __forceinline__ unsigned atom_inc_acq_rel(unsigned *p, unsigned wrap)
 {

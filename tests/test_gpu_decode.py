@@ -158,6 +158,23 @@ def test_decode_long_unwindowed_many_partitions(cuda_lib):
     _check(to_f64(g.run(), F16), oracle_decode(case), F16, "long")
 
 
+@pytest.mark.parametrize("H", [5, 12, 33])
+def test_decode_head_counts_not_powers_of_two(cuda_lib, H):
+    """Units of a sequence run partition-major (unit - first = p * H + h) and the
+    kernel splits them with a precomputed divisor for H: head counts that are
+    not powers of two, against contexts from empty to many partitions, and
+    more sequences than one CTA's warps so every split lands on every warp."""
+    rng = np.random.default_rng(4000 + H)
+    ctx = np.concatenate([[0, 1, 16, 17, 2047, 2048], rng.integers(0, 2100, size=40)])
+    case = synth.make_decode_case("heads", 4000 + H, BF16, len(ctx), H, 64, context_lens=ctx, bias="gauss",
+                                  bias_stride=2100, window=-1 if H != 12 else 1500)
+    g = GpuDecode(case, cuda_lib)
+    got = to_f64(g.run(), BF16)
+    _check(got, oracle_decode(case), BF16, f"H={H}")
+    np.testing.assert_array_equal(got[0], 0.0)
+    assert int(g.status.item()) == 0
+
+
 # ---------------------------------------------------------------------------
 # poison, invariants, status
 # ---------------------------------------------------------------------------
