@@ -904,7 +904,7 @@ def run_reference(args, rank, world):
         return None
     if args.workload in PREFILL_WORKLOADS:
         layers = host_prefill_cases(args.workload, small=True)
-        per = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
+        per = max(0.25, args.ref_seconds / max(1, args.steps + args.warmup))
         oracle_prefill_sample(layers, 0.5)
         f, s, th, desc = oracle_prefill_sample(layers, per * args.steps)
         val, unit = f / s / 1e12, "TFLOP/s"
@@ -913,7 +913,7 @@ def run_reference(args, rank, world):
     else:
         n = DECODE_WORKLOADS[args.workload]
         cases = [synth.decode_workload(n)] + ([synth.cross_workload()] if n == 3 else [])
-        per = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
+        per = max(0.25, args.ref_seconds / max(1, args.steps + args.warmup))
         oracle_decode_sample(cases, 0.5)
         b, s, th, desc = oracle_decode_sample(cases, per * args.steps)
         val, unit = b / s / 1e9, "GB/s"
@@ -932,7 +932,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
     ap.add_argument("--workload", default="t5-small-decode",
