@@ -12,10 +12,13 @@
 //
 // Design (memory-bound; everything below is about keeping HBM busy):
 //  * Work unit = (s, h, partition): `part_blocks` consecutive cache blocks of
-//    the visible range.  All units carry (almost) the same bytes, so a static
-//    round-robin over a compact unit list balances the GPU.  The list is the
-//    prefix sum over sequences of H * num_partitions(s), built by every CTA
-//    into shared memory at start (one read of context_lens).
+//    the visible range.  The unit list is the prefix sum over sequences of
+//    H * num_partitions(s), built by every CTA into shared memory at start
+//    (one read of context_lens); a sequence's units run partition-major, so
+//    neighbouring warps stream neighbouring heads of the same cache blocks.
+//    Warp gw takes units gw and gw + nwt; any further units are handed out
+//    one at a time by a wrapping atomic counter, so the warps that stream
+//    faster take more of them.
 //  * Persistent grid (SMs x resident CTAs); every warp is an independent
 //    streaming pipeline over its units with NSTAGE shared-memory stages.
 //    Per stage: the K and V runs of one (block, head) — each a contiguous
@@ -25,7 +28,9 @@
 //    mbarrier per stage counts both (32 lane arrivals + the bulk bytes).
 //    Loads run up to NSTAGE blocks ahead of the math and across unit
 //    boundaries; block-table entries of the next unit are fetched one unit
-//    ahead.  Block-table entries and blocks outside the window are never read.
+//    ahead, and the math side follows the copy side's unit ids through a
+//    ring of lane registers.  Block-table entries and blocks outside the
+//    window are never read.
 //  * Math per block: 2 lanes per key compute q.k from 16-byte shared loads
 //    with mixed-precision FMA (bf16 / f16 operands, f32 accumulate; chunk
 //    order rotated per key: no bank conflicts), online softmax in the log2
@@ -36,8 +41,9 @@
 //    it writes (m, l, acc) to the workspace and bumps a per-(s, h) counter with
 //    atomicInc(npart - 1), which wraps to zero: the last partition to arrive
 //    merges all partials (every load of a chunk of partials issued at once),
-//    writes `out` and zeroes the slots it read.  A call therefore leaves the
-//    whole workspace zero, ready for the next call of any shape.
+//    writes `out` and zeroes the slots it read.  The unit counter wraps to
+//    zero as well, so a call leaves the whole workspace zero, ready for the
+//    next call of any shape.
 //  * A launch may carry two problems (a decode step's self- and
 //    cross-attention, each with its own tables, caches and workspace); the
 //    unit list runs over the concatenated sequences.
