@@ -313,6 +313,11 @@ PKA_API pka_status pka_paged_attn_decode_noalloc(void *out, const void *q, const
  *                 PKA_DEVCHK_TIMEOUT)
  * Accumulation is f32; P is rounded to the operand type (bf16 or f16) before
  * the P.V product, whose operands must share one type.
+ * Work items are handed to the CTAs by one of 1024 device counter pairs that
+ * the library owns; a launch takes the next pair in turn and leaves it at zero
+ * (also after a PKA_DEVCHK_TIMEOUT), so at most 1024 launches of this and the
+ * other prefill entry points may be in flight on the GPU at once (a launch
+ * captured into a CUDA graph keeps its pair for every replay).
  */
 PKA_API pka_status pka_swa_prefill(void *out, const void *q, const void *k, const void *v,
                            const int32_t *cu_seqlens, int num_seqs, int num_tokens, int max_seqlen,
