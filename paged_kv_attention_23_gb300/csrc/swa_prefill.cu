@@ -361,26 +361,38 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             if (!publish(t) || t >= total_items || *abort_flag) break;
             const Item I = sched.get(t);
             t = dyn ? (int)gridDim.x + (int)ahead : (PAGED ? t + (int)gridDim.x : total_items);
-            if (t < total_items) ahead = atomicAdd(P.items, 1u);
+            if (dyn && t < total_items) ahead = atomicAdd(P.items, 1u);
             if (!wait_or_abort(BAR(B_QE), (wq & 1) ^ 1, abort_flag, P.status)) break;
             const bool two = I.r0 + BM < I.L;
             mbar_arrive_expect_tx(BAR(B_QF), (two ? 2 : 1) * TILE_BYTES);
             tc::tma_load_3d(sb + OFF_Q, &tm_q, 0, I.h, I.s0 + I.r0, BAR(B_QF));
             if (two) tc::tma_load_3d(sb + OFF_Q + TILE_BYTES, &tm_q, 0, I.h, I.s0 + I.r0 + BM, BAR(B_QF));
             bool ok = true;
+            // paged: the block-table entries of key tile j + 1 are read while tile j
+            // waits for its stage, so the table's latency leaves the copy path
+            auto tile_blocks = [&](int j) { return min(BN / CBS, (I.k_end - (I.c_lo + j * BN) + CBS - 1) / CBS); };
+            auto read_table = [&](int *ids, int j) {
+                const int nblk = tile_blocks(j);
+                const int32_t *bt = P.block_tables + (size_t)I.seq * P.mbps + (I.c_lo + j * BN) / CBS;
+#pragma unroll
+                for (int b = 0; b < BN / CBS; ++b) ids[b] = b < nblk ? __ldg(bt + b) : 0;
+            };
+            int ids_next[BN / CBS];
+            if constexpr (PAGED) read_table(ids_next, 0);
             for (int j = 0; j < I.nkv; ++j, ++g) {
+                int phys[BN / CBS];
+                if constexpr (PAGED) {
+#pragma unroll
+                    for (int b = 0; b < BN / CBS; ++b) phys[b] = ids_next[b];
+                    if (j + 1 < I.nkv) read_table(ids_next, j + 1);
+                }
                 const uint32_t st = g % NS;
                 if (!wait_or_abort(BAR(B_KVE + st), ((g / NS) & 1) ^ 1, abort_flag, P.status)) { ok = false; break; }
                 const uint32_t dk = sb + OFF_KV + st * 2 * TILE_BYTES, dv = dk + TILE_BYTES;
                 if constexpr (PAGED) {
                     // the tile's cache blocks below k_end, one 16-row box each; a
                     // 2 KB box keeps the 1024-byte swizzle atoms of a contiguous tile
-                    const int c0 = I.c_lo + j * BN;
-                    const int nblk = min(BN / CBS, (I.k_end - c0 + CBS - 1) / CBS);
-                    const int32_t *bt = P.block_tables + (size_t)I.seq * P.mbps + c0 / CBS;
-                    int phys[BN / CBS];
-#pragma unroll
-                    for (int b = 0; b < BN / CBS; ++b) phys[b] = b < nblk ? __ldg(bt + b) : 0;
+                    const int nblk = tile_blocks(j);
                     mbar_arrive_expect_tx(BAR(B_KVF + st), 2u * nblk * CBLK_BYTES);
 #pragma unroll
                     for (int b = 0; b < BN / CBS; ++b) {

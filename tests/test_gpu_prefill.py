@@ -315,3 +315,29 @@ def test_prefill_f16_large_logits_stay_finite(cuda_lib):
     got = to_f64(run_gpu_prefill(cuda_lib, case), F16)
     ref = oracle.prefill(case.q, case.k, case.v, case.cu_seqlens, -1, 0, 1.0, F16)
     _check(got, ref, "f16 large logits", F16)
+
+
+def test_prefill_item_counters_are_clean_after_every_launch(cuda_lib):
+    """Packed-key launches with more items than CTAs hand items out from one
+    of 1024 counter pairs that the library owns, taken in turn by every
+    prefill launch; each launch must leave its pair at zero.  A paged launch
+    with more items than CTAs, 1023 tiny launches, then a packed launch on
+    the paged launch's pair: it still matches the oracle."""
+    import torch
+    ctx = np.array([16 + 29 * i for i in range(60)])
+    ql = np.minimum(ctx, 5 + 3 * np.arange(60))
+    pc = synth.make_paged_prefill_case("paged-cycle", 530, BF16, ctx, ql, 3, 64, -1, 1, 0, scale=1 / 8)
+    gp = GpuPagedPrefill(pc, cuda_lib)
+    case = synth.make_prefill_case("cycle", 531, [256] * 40 + [300, 17], 4, 64, -1, 0, BF16, scale=1 / 8)
+    ref = oracle.prefill(case.q, case.k, case.v, case.cu_seqlens, -1, 0, case.scale, BF16)
+    tiny = synth.make_prefill_case("tiny", 532, [16], 1, 64, -1, 0, BF16, scale=1 / 8)
+    tq, tk, tv = (to_dev(a, BF16) for a in (tiny.q, tiny.k, tiny.v))
+    tout = torch.empty_like(tq)
+    tcu = torch.from_numpy(tiny.cu_seqlens).cuda()
+    for _ in range(2):
+        gp.run()                                        # 60 sequences x 3 heads: 180 items
+        for _ in range(1023):
+            cuda_lib.swa_prefill(tout, tq, tk, tv, tcu, 16, -1, 0, 1 / 8)
+        got = to_f64(run_gpu_prefill(cuda_lib, case), BF16)   # 172 items, the paged launch's pair
+        _check(got, ref, "packed launch after a full cycle of counter pairs")
+    assert int(gp.status.item()) == 0
