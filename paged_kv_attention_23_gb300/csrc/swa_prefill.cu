@@ -687,16 +687,17 @@ __device__ unsigned g_item_counters[2 * PREFILL_SLOTS];
 unsigned *next_item_counters()
 {
     static std::atomic<unsigned> next{0};
-    static unsigned *base[64] = {};
+    static std::atomic<unsigned *> base[64];         // per device: the array's address in that context
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return nullptr;
-    if (!base[dev]) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    unsigned *b = base[dev].load(std::memory_order_acquire);
+    if (!b) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_item_counters) != cudaSuccess) return nullptr;
-        base[dev] = static_cast<unsigned *>(p);
+        b = static_cast<unsigned *>(p);
+        base[dev].store(b, std::memory_order_release);   // every thread finds the same address
     }
-    return base[dev] + 2 * (next.fetch_add(1u) % PREFILL_SLOTS);
+    return b + 2 * (next.fetch_add(1u) % PREFILL_SLOTS);
 }
 
 // ---- host: tensor maps ---------------------------------------------------------
