@@ -726,7 +726,10 @@ def run_prefill(args, rank, world, local, peaks):
 
 def prefill_e2e(args, launches, flops, world):
     """The same step through the public API from pinned host buffers: each
-    call's inputs copied host->device, the call, its output read back."""
+    call's inputs copied host->device, the call, its output read back.  The
+    copies run on a second stream, ordered by events, so a layer's inputs
+    arrive while the previous layer computes (as a serving engine pipelines
+    a step); every copy of a step is still inside the timed region."""
     import torch
     hosts = []
     h2d = 0
@@ -740,21 +743,46 @@ def prefill_e2e(args, launches, flops, world):
         hosts.append(hs)
     hout = [torch.empty(l.out.shape, dtype=l.out.dtype, pin_memory=True) for l in launches]
     d2h = sum(l.out.numel() * l.out.element_size() for l in launches)
+    main = torch.cuda.current_stream()
+    copies = torch.cuda.Stream()
+    n = len(launches)
+    ev = lambda: torch.cuda.Event()
+    inputs_in = [ev() for _ in range(n)]           # layer l's inputs on the device
+    computed = [ev() for _ in range(n)]            # layer l's call done (its inputs free, its output ready)
+    read_back = [ev() for _ in range(n)]           # layer l's output copied out
+    started = [False] * n
 
     def step():
-        for l, hs, ho in zip(launches, hosts, hout):
-            for h, d in hs:
-                d.copy_(h, non_blocking=True)
+        for j, (l, hs) in enumerate(zip(launches, hosts)):
+            with torch.cuda.stream(copies):
+                if started[j]:
+                    copies.wait_event(computed[j])        # the previous step's call has read them
+                for h, d in hs:
+                    d.copy_(h, non_blocking=True)
+                inputs_in[j].record(copies)
+        for j, (l, ho) in enumerate(zip(launches, hout)):
+            main.wait_event(inputs_in[j])
+            if started[j]:
+                main.wait_event(read_back[j])            # the previous step's output has left
             l()
-            ho.copy_(l.out, non_blocking=True)
+            computed[j].record(main)
+            started[j] = True
+            with torch.cuda.stream(copies):
+                copies.wait_event(computed[j])
+                ho.copy_(l.out, non_blocking=True)
+                read_back[j].record(copies)
+        main.wait_event(read_back[n - 1])
 
     for _ in range(args.warmup):
         step()
     a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(); barrier(world)
     a.record()
+    copies.wait_event(a)                                   # no copy of the timed steps starts before a
     for _ in range(args.steps):
         step()
+    for j in range(n):
+        main.wait_event(read_back[j])
     b.record()
     torch.cuda.synchronize(); barrier(world)
     ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
