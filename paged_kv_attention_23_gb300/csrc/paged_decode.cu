@@ -670,7 +670,7 @@ size_t decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, const D
 {
     const size_t sh = (size_t)num_seqs * num_heads;
     const size_t slots = sh * plan.max_parts;
-    return round_up(sh * 4, 256) + round_up(slots * 8, 256) + round_up(slots * head_dim * 4, 256) + 256;
+    return 256 + round_up(sh * 4, 256) + round_up(slots * 8, 256) + round_up(slots * head_dim * 4, 256);
 }
 
 // Streaming warps per CTA of the configuration dispatch_cfg picks.
@@ -753,12 +753,11 @@ cudaError_t launch_paged_decode_multi(const DecodeArgs *a, const DecodePlan *siz
         R.num_buckets = a[i].num_buckets;
         R.k_new = static_cast<const unsigned char *>(a[i].k_new);
         R.v_new = static_cast<const unsigned char *>(a[i].v_new);
-        R.counters = reinterpret_cast<unsigned *>(ws);
-        R.ws_ml = reinterpret_cast<float2 *>(ws + round_up(shi * 4, 256));
-        R.ws_acc = reinterpret_cast<float *>(ws + round_up(shi * 4, 256) + round_up(slots * 8, 256));
-        if (i == 0)
-            queue = reinterpret_cast<unsigned *>(ws + round_up(shi * 4, 256) + round_up(slots * 8, 256) +
-                                                 round_up(slots * a[i].head_dim * 4, 256));
+        // [unit hand-out counter, 256 B | arrival counters | (m, l) | acc]
+        R.counters = reinterpret_cast<unsigned *>(ws + 256);
+        R.ws_ml = reinterpret_cast<float2 *>(ws + 256 + round_up(shi * 4, 256));
+        R.ws_acc = reinterpret_cast<float *>(ws + 256 + round_up(shi * 4, 256) + round_up(slots * 8, 256));
+        if (i == 0) queue = reinterpret_cast<unsigned *>(ws);
         R.scale_log2 = a[i].scale * 1.4426950408889634f;
         R.window = a[i].window;
         R.mbps = a[i].max_blocks_per_seq;

@@ -80,9 +80,9 @@ extern "C" PKA_API pka_status pka_paged_attn_decode_noalloc(
     const pka_status st = scratch_address(&scratch);
     if (st != PKA_OK) return st;
 
-    // the arrival counters (int32 per (sequence, head), at the start of the
-    // workspace) must start at zero
-    const size_t counter_bytes = (size_t)num_seqs * num_heads * sizeof(int32_t);
+    // the unit hand-out counter (the first 256 bytes of the workspace) and the
+    // arrival counters after it (int32 per (sequence, head)) must start at zero
+    const size_t counter_bytes = 256 + (size_t)num_seqs * num_heads * sizeof(int32_t);
     if (cudaMemsetAsync(scratch, 0, counter_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PKA_ERR_CUDA;
     return pka_paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, attn_bias, sliding_window,
