@@ -362,37 +362,113 @@ def build_decode_sides(workload, device, on_device_draw, num_seqs=None):
     return cases
 
 
+def graph_ms(fn, K, world=1):
+    """Mean device time of one fn(k), k < K: the K calls are captured into one
+    CUDA graph, uploaded by an untimed replay, and one replay is timed with CUDA
+    events queued behind a GPU-side sleep (the region holds device work only)."""
+    import torch
+    g = capture_graph(lambda: [fn(k) for k in range(K)])
+    g.replay()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(); barrier(world)
+    queue_ahead()
+    t0.record()
+    g.replay()
+    t1.record()
+    torch.cuda.synchronize(); barrier(world)
+    ms = max_over_ranks(t0.elapsed_time(t1), world) / K
+    del g
+    return ms
+
+
+class DecodeBench:
+    """A decode workload resident on the device: its sides (self-attention,
+    and cross-attention for the T5-large step), rotated over enough input
+    copies that every step reads cold data."""
+
+    def __init__(self, workload, pka, device, num_seqs=None, t5_table=False, keep_tokens=False):
+        import torch
+        self.workload = workload
+        self.pka = pka
+        big = workload in ("t5-large-decode", "long-ctx-decode")
+        self.cases = build_decode_sides(workload, device, big, num_seqs)
+        self.sides = [DecodeSide(c, pka, device) for c in self.cases]
+        for sd in self.sides:
+            sd.use_table = t5_table
+        if not keep_tokens:
+            for c in self.cases:          # the token arrays are only needed again by the CPU leg
+                c.device_kv = None
+            torch.cuda.empty_cache()
+        self.t5_table = t5_table
+        self.bytes_on = [decode_alg_bytes(c, True, t5_table) for c in self.cases]
+        self.bytes_off = [decode_alg_bytes(c, False) for c in self.cases]
+        self.per_copy = sum(s.nbytes() for s in self.sides)
+        self.copies = max(1, min(16, math.ceil(3 * L2_BYTES / self.per_copy)))
+        self.rot = [self.sides] + [[s.clone() for s in self.sides] for _ in range(self.copies - 1)]
+        if len(self.sides) > 1:
+            for s in rot_sides_cross(self.rot):
+                s.append = False
+        torch.cuda.synchronize()
+
+    @property
+    def has_bias(self):
+        return any(s.bias is not None for s in self.sides)
+
+    def step(self, k, bias_on=True, fused=True, events=None):
+        decode_all(self.pka, self.rot[k % self.copies], fused, bias_on, events, k)
+
+    def total(self, bias_on):
+        return sum(b["total"] for b in (self.bytes_on if bias_on else self.bytes_off))
+
+    def l2_note(self):
+        return (f"inputs rotated over {self.copies} copies ({self.per_copy * self.copies / 2**20:.0f} MiB > L2)"
+                if self.copies > 1 else f"inputs {self.per_copy / 2**20:.0f} MiB > L2")
+
+    def record(self, K, peaks, world=1):
+        """Graph-timed launch times of the step, bias on and off, each side's
+        own launch for a two-sided step, and the bytes / fractions they give."""
+        seqs = self.cases[0].num_seqs
+        hbm = peaks["hbm_gbs"]
+
+        def entry(ms, nbytes, nseqs):
+            return {"ms_per_launch": round(ms, 5), "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                    "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4), "seqs_per_s": round(nseqs / (ms * 1e-3), 1),
+                    "alg_bytes": nbytes}
+
+        rec = {"launch": ("one launch: newest token appended + decode" +
+                          (" of self and cross" if len(self.sides) > 1 else ""))}
+        for on in ((True, False) if self.has_bias else (True,)):
+            ms = graph_ms(lambda k: self.step(k, on), K, world)
+            rec["bias_on" if on else "bias_off"] = entry(ms, self.total(on), seqs)
+        if not self.has_bias:
+            rec["bias_off"] = rec["bias_on"]
+        if len(self.sides) > 1:
+            names = ["self", "cross"]
+            for j, sd in enumerate(self.sides):
+                for on in ((True, False) if sd.bias is not None else (True,)):
+                    ms = graph_ms(lambda k: self.rot[k % self.copies][j].decode(self.pka, on), K, world)
+                    b = (self.bytes_on if on else self.bytes_off)[j]["total"]
+                    key = f"{names[j]}_separate_launch" + ("" if sd.bias is None else
+                                                             ("_bias_on" if on else "_bias_off"))
+                    rec[key] = entry(ms, b, self.cases[j].num_seqs)
+        return rec
+
+
 def run_decode(args, rank, world, local, peaks):
     import torch
     import paged_kv_attention_23_gb300 as pka
     pka.load()
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    big = args.workload in ("t5-large-decode", "long-ctx-decode")
-    cases = build_decode_sides(args.workload, device, big, args.num_seqs)
-    sides = [DecodeSide(c, pka, device) for c in cases]
-    for sd in sides:
-        sd.use_table = args.t5_table
-    if args.no_cpu_baseline:
-        for c in cases:               # the token arrays are only needed again by the CPU leg
-            c.device_kv = None
-        torch.cuda.empty_cache()
-    bytes_on = [decode_alg_bytes(c, True, args.t5_table) for c in cases]
-    bytes_off = [decode_alg_bytes(c, False) for c in cases]
-    step_bytes = sum(b["total"] for b in bytes_on)
-    per_copy = sum(s.nbytes() for s in sides)
-    copies = max(1, min(16, math.ceil(3 * L2_BYTES / per_copy)))
-    rot = [sides] + [[s.clone() for s in sides] for _ in range(copies - 1)]
-    torch.cuda.synchronize()
-
+    db = DecodeBench(args.workload, pka, device, args.num_seqs, args.t5_table)
+    cases, sides = db.cases, db.sides
     fused = not args.separate_launches
     nlaunch = 1 if fused else len(sides)
-    if len(sides) > 1:
-        for s in rot_sides_cross(rot):
-            s.append = False
+    step_bytes = db.total(True)
 
     def step(i, bias_on=True, events=None):
-        decode_all(pka, rot[i % copies], fused, bias_on, events, i)
+        db.step(i, bias_on, fused, events)
 
     clocks = ClockSampler(gpu_id(local))
     clocks.start()
@@ -417,58 +493,56 @@ def run_decode(args, rank, world, local, peaks):
     graph.replay()
     t1.record()
     torch.cuda.synchronize(); barrier(world)
-    clk = clocks.stop()
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
     ms_step = total_ms / K
+    del graph
+    # bias off, timed the same way (one graph of K steps)
+    off_ms = graph_ms(lambda k: step(k, False), K, world) if db.has_bias else None
+    clk = clocks.stop()
     # warm-L2 reference (labelled, not the metric): the same steps on one input copy
-    warm_ms = None
-    if copies > 1:
-        wgraph = capture_graph(lambda: [step(0) for _ in range(K)])
-        wgraph.replay()
-        torch.cuda.synchronize(); barrier(world)
-        queue_ahead()
-        t0.record()
-        wgraph.replay()
-        t1.record()
-        torch.cuda.synchronize(); barrier(world)
-        warm_ms = max_over_ranks(t0.elapsed_time(t1), world) / K
-    # per-launch durations: the same K steps eagerly, queued behind a GPU-side
-    # sleep so the host is ahead and events see kernel time, not launch gaps
+    warm_ms = graph_ms(lambda k: step(0), K, world) if db.copies > 1 else None
+    # per-launch durations by event pairs (labelled; they add a few microseconds
+    # of their own to a short launch), and, for separate launches, each side's
+    # launch graph-timed on its own
     launch_ms = per_launch_ms(lambda ev: [step(k, True, ev) for k in range(K)], nlaunch, K)
-    off_ms = None
-    if any(s.bias is not None for s in sides):
-        off_ms = sum(per_launch_ms(lambda ev: [step(k, False, ev) for k in range(K)], nlaunch, K))
+    bytes_on, bytes_off = db.bytes_on, db.bytes_off
     if fused:                          # one launch carries every side's bytes
         bytes_on = [{k: sum(b[k] for b in bytes_on) for k in bytes_on[0]}]
         bytes_off = [{k: sum(b[k] for b in bytes_off) for k in bytes_off[0]}]
+        graph_launch_ms = [ms_step]
+    else:
+        graph_launch_ms = [graph_ms(lambda k: db.rot[k % db.copies][j].decode(pka, True), K, world)
+                           for j in range(len(sides))]
 
     value = step_bytes * world / (ms_step * 1e-3) / 1e9
-    # dominant kernel: the decode launch carrying the most bytes
+    # dominant kernel: the decode launch carrying the most bytes, its average
+    # duration from a graph of its launches alone (the fused step is one launch)
     jd = int(np.argmax([b["total"] for b in bytes_on]))
-    # The launch's average duration: when a step is exactly one kernel launch (the fused step), the
-    # event-timed graph region / K; otherwise per-launch event pairs, which add a few microseconds of
-    # their own to a short launch (an empty launch of this shape reads ~4.5 us that way, ~1.3 us in
-    # the graph).
-    launch_avg_ms = ms_step if fused else launch_ms[jd]
+    launch_avg_ms = graph_launch_ms[jd]
     achieved = bytes_on[jd]["total"] / (launch_avg_ms * 1e-3) / 1e9
     traffic = recorded_traffic("paged_decode.cu", args.workload)
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
             "kernel": "paged_decode_kernel", "alg_bytes_per_launch": bytes_on[jd]["total"],
             "launch_ms": round(launch_avg_ms, 5),
-            "launch_timing": ("timed region / steps (one launch per step)" if fused else "per-launch event pairs"),
+            "launch_timing": ("timed graph region / steps (one launch per step)" if fused
+                              else "a graph of that launch alone / launches"),
             "launch_ms_event_pairs": round(launch_ms[jd], 5), "peak_src": peaks["src"] + " hbm_gbs (copy)"}
     e2e = decode_e2e(args, sides, pka, step_bytes, world, fused) if not args.no_e2e else None
-    seqs = sum(c.num_seqs for c in cases[:1])
+    seqs = cases[0].num_seqs
+    off_bytes = db.total(False)
     extra = {
-        "decode_ms_per_launch": [round(x, 5) for x in launch_ms],
-        "decode_GBps_per_launch": [round(b["total"] / (m * 1e-3) / 1e9, 1) for b, m in zip(bytes_on, launch_ms)],
-        "kv_GBps": round(sum(b["kv"] for b in bytes_on) / (sum(launch_ms) * 1e-3) / 1e9, 1),
-        "seqs_per_s": round(seqs / (sum(launch_ms) * 1e-3), 1),
-        "bias_off_decode_GBps": (round(sum(b["total"] for b in bytes_off) / (off_ms * 1e-3) / 1e9, 1)
-                                 if off_ms else None),
-        "bias_off_seqs_per_s": round(seqs / (off_ms * 1e-3), 1) if off_ms else None,
-        "alg_bytes_per_step": step_bytes,
+        "bias_on": {"ms_per_step": round(ms_step, 5), "GBps": round(value / world, 1),
+                    "frac": round(step_bytes / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                    "kv_GBps": round(sum(b["kv"] for b in db.bytes_on) / (ms_step * 1e-3) / 1e9, 1),
+                    "seqs_per_s": round(seqs / (ms_step * 1e-3), 1), "alg_bytes": step_bytes},
+        "bias_off": ({"ms_per_step": round(off_ms, 5), "GBps": round(off_bytes / (off_ms * 1e-3) / 1e9, 1),
+                      "frac": round(off_bytes / (off_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                      "seqs_per_s": round(seqs / (off_ms * 1e-3), 1), "alg_bytes": off_bytes}
+                     if off_ms else None),
+        "timing": "bias on and off: one CUDA graph of the K steps each, cold L2",
+        "decode_ms_per_launch_graph": [round(x, 5) for x in graph_launch_ms],
+        "decode_ms_per_launch_event_pairs": [round(x, 5) for x in launch_ms],
         "warm_l2_GBps": round(step_bytes * world / (warm_ms * 1e-3) / 1e9, 1) if warm_ms else None,
         "warm_l2_ms_per_step": round(warm_ms, 5) if warm_ms else None,
     }
@@ -477,13 +551,18 @@ def run_decode(args, rank, world, local, peaks):
            "window": [c.window for c in cases],
            "bias": [("t5 table in kernel" if args.t5_table and c.bias_table is not None else "materialised")
                     if c.bias is not None else None for c in cases],
-           "l2": f"inputs rotated over {copies} copies ({per_copy * copies / 2**20:.0f} MiB > L2)"
-           if copies > 1 else f"inputs {per_copy / 2**20:.0f} MiB > L2", "parallelism": f"replicas x{world}",
+           "l2": db.l2_note(), "parallelism": f"replicas x{world}",
            "launches_per_step": ("one: append of the newest token + decode" + (" of self and cross" if len(sides) > 1 else ""))
            if fused else "reshape_and_cache per side, then one decode per side"}
-    return {"value": value, "unit": "GB/s", "ms_per_step": ms_step, "dtype": synth.DTYPE_NAMES[cases[0].dtype],
-            "config": cfg, "roofline": roof, "e2e": e2e, "clocks": clk,
-            "gpu_launches": K * (1 if fused else 2 * len(sides)), "extra": extra, "cases": cases}
+    res = {"value": value, "unit": "GB/s", "ms_per_step": ms_step, "dtype": synth.DTYPE_NAMES[cases[0].dtype],
+           "config": cfg, "roofline": roof, "e2e": e2e, "clocks": clk,
+           "gpu_launches": K * (1 if fused else 2 * len(sides)), "extra": extra}
+    if not args.separate_launches and not args.t5_table and args.num_seqs is None:
+        res["record"] = db.record(K, peaks, world) if args.per_config else None
+    del db, sides, cases
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
 
 
 def decode_e2e(args, sides, pka, step_bytes, world, fused=False):
@@ -679,9 +758,12 @@ def run_prefill(args, rank, world, local, peaks):
     graph.replay()
     t1.record()
     torch.cuda.synchronize(); barrier(world)
-    clk = clocks.stop()
     ms_step = max_over_ranks(t0.elapsed_time(t1), world) / K
-    launch_ms = per_launch_ms(lambda ev: [step(ev, k) for k in range(K)], len(launches), K)
+    del graph
+    # each call's launch time from a graph of K launches of that call alone
+    launch_ms = [graph_ms(lambda k, l=l: l.fn(), K, world) for l in launches]
+    clk = clocks.stop()
+    pair_ms = per_launch_ms(lambda ev: [step(ev, k) for k in range(K)], len(launches), K)
     value = sum(flops) * world / (ms_step * 1e-3) / 1e12
     jd = int(np.argmax(flops))
     ach = flops[jd] / (launch_ms[jd] * 1e-3) / 1e12
@@ -695,8 +777,10 @@ def run_prefill(args, rank, world, local, peaks):
     roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
             "frac": round(ach / peak, 4), "traffic": recorded_traffic("swa_prefill.cu", args.workload),
             "kernel": kname, "alg_flops_per_launch": flops[jd],
-            "launch_ms": round(launch_ms[jd], 4), "peak_src": peaks["src"] + " bf16_tflops (burst)"}
+            "launch_ms": round(launch_ms[jd], 4), "launch_timing": "a graph of that launch alone / launches",
+            "peak_src": peaks["src"] + " bf16_tflops (burst)"}
     extra = {"launch_ms": [round(x, 4) for x in launch_ms],
+             "launch_ms_event_pairs": [round(x, 4) for x in pair_ms],
              "launch_TFLOPs": [round(f / (m * 1e-3) / 1e12, 2) for f, m in zip(flops, launch_ms)],
              "flops_per_step": sum(flops)}
     if args.workload == "encoder-prefill":
@@ -718,10 +802,79 @@ def run_prefill(args, rank, world, local, peaks):
         cfg["query_lens"] = "min(ctx, U[1,256])"
         cfg["bias"] = ["T5 table, non-negative half (self)", None]
         cfg["l2"] = "self + cross caches 1.6 GB > L2"
-    return {"value": value, "unit": "TFLOP/s", "ms_per_step": ms_step, "dtype": "bf16", "config": cfg,
-            "roofline": roof, "e2e": e2e, "clocks": clk,
-            "gpu_launches": K * sum(1 + (l.pre is not None) for l in launches), "extra": extra, "cases": cases,
-            "launches": launches}
+    res = {"value": value, "unit": "TFLOP/s", "ms_per_step": ms_step, "dtype": "bf16", "config": cfg,
+           "roofline": roof, "e2e": e2e, "clocks": clk,
+           "gpu_launches": K * sum(1 + (l.pre is not None) for l in launches), "extra": extra}
+    if args.workload == "encoder-prefill" and args.per_config:
+        res["record"] = prefill_record(launches, K, peaks, world, ms_step=ms_step, launch_ms=launch_ms)
+    del launches
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def prefill_record(launches, K, peaks, world=1, ms_step=None, launch_ms=None):
+    """Graph-timed layer launches and step of the encoder prefill: TFLOP/s and
+    the fraction of the bf16 peak per layer and for the step; the window
+    layers also in GB/s of their q, k, v reads and out writes."""
+    if launch_ms is None:
+        launch_ms = [graph_ms(lambda k, l=l: l.fn(), K, world) for l in launches]
+    if ms_step is None:
+        ms_step = graph_ms(lambda k: [l.fn() for l in launches], K, world)
+    bf16, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    layers = []
+    for l, ms in zip(launches, launch_ms):
+        c = l.case
+        tf = l.flops / (ms * 1e-3) / 1e12
+        e = {"layer": c.name, "window": c.window, "ms_per_launch": round(ms, 4), "TFLOPs": round(tf, 1),
+             "frac_bf16": round(tf / bf16, 4), "alg_flops": l.flops}
+        if c.window > 0:
+            nbytes = 4 * c.num_tokens * c.num_heads * c.head_dim * 2
+            e["GBps"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
+            e["frac_hbm"] = round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4)
+            e["alg_bytes"] = nbytes
+        layers.append(e)
+    flops = sum(l.flops for l in launches)
+    tf = flops / (ms_step * 1e-3) / 1e12
+    return {"layers": layers, "step": {"ms_per_step": round(ms_step, 4), "TFLOPs": round(tf, 1),
+                                       "frac_bf16": round(tf / bf16, 4), "alg_flops": flops},
+            "timing": "one CUDA graph of K launches per layer, and of K steps"}
+
+
+def per_config_records(args, world, local, peaks, headline):
+    """Every target workload measured the same way in the same run: decode
+    configs graph-timed bias on and off (and, for the T5-large step, each
+    attention type's own launch); the encoder prefill per layer and per step.
+    The headline workload's record comes from its own run."""
+    import torch
+    import paged_kv_attention_23_gb300 as pka
+    device = f"cuda:{local}"
+    out = {}
+    clocks = ClockSampler(gpu_id(local))
+    clocks.start()
+    for n, name in ((1, "tiny-decode"), (2, "t5-small-decode"), (3, "t5-large-decode"), (4, "encoder-prefill"),
+                    (5, "long-ctx-decode")):
+        key = f"config {n}: {name}"
+        if name == args.workload and headline is not None:
+            out[key] = headline
+            continue
+        if name == "encoder-prefill":
+            launches = build_prefill_launches(argparse.Namespace(workload=name), pka, device)
+            for _ in range(args.warmup):
+                for l in launches:
+                    l()
+            out[key] = prefill_record(launches, args.steps, peaks, world)
+            del launches
+        else:
+            db = DecodeBench(name, pka, device)
+            for w in range(args.warmup):
+                db.step(w)
+            out[key] = db.record(args.steps, peaks, world)
+            del db
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    out["clocks"] = clocks.stop()
+    return out
 
 
 def prefill_e2e(args, launches, flops, world):
@@ -731,11 +884,21 @@ def prefill_e2e(args, launches, flops, world):
     arrive while the previous layer computes (as a serving engine pipelines
     a step); every copy of a step is still inside the timed region."""
     import torch
+    # Each distinct device input is copied once per step, in the batch of the
+    # first call that reads it (several calls share cu_seqlens, or q); the
+    # next step's copy of a batch waits for the last call that reads any of it.
     hosts = []
     h2d = 0
-    for l in launches:
+    first = {}
+    last_reader = list(range(len(launches)))
+    for j, l in enumerate(launches):
         hs = []
         for t in l.host_inputs:
+            if t.data_ptr() in first:
+                i = first[t.data_ptr()]
+                last_reader[i] = max(last_reader[i], j)
+                continue
+            first[t.data_ptr()] = j
             h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
             h.copy_(t)
             hs.append((h, t))
@@ -755,8 +918,8 @@ def prefill_e2e(args, launches, flops, world):
     def step():
         for j, (l, hs) in enumerate(zip(launches, hosts)):
             with torch.cuda.stream(copies):
-                if started[j]:
-                    copies.wait_event(computed[j])        # the previous step's call has read them
+                if started[last_reader[j]]:
+                    copies.wait_event(computed[last_reader[j]])   # the previous step's calls have read them
                 for h, d in hs:
                     d.copy_(h, non_blocking=True)
                 inputs_in[j].record(copies)
@@ -933,16 +1096,54 @@ def host_prefill_cases(workload, small=False):
     return [synth.prefill_workload(l) for l in range(3)]
 
 
-def cpu_baseline(res, args):
-    budget = args.cpu_seconds
-    if args.workload in PREFILL_WORKLOADS:
-        cases = host_prefill_cases(args.workload, small=True) if args.workload == "t5-paged-prefill" else res["cases"]
-        f, s, th, desc = oracle_prefill_sample(cases, budget)
-        if args.workload == "t5-paged-prefill":
+def host_decode_cases(workload):
+    """Host-drawn cases of a decode workload for the oracle: the whole batch
+    for the small workloads, 32 sequences of the same shapes (the first 32
+    draws of the same laws) for the multi-GB ones."""
+    n = DECODE_WORKLOADS[workload]
+    if n in (3, 5):
+        cases = [synth.decode_workload(n, num_seqs=32)] + ([synth.cross_workload(num_seqs=32)] if n == 3 else [])
+        return cases, "32 sequences of the same shapes, drawn on the host"
+    return [synth.decode_workload(n)], "the whole batch, drawn on the host"
+
+
+def oracle_leg(workload, budget_s):
+    """The fp64 oracle timed on the host cores on a bounded sample of the
+    workload: (value, unit, threads, sample description, seconds)."""
+    if workload in PREFILL_WORKLOADS:
+        cases = host_prefill_cases(workload, small=True)
+        oracle_prefill_sample(cases, 0.5)             # warm-up: pages the arrays in
+        f, s, th, desc = oracle_prefill_sample(cases, budget_s)
+        if workload == "t5-paged-prefill" or workload == "t5-encoder-prefill":
             desc += " (32 sequences of the same shapes, drawn on the host)"
-        return {"value": round(f / s / 1e12, 6), "unit": "TFLOP/s", "cores": th, "kind": "oracle", "sample": desc}
-    b, s, th, desc = oracle_decode_sample(res["cases"], budget)
-    return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": th, "kind": "oracle", "sample": desc}
+        return f / s / 1e12, "TFLOP/s", th, desc, s
+    cases, note = host_decode_cases(workload)
+    oracle_decode_sample(cases, 0.5)
+    b, s, th, desc = oracle_decode_sample(cases, budget_s)
+    return b / s / 1e9, "GB/s", th, f"{desc} ({note})", s
+
+
+def cpu_baseline(args):
+    """The oracle leg in a child process: no CUDA context, no torch threads,
+    no clock sampler -- the same conditions as the reference arm -- so the two
+    arms' oracle numbers agree on the same box."""
+    load = os.getloadavg()
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-leg", "--workload", args.workload,
+           "--cpu-seconds", str(args.cpu_seconds)]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600 + 4 * args.cpu_seconds)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle leg failed: {r.stderr[-2000:]}")
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    d["conditions"] = (f"child process without a CUDA context, {d['cores']} oracle threads; host load average "
+                       f"{load[0]:.2f} (1 min) before it started")
+    return d
+
+
+def oracle_leg_main(args):
+    val, unit, th, desc, _ = oracle_leg(args.workload, args.cpu_seconds)
+    print(json.dumps({"value": round(val, 6), "unit": unit, "cores": th, "kind": "oracle", "sample": desc}),
+          flush=True)
 
 
 def run_reference(args, rank, world):
@@ -950,28 +1151,15 @@ def run_reference(args, rank, world):
     bounded sample per step."""
     if rank != 0:
         return None
-    if args.workload in PREFILL_WORKLOADS:
-        layers = host_prefill_cases(args.workload, small=True)
-        per = max(0.25, args.ref_seconds / max(1, args.steps + args.warmup))
-        oracle_prefill_sample(layers, 0.5)
-        f, s, th, desc = oracle_prefill_sample(layers, per * args.steps)
-        val, unit = f / s / 1e12, "TFLOP/s"
-        cfg = {"workload": args.workload}
-        dt = "f64"
-    else:
-        n = DECODE_WORKLOADS[args.workload]
-        cases = [synth.decode_workload(n)] + ([synth.cross_workload()] if n == 3 else [])
-        per = max(0.25, args.ref_seconds / max(1, args.steps + args.warmup))
-        oracle_decode_sample(cases, 0.5)
-        b, s, th, desc = oracle_decode_sample(cases, per * args.steps)
-        val, unit = b / s / 1e9, "GB/s"
-        cfg = {"workload": args.workload}
-        dt = "f64"
+    per = max(0.25, args.ref_seconds / max(1, args.steps + args.warmup))
+    load = os.getloadavg()
+    val, unit, th, desc, s = oracle_leg(args.workload, per * args.steps)
     line = {"metric": METRIC, "value": round(val, 6), "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(s * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic", "config": cfg,
-            "impl": "reference",
-            "cpu_baseline": {"value": round(val, 6), "unit": unit, "cores": th, "kind": "oracle", "sample": desc},
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload}, "impl": "reference",
+            "cpu_baseline": {"value": round(val, 6), "unit": unit, "cores": th, "kind": "oracle", "sample": desc,
+                             "conditions": f"{th} oracle threads; host load average {load[0]:.2f} (1 min) before"},
             "e2e": {"value": round(val, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     return line
 
@@ -983,7 +1171,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
-    ap.add_argument("--workload", default="t5-small-decode",
+    ap.add_argument("--workload", default="long-ctx-decode",
                     choices=sorted(DECODE_WORKLOADS) + list(PREFILL_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--separate-launches", action="store_true",
@@ -997,9 +1185,19 @@ def main():
                     help="profiling only: fewer sequences than the named decode workload")
     ap.add_argument("--clock-soak", type=float, default=1.5,
                     help="seconds of untimed steps while nvidia-smi samples clocks before the warm-up")
+    ap.add_argument("--per-config", dest="per_config", action="store_true", default=None,
+                    help="also measure every target workload (default with one GPU and the default step)")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false")
+    ap.add_argument("--oracle-leg", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.oracle_leg:
+        oracle_leg_main(args)
+        return
     rank, world, local = dist_setup()
+    if args.per_config is None:
+        args.per_config = (world == 1 and not args.separate_launches and not args.t5_table
+                           and args.num_seqs is None)
     if args.impl == "reference":
         line = run_reference(args, rank, world)
         if line is not None:
@@ -1012,15 +1210,16 @@ def main():
         res = run_decode(args, rank, world, local, peaks)
     if rank != 0:
         return
+    per_cfg = per_config_records(args, world, local, peaks, res.get("record")) if args.per_config else None
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(res, args)
+        cpu = cpu_baseline(args)
     line = {"metric": METRIC, "value": round(res["value"], 3), "unit": res["unit"], "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": res["dtype"],
             "data": "synthetic (seeded)", "config": res["config"], "roofline": res["roofline"],
             "cpu_baseline": cpu, "e2e": res["e2e"], "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
-            "extra": res["extra"]}
+            "extra": dict(res["extra"], per_config=per_cfg)}
     print(json.dumps(line), flush=True)
 
 

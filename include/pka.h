@@ -112,7 +112,10 @@ PKA_API pka_status pka_reshape_and_cache(const void *key, const void *value, voi
  * block-table entries outside the window are never read — blocks before the
  * window may be evicted ("[V1] Add sliding window support to Flex Attention
  * backend": the direct build skips blocks outside the window when the page
- * table evicts them).
+ * table evicts them).  Cache rows outside [start, ctx) inside the blocks
+ * that are read -- the rows past ctx in the sequence's last block (not yet
+ * written), the rows before start in the window's first block -- may hold any
+ * bits, NaN and Inf included: they contribute exactly nothing.
  *
  *   out           [num_seqs, num_heads, head_dim] of dtype
  *   q             [num_seqs, num_heads, head_dim] of dtype
@@ -313,11 +316,18 @@ PKA_API pka_status pka_paged_attn_decode_noalloc(void *out, const void *q, const
  *                 PKA_DEVCHK_TIMEOUT)
  * Accumulation is f32; P is rounded to the operand type (bf16 or f16) before
  * the P.V product, whose operands must share one type.
- * Work items are handed to the CTAs by one of 1024 device counter pairs that
- * the library owns; a launch takes the next pair in turn and leaves it at zero
- * (also after a PKA_DEVCHK_TIMEOUT), so at most 1024 launches of this and the
- * other prefill entry points may be in flight on the GPU at once (a launch
- * captured into a CUDA graph keeps its pair for every replay).
+ * Work items are handed to the CTAs through a pair of device counters that
+ * the library owns (no workspace argument); a launch leaves its pair at zero
+ * when it ends (also after a PKA_DEVCHK_TIMEOUT).
+ *  - An eager launch takes the next of 1024 pairs in turn, shared by this and
+ *    the other prefill entry points: at most 1024 eager launches may be in
+ *    flight on the GPU at once.
+ *  - A launch made while `stream` is being captured into a CUDA graph takes a
+ *    pair that no other launch is ever given (8192 such pairs per device per
+ *    process), which the graph keeps for every replay; replays of one
+ *    instantiated graph are ordered, so they never share it at once.  Do not
+ *    run two instances of one captured graph at the same time.  Captures past
+ *    the 8192th deal items statically (no counter; correct, somewhat slower).
  */
 PKA_API pka_status pka_swa_prefill(void *out, const void *q, const void *k, const void *v,
                            const int32_t *cu_seqlens, int num_seqs, int num_tokens, int max_seqlen,

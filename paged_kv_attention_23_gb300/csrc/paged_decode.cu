@@ -35,6 +35,9 @@
 //    with mixed-precision FMA (bf16 / f16 operands, f32 accumulate; chunk
 //    order rotated per key: no bank conflicts), online softmax in the log2
 //    domain (ex2.approx), P.V with one 16-byte V load per lane per row group.
+//    In a block at the window's start or the context's end, the V rows of
+//    keys outside [start, ctx) are replaced by zeros before P.V: those cache
+//    rows may hold any bits (an unwritten tail, NaN included).
 //  * Bias: a materialised A (streamed with the keys), or the T5 table read
 //    from shared memory at column min(ctx-1-j, buckets-1), or none.
 //  * A unit that is its (s, h)'s only partition writes `out` directly.  Else
@@ -489,12 +492,21 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
             m_run = m_new;
 #pragma unroll
             for (int e = 0; e < R::EPC; ++e) acc[e] *= corr;
+            // A block at the window's start or the context's end holds rows
+            // outside [start, ctx): cache rows that were never written, or
+            // were written for another request, may hold any bits (NaN, Inf).
+            // Their weight is 0, and their V row is replaced by zeros, so
+            // such a row contributes exactly nothing (0 * NaN would be NaN).
+            const int jb0 = (cu.b0 + cb) * BS;
+            const bool edge = jb0 < cu.start || jb0 + BS > cu.ctx;
 #pragma unroll
             for (int it = 0; it < R::PV_IT; ++it) {
                 const int row = it * R::RPI + vr;
                 const float pr = __shfl_sync(kFull, p, row * 2);
+                uint4 raw = *reinterpret_cast<const uint4 *>(stp + R::V_OFF + row * R::ROW + vc * 16);
+                if (edge && (jb0 + row < cu.start || jb0 + row >= cu.ctx)) raw = make_uint4(0u, 0u, 0u, 0u);
                 float vf[R::EPC];
-                Vec<T>::to_f32(*reinterpret_cast<const uint4 *>(stp + R::V_OFF + row * R::ROW + vc * 16), vf);
+                Vec<T>::to_f32(raw, vf);
 #pragma unroll
                 for (int e = 0; e < R::EPC; ++e) acc[e] = fmaf(pr, vf[e], acc[e]);
             }

@@ -15,13 +15,16 @@
 //  * A call whose scratch need (pka_paged_attn_decode_workspace_size) exceeds
 //    that size is rejected with PKA_ERR_WORKSPACE before anything is enqueued.
 //  * All calls on a device share the one array, and it keeps whatever the last
-//    call left in it.  Each call clears the part that must start at zero (the
-//    split-K arrival counters) on its own stream before the kernel runs.  Two
+//    call left in it.  Each call clears the part that must start at zero -- the
+//    first 256 bytes (the unit hand-out counter) and the split-K arrival
+//    counters after them -- on its own stream before the kernel runs.  Two
 //    calls whose work overlaps on the GPU (different streams, not ordered by
 //    events) race on the array and give wrong results.
 //  * The array's device address is looked up once per device, on the first
-//    call made while that device is current; make that first call before any
-//    stream capture begins.
+//    call made while that device is current (and again if the device's
+//    context was created anew, e.g. after cudaDeviceReset, since the module
+//    then lives at a new address); make that first call before any stream
+//    capture begins.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -34,24 +37,32 @@ static __device__ __align__(256) unsigned char pka_noalloc_scratch[PKA_NOALLOC_S
 
 constexpr int kMaxDevices = 128;
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices];   // device address of the array, per device ordinal
+struct ScratchAddr {
+    void *ctx;    // the context the address belongs to
+    void *addr;   // device address of the array in that context
+};
+ScratchAddr g_scratch_addr[kMaxDevices];   // per device ordinal
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, never a device address, so
-// the address comes from the runtime, once per device.
+// the address comes from the runtime, once per device (and once more for a
+// context that replaced the one the cached address belongs to).
 pka_status scratch_address(void **addr)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return PKA_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    ScratchAddr &c = g_scratch_addr[dev];
+    void *ctx = pka::current_context();
+    if (c.addr == nullptr || ctx == nullptr || c.ctx != ctx) {
         void *p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, pka_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr) return PKA_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        c.addr = p;
+        c.ctx = pka::current_context();   // the lookup made the context current if none was
     }
-    *addr = g_scratch_addr[dev];
+    *addr = c.addr;
     return PKA_OK;
 }
 

@@ -1,9 +1,33 @@
 // pka_abi.cu — the extern "C" entry points of libpka.so: argument checks on
 // the host, then one launch on the caller's stream.  Nothing here allocates.
+#include <cuda.h>
+
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "pka_launch.h"
+
+namespace pka {
+
+void *current_context()
+{
+    using GetCurrentFn = CUresult (*)(CUcontext *);
+    static GetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<GetCurrentFn>(p);
+    });
+    CUcontext c = nullptr;
+    if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+}  // namespace pka
 
 namespace {
 

@@ -9,6 +9,12 @@
 
 namespace pka {
 
+// The driver's handle of the CUDA context current on this thread (NULL when
+// none is).  Host code that caches a device address of a static __device__
+// array keys the cache on it: a context created anew (after cudaDeviceReset)
+// loads the module again, at a new address.
+void *current_context();
+
 // ---- reshape_and_cache ------------------------------------------------------
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
                                      const int64_t *slot_mapping, int num_tokens, int num_heads,

@@ -332,11 +332,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     // counter one at a time: CTAs that finish early take more, where a static
     // deal left the last CTA 5-20 % behind the average (full layer 1.97 ->
     // 1.92 ms, chunked layer 0.41 -> 0.37 ms).  The paged instance keeps the
-    // static deal c, c + G, c + 2G, ... (15 % faster there).  The producer
+    // static deal c, c + G, c + 2G, ... (15 % faster there), as does a launch
+    // given no counter pair (P.items == NULL).  The producer
     // thread hands each id to the MMA threads and softmax warps through a
     // two-entry ring in shared memory; an id >= total_items ends the CTA's work.
     volatile int *item_ring = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);
-    const bool dyn = !PAGED && total_items > (int)gridDim.x;
+    const bool dyn = !PAGED && P.items != nullptr && total_items > (int)gridDim.x;
 
     if (warp == 0 && lane == 0) {
         // ======================= TMA producer =======================
@@ -360,7 +361,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         for (;; ++wq) {
             if (!publish(t) || t >= total_items || *abort_flag) break;
             const Item I = sched.get(t);
-            t = dyn ? (int)gridDim.x + (int)ahead : (PAGED ? t + (int)gridDim.x : total_items);
+            t = dyn ? (int)gridDim.x + (int)ahead : t + (int)gridDim.x;
             if (dyn && t < total_items) ahead = atomicAdd(P.items, 1u);
             if (!wait_or_abort(BAR(B_QE), (wq & 1) ^ 1, abort_flag, P.status)) break;
             const bool two = I.r0 + BM < I.L;
@@ -677,27 +678,65 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
 }
 
-// Item counters of prefill launches: a launch takes the next of PREFILL_SLOTS
-// pairs in turn (zero between launches: the last CTA of a launch resets its
-// pair), so launches that may run at the same time use different pairs as
-// long as fewer than PREFILL_SLOTS are in flight at once.
+// Item counters of prefill launches.  An eager launch takes the next of
+// PREFILL_SLOTS pairs in turn (zero between launches: the last CTA of a launch
+// resets its pair), so eager launches that may run at the same time use
+// different pairs as long as fewer than PREFILL_SLOTS are in flight at once.
+// A launch captured into a CUDA graph keeps its pair for every replay, so it
+// takes a pair of its own from CAPTURE_SLOTS pairs that are never handed out
+// again; once those are used up, captured launches get no pair and deal items
+// statically (CTA c takes items c, c + G, ...), which needs no counter.
 constexpr int PREFILL_SLOTS = 1024;
+constexpr int CAPTURE_SLOTS = 8192;
 __device__ unsigned g_item_counters[2 * PREFILL_SLOTS];
+__device__ unsigned g_capture_counters[2 * CAPTURE_SLOTS];
 
-unsigned *next_item_counters()
+struct CounterArrays {
+    void *ctx;                    // the context the addresses belong to
+    unsigned *eager, *captured;   // device addresses of the two arrays there
+};
+
+// The two arrays' device addresses in the current context (looked up once per
+// device, and again for a context that replaced the cached one).
+bool counter_arrays(unsigned **eager, unsigned **captured)
 {
-    static std::atomic<unsigned> next{0};
-    static std::atomic<unsigned *> base[64];         // per device: the array's address in that context
+    static std::mutex mu;
+    static CounterArrays cache[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    unsigned *b = base[dev].load(std::memory_order_acquire);
-    if (!b) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_item_counters) != cudaSuccess) return nullptr;
-        b = static_cast<unsigned *>(p);
-        base[dev].store(b, std::memory_order_release);   // every thread finds the same address
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    CounterArrays &c = cache[dev];
+    void *ctx = current_context();
+    if (c.eager == nullptr || ctx == nullptr || c.ctx != ctx) {
+        void *a = nullptr, *b = nullptr;
+        if (cudaGetSymbolAddress(&a, g_item_counters) != cudaSuccess ||
+            cudaGetSymbolAddress(&b, g_capture_counters) != cudaSuccess)
+            return false;
+        c.eager = static_cast<unsigned *>(a);
+        c.captured = static_cast<unsigned *>(b);
+        c.ctx = current_context();
     }
-    return b + 2 * (next.fetch_add(1u) % PREFILL_SLOTS);
+    *eager = c.eager;
+    *captured = c.captured;
+    return true;
+}
+
+// The counter pair of the next launch on `stream`: *pair = NULL (with true)
+// means a captured launch past CAPTURE_SLOTS, which deals items statically.
+bool next_item_counters(cudaStream_t stream, unsigned **pair)
+{
+    static std::atomic<unsigned> next_eager{0}, next_captured{0};
+    unsigned *eager = nullptr, *captured = nullptr;
+    if (!counter_arrays(&eager, &captured)) return false;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return false;
+    if (cs == cudaStreamCaptureStatusActive) {
+        const unsigned i = next_captured.fetch_add(1u);
+        *pair = i < (unsigned)CAPTURE_SLOTS ? captured + 2 * i : nullptr;
+        return true;
+    }
+    *pair = eager + 2 * (next_eager.fetch_add(1u) % PREFILL_SLOTS);
+    return true;
 }
 
 // ---- host: tensor maps ---------------------------------------------------------
@@ -769,8 +808,7 @@ cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
         }
         const long long tiles_upper = (long long)P.num_seqs * ((a.max_seqlen + 2 * BM - 1) / (2 * BM)) * a.num_heads;
         const int grid = (int)std::max<long long>(1, std::min<long long>(sms, tiles_upper));
-        P.items = next_item_counters();
-        if (!P.items) return cudaErrorInvalidDevice;
+        if (!next_item_counters(stream, &P.items)) return cudaErrorInvalidDevice;
         kern<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mo, P);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -202,6 +202,76 @@ def test_decode_ignores_padding_and_evicted_blocks(cuda_lib):
     assert int(g.status.item()) == 0
 
 
+def _poison_rows_outside_window(case, kc, vc):
+    """Fill every cache row of a sequence's visible blocks that lies outside
+    [start, ctx) -- the tail of the last block past the context, the head of
+    the first visible block before the window -- with NaN, +Inf and -Inf in
+    turn.  Each block belongs to one sequence, so no other key is touched."""
+    import torch
+    bs = case.block_size
+    vals = (float("nan"), float("inf"), float("-inf"))
+    n = 0
+    for s, c in enumerate(case.context_lens.tolist()):
+        if c == 0:
+            continue
+        start = max(0, c - case.window) if case.window > 0 else 0
+        rows = [j for j in range(start // bs * bs, start)] + [j for j in range(c, (c - 1) // bs * bs + bs)]
+        for j in rows:
+            b = int(case.block_tables[s, j // bs])
+            kc[b, :, j % bs] = vals[n % 3]
+            vc[b, :, j % bs] = vals[(n + 1) % 3]
+            n += 1
+    torch.cuda.synchronize()
+    return n
+
+
+@pytest.mark.parametrize("dtype", [F32, F16, BF16])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("window", [-1, 20])
+def test_decode_stale_cache_rows_contribute_nothing(cuda_lib, dtype, D, window):
+    """A serving engine's newest block is only partly written, and a window's
+    first block holds keys the window drops: cache rows outside [start, ctx)
+    may hold any bits.  With those rows NaN / +Inf / -Inf the output is
+    bit-identical to the clean cache's, and matches the oracle (which never
+    reads them)."""
+    case = synth.make_decode_case("stale", 300 + D + window, dtype, len(EDGE_CTX), 3, D,
+                                  context_lens=np.array(EDGE_CTX), pool_blocks=120, bias="gauss",
+                                  bias_stride=1003, window=window, scale=0.17)
+    g = GpuDecode(case, cuda_lib)
+    clean = to_host_storage(g.run(), dtype).copy()
+    assert _poison_rows_outside_window(case, g.k_cache, g.v_cache) > 0
+    got = g.run()
+    assert to_host_storage(got, dtype).tobytes() == clean.tobytes()
+    _check(to_f64(got, dtype), oracle_decode(case), dtype, "stale rows")
+    assert int(g.status.item()) == 0
+
+
+@pytest.mark.parametrize("dtype,D", [(BF16, 64), (F16, 128), (F32, 64)])
+def test_decode_stale_rows_with_fused_append(cuda_lib, dtype, D):
+    """The fused append writes the newest row into a block whose later rows
+    hold NaN / Inf: outputs and cache bytes equal scatter + decode on the
+    clean cache, bit for bit."""
+    import torch
+    case = synth.make_decode_case("stale-app", 320 + D, dtype, len(EDGE_CTX), 3, D,
+                                  context_lens=np.array(EDGE_CTX), pool_blocks=160, window=40, bias="gauss",
+                                  scale=0.2)
+    g = GpuDecode(case, cuda_lib)
+    ref_out = g.run().clone()
+    kc, vc, k_new, v_new = _append_state(case, cuda_lib)
+    _poison_rows_outside_window(case, kc, vc)
+    kref, vref = g.k_cache.clone(), g.v_cache.clone()
+    _poison_rows_outside_window(case, kref, vref)
+    out = torch.empty_like(ref_out)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cuda_lib.paged_attn_decode_multi([dict(g.problem("bias"), out=out, k_cache=kc, v_cache=vc, key_new=k_new,
+                                           value_new=v_new)], status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(out.view(torch.uint8), ref_out.view(torch.uint8))
+    assert torch.equal(kc.view(torch.uint8), kref.view(torch.uint8))
+    assert torch.equal(vc.view(torch.uint8), vref.view(torch.uint8))
+
+
 def test_decode_block_permutation_is_bitwise_invariant(cuda_lib):
     import torch
     case = synth.decode_workload(2)

@@ -54,18 +54,75 @@ def _sample_rows(case, rng, per_seq=48):
     return np.array(rows, dtype=np.int64)
 
 
-@pytest.mark.parametrize("layer", [0, 1])
-def test_prefill_encoder_workload_sampled(cuda_lib, layer):
+def test_prefill_encoder_workload_sampled(cuda_lib):
     """The encoder workload (32 sequences, lengths U[128, 8192], 12 heads,
-    head_dim 64) at full size: layer 0 is full attention, layer 1 window 64;
-    the oracle checks every sequence's first/last rows, the rows at the
-    128-row tile edge and a seeded random sample."""
+    head_dim 64) at full size, full-attention layer 0: the oracle checks every
+    sequence's first/last rows, the rows at the 128-row tile edge and a
+    seeded random sample."""
+    case = synth.prefill_workload(0, device="cuda")
+    got = run_gpu_prefill(cuda_lib, case)
+    q, k, v = (to_host_storage(t, BF16) for t in case.device_qkv)
+    rows = _sample_rows(case, np.random.default_rng(400), per_seq=48)
+    ref = oracle.prefill(q, k, v, case.cu_seqlens, case.window, case.causal, case.scale, BF16, rows=rows)
+    _check(to_f64(got[rows], BF16), ref, "encoder layer 0")
+
+
+@pytest.mark.parametrize("layer", [1, 2])
+def test_prefill_encoder_window_layers_every_row(cuda_lib, layer):
+    """The encoder workload's two window-64 layers at full size, every row
+    (each row keeps at most 127 keys, so the oracle covers all of them)."""
     case = synth.prefill_workload(layer, device="cuda")
     got = run_gpu_prefill(cuda_lib, case)
     q, k, v = (to_host_storage(t, BF16) for t in case.device_qkv)
-    rows = _sample_rows(case, np.random.default_rng(400 + layer), per_seq=48 if layer == 0 else 400)
-    ref = oracle.prefill(q, k, v, case.cu_seqlens, case.window, case.causal, case.scale, BF16, rows=rows)
-    _check(to_f64(got[rows], BF16), ref, f"encoder layer {layer}")
+    ref = oracle.prefill(q, k, v, case.cu_seqlens, case.window, case.causal, case.scale, BF16)
+    _check(to_f64(got, BF16), ref, f"encoder layer {layer}")
+
+
+def test_prefill_captured_and_eager_launches(cuda_lib):
+    """Launches captured into CUDA graphs keep item counters no other launch
+    is given: replays of two captured graphs on one stream, while more eager
+    launches than the eager counter ring holds run on another, all give the
+    eager result bit for bit.  A graph holding more captured launches than
+    there are reserved counter pairs ends with launches that deal their items
+    statically; those give the same bits too."""
+    import torch
+    lens = [300] * 40                                  # 2 items per (sequence, head): more items than CTAs
+    case = synth.make_prefill_case("capture", 610, lens, 4, 64, 64, 0, BF16, scale=1 / 8)
+    q, k, v = (to_dev(a, BF16) for a in (case.q, case.k, case.v))
+    cu = torch.from_numpy(case.cu_seqlens).cuda()
+    ref = torch.empty_like(q)
+    cuda_lib.swa_prefill(ref, q, k, v, cu, case.max_seqlen, case.window, case.causal, case.scale)
+    torch.cuda.synchronize()
+
+    def capture(out, n):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(n):
+                    cuda_lib.swa_prefill(out, q, k, v, cu, case.max_seqlen, case.window, case.causal, case.scale)
+        torch.cuda.current_stream().wait_stream(s)
+        return g
+
+    outs = [torch.zeros_like(q) for _ in range(3)]
+    g1, g2 = capture(outs[0], 1), capture(outs[1], 1)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(1100):
+            cuda_lib.swa_prefill(outs[2], q, k, v, cu, case.max_seqlen, case.window, case.causal, case.scale)
+    for _ in range(20):
+        g1.replay()
+        g2.replay()
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
+    big = torch.zeros_like(q)
+    g3 = capture(big, 8192 + 8)                        # at least the last 8 launches find no reserved pair
+    g3.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(big.view(torch.int16), ref.view(torch.int16))
 
 
 # ---------------------------------------------------------------------------

@@ -5,9 +5,11 @@ the device).  It takes no workspace and uses one fixed scratch array inside
 the library instead.
 
 The GPU test calls it through the C ABI twice in a row and checks each result
-against pka_paged_attn_decode given its own workspace, within the tolerance
-the other decode tests use.  This file is named to be collected last, so a
-run that stops at the first failure has run every other test before it."""
+against pka_paged_attn_decode given its own workspace: the same kernel runs
+with the same split of the work, so the outputs must be identical bit for
+bit (and so within the tolerance the other decode tests use).  This file is
+named to be collected last, so a run that stops at the first failure has run
+every other test before it."""
 import ctypes
 
 import numpy as np
@@ -54,7 +56,8 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls(cuda_lib):
         assert need <= NOALLOC_SCRATCH_BYTES
         g = GpuDecode(case, cuda_lib)
         ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
-        ref = to_f64(g.run(workspace=ws), case.dtype).copy()
+        ref_t = g.run(workspace=ws).clone()
+        ref = to_f64(ref_t, case.dtype)
         for call in range(2):
             out = torch.full_like(g.out, float("nan"))
             assert _call_noalloc(lib, g, out) == cuda_lib.PKA_OK
@@ -63,6 +66,7 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls(cuda_lib):
             assert np.isfinite(got).all(), f"workload {n} call {call}"
             err = max_err(got, ref)
             assert err <= TOL[case.dtype], f"workload {n} call {call}: max abs diff {err:.3g}"
+            assert torch.equal(out.view(torch.uint8), ref_t.view(torch.uint8)), f"workload {n} call {call}"
         assert int(g.status.item()) == 0
 
 
