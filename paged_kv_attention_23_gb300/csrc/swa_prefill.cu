@@ -76,7 +76,8 @@ constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NS, B_SF = 2 + 2 * NS, 
               B_OF = B_PF + 2, B_OE = B_OF + 2, B_EW = B_OE + 2, B_ER = B_EW + 2, B_IF = B_ER + 2, B_IE = B_IF + 2,
               NBAR = B_IE + 2;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, abort flag, item ring [2]
-constexpr uint32_t OFF_SCHED = (OFF_MISC + 16 + 127) / 128 * 128;
+constexpr uint32_t OFF_RING = (OFF_MISC + 16 + 127) / 128 * 128;   // the two ring entries' items (64 B each)
+constexpr uint32_t OFF_SCHED = OFF_RING + 128;
 constexpr uint32_t SMEM_BYTES = OFF_SCHED + (6 * MAX_SEQS + 1) * 4 + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 227u * 1024u, "dynamic shared memory per CTA");
 constexpr int CBS = 16;                   // paged cache block: 16 key rows of one head
@@ -110,10 +111,12 @@ struct Params {
 // Query tile w multiplies key tiles jb[w] .. je[w] (empty when jb > je).
 // Query row r sits at key position r + qoff (qoff = Lk - L: the queries are
 // the sequence's last L positions); keys at k_end and beyond are not needed.
-struct Item {
+struct alignas(16) Item {
     int s0, L, Lk, qoff, seq, h, r0, c_lo, nkv, k_end;
     int jb[2], je[2];
+    int pad[2];
 };
+static_assert(sizeof(Item) == 64, "an item is four 16-byte words in the ring");
 
 struct Sched {
     const int *cum, *start, *len, *lenk, *seqid;
@@ -337,6 +340,25 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     // thread hands each id to the MMA threads and softmax warps through a
     // two-entry ring in shared memory; an id >= total_items ends the CTA's work.
     volatile int *item_ring = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);
+    // the producer also writes each published item's description (the roles
+    // then skip the schedule search): ring entry e's item at OFF_RING + 64 e
+    auto put_item = [&](uint32_t slot, const Item &it) {
+        int4 *dst = reinterpret_cast<int4 *>(smem + OFF_RING + slot * sizeof(Item));
+        dst[0] = make_int4(it.s0, it.L, it.Lk, it.qoff);
+        dst[1] = make_int4(it.seq, it.h, it.r0, it.c_lo);
+        dst[2] = make_int4(it.nkv, it.k_end, it.jb[0], it.jb[1]);
+        dst[3] = make_int4(it.je[0], it.je[1], 0, 0);
+    };
+    auto get_item = [&](uint32_t slot) {
+        const int4 *src = reinterpret_cast<const int4 *>(smem + OFF_RING + slot * sizeof(Item));
+        const int4 a = src[0], b = src[1], c = src[2], d = src[3];
+        Item it;
+        it.s0 = a.x; it.L = a.y; it.Lk = a.z; it.qoff = a.w;
+        it.seq = b.x; it.h = b.y; it.r0 = b.z; it.c_lo = b.w;
+        it.nkv = c.x; it.k_end = c.y; it.jb[0] = c.z; it.jb[1] = c.w;
+        it.je[0] = d.x; it.je[1] = d.y;
+        return it;
+    };
     const bool dyn = !PAGED && P.items != nullptr && total_items > (int)gridDim.x;
 
     if (warp == 0 && lane == 0) {
@@ -346,11 +368,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         tc::prefetch_tensormap(&tm_v);
         tc::prefetch_tensormap(&tm_o);
         uint32_t g = 0, wq = 0, ik = 0;
-        auto publish = [&](int id) -> bool {
+        auto publish = [&](int id, const Item &it) -> bool {
             if constexpr (PAGED) return true;          // the paged instance's roles follow the static deal
             const uint32_t slot = ik & 1;
             if (!wait_or_abort(BAR(B_IE + slot), ((ik >> 1) & 1) ^ 1, abort_flag, P.status)) return false;
             item_ring[slot] = id;
+            if (id < total_items) put_item(slot, it);
             mbar_arrive(BAR(B_IF + slot));
             ++ik;
             return true;
@@ -359,8 +382,9 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         unsigned ahead = 0;                                // the counter's answer for the item after t
         if (dyn && t < total_items) ahead = atomicAdd(P.items, 1u);
         for (;; ++wq) {
-            if (!publish(t) || t >= total_items || *abort_flag) break;
-            const Item I = sched.get(t);
+            Item I;
+            if (t < total_items) I = sched.get(t);
+            if (!publish(t, I) || t >= total_items || *abort_flag) break;
             t = dyn ? (int)gridDim.x + (int)ahead : t + (int)gridDim.x;
             if (dyn && t < total_items) ahead = atomicAdd(P.items, 1u);
             if (!wait_or_abort(BAR(B_QE), (wq & 1) ^ 1, abort_flag, P.status)) break;
@@ -428,10 +452,11 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             } else {
                 if (!wait_or_abort(BAR(B_IF + (wq & 1)), (wq >> 1) & 1, abort_flag, P.status)) break;
                 t = item_ring[wq & 1];
-                mbar_arrive(BAR(B_IE + (wq & 1)));
             }
+            Item I;
+            if (t < total_items) I = PAGED ? sched.get(t) : get_item(wq & 1);
+            if constexpr (!PAGED) mbar_arrive(BAR(B_IE + (wq & 1)));
             if (t >= total_items || *abort_flag) break;
-            const Item I = sched.get(t);
             if (!wait_or_abort(BAR(B_QF), wq & 1, abort_flag, P.status)) break;
             const bool mine = I.jb[w] <= I.je[w];
             if (!mine) mbar_arrive(BAR(B_QE));
@@ -498,11 +523,14 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             } else {
                 if (!wait_or_abort(BAR(B_IF + (kq & 1)), (kq >> 1) & 1, abort_flag, P.status)) break;
                 t = item_ring[kq & 1];
+            }
+            Item I;
+            if (t < total_items) I = PAGED ? sched.get(t) : get_item(kq & 1);
+            if constexpr (!PAGED) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(B_IE + (kq & 1)));
             }
             if (t >= total_items || *abort_flag) break;
-            const Item I = sched.get(t);
             const uint32_t g_item = g;                 // K/V stages of this item start at g_item
             g += I.nkv;
             const int rr = I.r0 + w * BM + row;        // query row within its sequence
@@ -566,8 +594,16 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 const int ilo = lo - c0, ihi = hi - c0;
                 const bool masked = ilo > 0 || ihi < BN;
                 if (masked) {
+                    uint32_t mw[4];
 #pragma unroll
-                    for (int i = 0; i < BN; ++i) x[i] = (i >= ilo && i < ihi) ? x[i] : -INFINITY;
+                    for (int k = 0; k < 4; ++k) {
+                        const int a = min(max(ilo - 32 * k, 0), 32), b = min(max(ihi - 32 * k, 0), 32);
+                        const uint32_t hiw = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+                        const uint32_t low = a >= 32 ? 0xffffffffu : ((1u << a) - 1u);
+                        mw[k] = hiw & ~low;
+                    }
+#pragma unroll
+                    for (int i = 0; i < BN; ++i) x[i] = (mw[i >> 5] & (1u << (i & 31))) ? x[i] : -INFINITY;
                 }
                 float mx[4];
 #pragma unroll
