@@ -16,7 +16,10 @@
 // Model support": T5's custom attention bias; prefill kernels that read
 // cross-attention keys through their block table):
 //   BIAS   adds rel[h, cap + clamp(d, -cap, cap)] to q.k before the scale,
-//          d = query position - key position (the T5 relative-position bias).
+//          d = query position - key position (the T5 relative-position bias);
+//          every head's table, widened by a key tile's span with its clamped
+//          end values, is copied to shared memory when it fits, so a score's
+//          bias is one shared load at a constant offset.
 //   PAGED  reads K/V from the paged cache [num_blocks, H, 16, 64] through the
 //          block table, for each sequence's last Lq queries: query row r sits
 //          at key position ctx - Lq + r, and the masks and the bias use it.
@@ -36,7 +39,7 @@
 //   warps 2..5  softmax of query tile 0, warps 6..9 of query tile 1 (the two
 //               groups ping-pong on the tensor core): one thread per row
 //               loads its S row, frees the S columns at once, masks, takes
-//               the max (3-input max), and writes P = 2^(scale*s - m) as bf16
+//               the max (two-input max chains), and writes P = 2^(scale*s - m) as bf16
 //               pairs into the tile's P columns of TMEM (tcgen05.st); the
 //               scale is folded into the exponent's FMA.  O stays in TMEM: the running max is raised
 //               only when a row's max grows by more than 2^8, and only then
@@ -311,6 +314,22 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         seqid[rk] = s;
         if (PAGED) lenk[rk] = min(max(P.context_lens[s], 0), P.mbps * CBS);
     }
+    // The bias instances store outputs without the staging tiles; that space
+    // holds every head's relative-position table instead, widened to the
+    // distances a key tile in the band can present (|d| < cap + BN) with the
+    // clamped values, so a score's bias is one shared load at a constant
+    // offset: no clamp, no global load.  Tables too large for it stay in
+    // global memory (read through the clamp, as before).
+    const int bias_cap = BIAS ? P.num_buckets - 1 : 0;
+    const int tab_span = 2 * (bias_cap + BN) - 1;
+    const bool tab_sm = BIAS && (long long)P.H * tab_span <= (long long)(2 * TILE_BYTES / 4);
+    float *tab = reinterpret_cast<float *>(smem + OFF_OST);
+    if (tab_sm) {
+        for (int i = threadIdx.x; i < P.H * tab_span; i += NTHREADS) {
+            const int h = i / tab_span, d = i - h * tab_span - (bias_cap + BN - 1);
+            tab[i] = __ldg(P.rel_bias + (size_t)h * (2 * bias_cap + 1) + bias_cap + min(max(d, -bias_cap), bias_cap));
+        }
+    }
     __syncthreads();
     if (warp == 0) {
         const int per = (S + 31) / 32;
@@ -369,7 +388,6 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         tc::prefetch_tensormap(&tm_o);
         uint32_t g = 0, wq = 0, ik = 0;
         auto publish = [&](int id, const Item &it) -> bool {
-            if constexpr (PAGED) return true;          // the paged instance's roles follow the static deal
             const uint32_t slot = ik & 1;
             if (!wait_or_abort(BAR(B_IE + slot), ((ik >> 1) & 1) ^ 1, abort_flag, P.status)) return false;
             item_ring[slot] = id;
@@ -446,16 +464,11 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const int w = warp == 1 ? 0 : 1;
         uint32_t g = 0, wq = 0, cs = 0, co = 0;
         for (;; ++wq) {
-            int t;
-            if constexpr (PAGED) {
-                t = (int)blockIdx.x + (int)wq * (int)gridDim.x;
-            } else {
-                if (!wait_or_abort(BAR(B_IF + (wq & 1)), (wq >> 1) & 1, abort_flag, P.status)) break;
-                t = item_ring[wq & 1];
-            }
+            if (!wait_or_abort(BAR(B_IF + (wq & 1)), (wq >> 1) & 1, abort_flag, P.status)) break;
+            const int t = item_ring[wq & 1];
             Item I;
-            if (t < total_items) I = PAGED ? sched.get(t) : get_item(wq & 1);
-            if constexpr (!PAGED) mbar_arrive(BAR(B_IE + (wq & 1)));
+            if (t < total_items) I = get_item(wq & 1);
+            mbar_arrive(BAR(B_IE + (wq & 1)));
             if (t >= total_items || *abort_flag) break;
             if (!wait_or_abort(BAR(B_QF), wq & 1, abort_flag, P.status)) break;
             const bool mine = I.jb[w] <= I.je[w];
@@ -517,19 +530,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const uint32_t tP = tmem + lane_addr + COL_P + w * (BN / 2);
         uint32_t cs = 0, co = 0, g = 0, ep = 0;
         for (uint32_t kq = 0;; ++kq) {
-            int t;
-            if constexpr (PAGED) {
-                t = (int)blockIdx.x + (int)kq * (int)gridDim.x;
-            } else {
-                if (!wait_or_abort(BAR(B_IF + (kq & 1)), (kq >> 1) & 1, abort_flag, P.status)) break;
-                t = item_ring[kq & 1];
-            }
+            if (!wait_or_abort(BAR(B_IF + (kq & 1)), (kq >> 1) & 1, abort_flag, P.status)) break;
+            const int t = item_ring[kq & 1];
             Item I;
-            if (t < total_items) I = PAGED ? sched.get(t) : get_item(kq & 1);
-            if constexpr (!PAGED) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(B_IE + (kq & 1)));
-            }
+            if (t < total_items) I = get_item(kq & 1);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_IE + (kq & 1)));
             if (t >= total_items || *abort_flag) break;
             const uint32_t g_item = g;                 // K/V stages of this item start at g_item
             g += I.nkv;
@@ -549,10 +555,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             else if (P.window > 0) { lo = max(lo, pos - P.window + 1); hi = min(hi, pos + P.window); }
             if (P.causal) hi = min(hi, pos + 1);
             const float *rel = nullptr;                // rel[d]: bias of a key d positions before the row
+            const float *trel = nullptr;               // the same, widened, in shared memory (tab_sm)
             int cap = 0;
             if constexpr (BIAS) {
                 cap = P.num_buckets - 1;
                 rel = P.rel_bias + (size_t)I.h * (2 * cap + 1) + cap;
+                trel = tab + I.h * tab_span + (cap + BN - 1);
             }
             float m = -INFINITY, l = 0.f;
             bool ok = true;
@@ -584,7 +592,11 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     const int dhi = pos - c0, dlo = dhi - (BN - 1);
                     if (dlo >= cap) boff = __ldg(rel + cap);
                     else if (dhi <= -cap) boff = __ldg(rel - cap);
-                    else {
+                    else if (tab_sm) {
+                        const float *tr = trel + dhi;      // |dhi - i| < cap + BN in the band
+#pragma unroll
+                        for (int i = 0; i < BN; ++i) x[i] += tr[-i];
+                    } else {
 #pragma unroll
                         for (int i = 0; i < BN; ++i) x[i] += __ldg(rel + min(max(dhi - i, -cap), cap));
                     }
@@ -608,10 +620,10 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 float mx[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    float a = x[k * 32];
+                    float a0 = x[k * 32], a1 = x[k * 32 + 1];
 #pragma unroll
-                    for (int i = 1; i < 32; i += 2) a = tc::max3(a, x[k * 32 + i], x[k * 32 + i + 1]);
-                    mx[k] = fmaxf(a, x[k * 32 + 31]);
+                    for (int i = 2; i < 32; i += 2) { a0 = fmaxf(a0, x[k * 32 + i]); a1 = fmaxf(a1, x[k * 32 + i + 1]); }
+                    mx[k] = fmaxf(a0, a1);
                 }
                 const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * P.scale_log2 + boff;
                 // raise the running max only when it grows by more than 2^8

@@ -205,6 +205,20 @@ def test_biased_prefill_small_parity(cuda_lib, window, causal, buckets):
     _check(got, ref, f"biased W={window} causal={causal} B={buckets}")
 
 
+@pytest.mark.parametrize("causal", [0, 1])
+def test_biased_prefill_table_larger_than_shared_memory(cuda_lib, causal):
+    """A relative-position table too wide for the kernel's shared-memory copy
+    (4 heads x 1100 buckets) is read from global memory through the clamp;
+    sequences longer than the cap reach the saturated columns on both sides."""
+    lens = [1, 300, 1300, 2600]
+    case = synth.make_prefill_case("biased-wide", 330 + causal, lens, 4, 64, -1, causal, BF16, scale=1 / 8)
+    case.rel_bias = synth.rel_bias_table(1100, 4, 1100) * np.float32(2.0)
+    got = to_f64(run_gpu_biased(cuda_lib, case), BF16)
+    ref = oracle.prefill_biased(case.q, case.k, case.v, case.cu_seqlens, -1, causal, case.scale, BF16,
+                                case.rel_bias)
+    _check(got, ref, f"biased wide table causal={causal}")
+
+
 def test_biased_prefill_t5_encoder_workload_sampled(cuda_lib):
     """The T5-large-shaped encoder (256 x 512 tokens, 16 heads, bias table
     [16, 257]) at full size, checked on sampled rows."""
