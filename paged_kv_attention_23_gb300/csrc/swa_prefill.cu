@@ -283,6 +283,10 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         if (PAGED) {
             const int c = P.context_lens[s];
             if (c < 0 || c > P.mbps * CBS) flag_status(P.status, PKA_DEVCHK_CONTEXT_LEN);
+            // paged: order by the work of the sequence, query tiles x key tiles
+            const unsigned qt = (unsigned)min((b - a + BM - 1) / BM, 65535);
+            const unsigned kt = (unsigned)min((min(max(c, 0), P.mbps * CBS) + BN - 1) / BN, 65535);
+            rank_tmp[s] = (int)min(qt * kt * 65536u + (unsigned)min(b - a, 65535), 0x7fffffffu);
         }
     }
     if (threadIdx.x == 0) {
@@ -310,7 +314,9 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         }
         const int a = P.cu_seqlens[s];
         start[rk] = a < 0 ? 0 : a;
-        len[rk] = Ls;
+        len[rk] = PAGED ? (a < 0 || P.cu_seqlens[s + 1] < a || P.cu_seqlens[s + 1] > P.num_tokens ? 0
+                                                                                                 : P.cu_seqlens[s + 1] - a)
+                        : Ls;
         seqid[rk] = s;
         if (PAGED) lenk[rk] = min(max(P.context_lens[s], 0), P.mbps * CBS);
     }
@@ -378,7 +384,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         it.je[0] = d.x; it.je[1] = d.y;
         return it;
     };
-    const bool dyn = !PAGED && P.items != nullptr && total_items > (int)gridDim.x;
+    const bool dyn = P.items != nullptr && total_items > (int)gridDim.x;
 
     if (warp == 0 && lane == 0) {
         // ======================= TMA producer =======================
