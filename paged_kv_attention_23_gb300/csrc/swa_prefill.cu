@@ -356,14 +356,15 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     const Sched sched{cum, start, len, lenk, seqid, S, P.H, P.window, P.causal, P.chunk, PAGED};
     const int total_items = cum[S];
     const uint32_t tmem = *tmem_base_sm;
-    // Items: CTA c takes item c, then (packed keys) items from a global
-    // counter one at a time: CTAs that finish early take more, where a static
-    // deal left the last CTA 5-20 % behind the average (full layer 1.97 ->
-    // 1.92 ms, chunked layer 0.41 -> 0.37 ms).  The paged instance keeps the
-    // static deal c, c + G, c + 2G, ... (15 % faster there), as does a launch
-    // given no counter pair (P.items == NULL).  The producer
-    // thread hands each id to the MMA threads and softmax warps through a
-    // two-entry ring in shared memory; an id >= total_items ends the CTA's work.
+    // Items: CTA c takes item c, then items from a global counter one at a
+    // time: CTAs that finish early take more, where a static deal left the
+    // last CTA 5-20 % behind the average (full layer 1.97 -> 1.92 ms, chunked
+    // layer 0.41 -> 0.37 ms).  A launch given no counter pair (P.items == NULL)
+    // deals statically: c, c + G, c + 2G, ...  The producer thread hands each
+    // id and its item's description to the MMA threads and softmax warps
+    // through a two-entry ring in shared memory; an id >= total_items ends the
+    // CTA's work.  Sequences are ordered longest first (paged: by query tiles
+    // x key tiles, an estimate of their work).
     volatile int *item_ring = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);
     // the producer also writes each published item's description (the roles
     // then skip the schedule search): ring entry e's item at OFF_RING + 64 e
