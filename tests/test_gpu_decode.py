@@ -586,3 +586,34 @@ def test_multi_materialised_bias_then_table(cuda_lib):
     cuda_lib.paged_attn_decode_multi([ga.problem("bias"), gb.problem("t5")])
     _check(to_f64(ga.out, BF16), oracle_decode(a), BF16, "materialised problem 0")
     _check(to_f64(gb.out, BF16), oracle_decode_t5(b), BF16, "table problem 1")
+
+
+# ---------------------------------------------------------------------------
+# the small-batch kernel (at most one (sequence, head) pair per SM) and the
+# persistent kernel take the same problems
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype,D", [(BF16, 64), (F16, 128), (F32, 64), (F32, 128)])
+@pytest.mark.parametrize("num_seqs", [9, 400])
+def test_decode_small_and_large_batches_two_problems(cuda_lib, dtype, D, num_seqs):
+    """A decode step of two problems -- self-attention with a materialised
+    bias, a window and the fused append; cross-attention with the T5 table --
+    at 9 sequences (the small-batch kernel: 72 pairs) and at 400 (the
+    persistent kernel), each against the oracle; contexts reach 2047 keys."""
+    import torch
+    rng = np.random.default_rng(700 + D + num_seqs)
+    ctx_a = rng.integers(0, 2048, size=num_seqs)
+    ctx_a[:3] = [0, 1, 2047]
+    a = synth.make_decode_case("two-a", 701 + D, dtype, num_seqs, 4, D, context_lens=ctx_a, bias="gauss",
+                               bias_stride=2048, window=300, scale=0.15)
+    b = synth.make_decode_case("two-b", 702 + D, dtype, num_seqs, 4, D, ctx_range=(1, 700), scale=0.1)
+    b.bias_table = np.random.default_rng(703).standard_normal((4, 40)).astype(np.float32)
+    ga, gb = GpuDecode(a, cuda_lib), GpuDecode(b, cuda_lib)
+    kc, vc, k_new, v_new = _append_state(a, cuda_lib)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cuda_lib.paged_attn_decode_multi([dict(ga.problem("bias"), k_cache=kc, v_cache=vc, key_new=k_new,
+                                           value_new=v_new), gb.problem("t5")], status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _check(to_f64(ga.out, dtype), oracle_decode(a), dtype, f"self {num_seqs}")
+    _check(to_f64(gb.out, dtype), oracle_decode_t5(b), dtype, f"cross {num_seqs}")
+    assert torch.equal(kc.view(torch.uint8), ga.k_cache.view(torch.uint8))
