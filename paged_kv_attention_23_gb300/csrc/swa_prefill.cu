@@ -123,6 +123,24 @@ struct alignas(16) Item {
 };
 static_assert(sizeof(Item) == 64, "an item is four 16-byte words in the ring");
 
+// An item's description read in place from its ring entry (the layout that
+// the producer writes: s0, L, Lk, qoff | seq, h, r0, c_lo | nkv, k_end, jb[2] | je[2]).
+struct RingItem {
+    const volatile int *p;
+    __device__ __forceinline__ int s0() const { return p[0]; }
+    __device__ __forceinline__ int L() const { return p[1]; }
+    __device__ __forceinline__ int Lk() const { return p[2]; }
+    __device__ __forceinline__ int qoff() const { return p[3]; }
+    __device__ __forceinline__ int seq() const { return p[4]; }
+    __device__ __forceinline__ int h() const { return p[5]; }
+    __device__ __forceinline__ int r0() const { return p[6]; }
+    __device__ __forceinline__ int c_lo() const { return p[7]; }
+    __device__ __forceinline__ int nkv() const { return p[8]; }
+    __device__ __forceinline__ int k_end() const { return p[9]; }
+    __device__ __forceinline__ int jb(int w) const { return p[10 + w]; }
+    __device__ __forceinline__ int je(int w) const { return p[12 + w]; }
+};
+
 struct Sched {
     const int *cum, *start, *len, *lenk, *seqid;
     int nseq, H, window, causal, chunk;
@@ -550,25 +568,30 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         for (uint32_t kq = 0;; ++kq) {
             if (!wait_or_abort(BAR(B_IF + (kq & 1)), (kq >> 1) & 1, abort_flag, P.status)) break;
             const int t = item_ring[kq & 1];
-            Item I;
-            if (t < total_items) I = get_item(kq & 1);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_IE + (kq & 1)));
-            if (t >= total_items || *abort_flag) break;
+            // the item's description stays in its ring entry, read from shared
+            // memory where used (fewer live registers); the entry is released
+            // once the item is done
+            const RingItem I{reinterpret_cast<const volatile int *>(smem + OFF_RING + (kq & 1) * sizeof(Item))};
+            auto release_item = [&]() {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_IE + (kq & 1)));
+            };
+            if (t >= total_items || *abort_flag) { release_item(); break; }
             const uint32_t g_item = g;                 // K/V stages of this item start at g_item
-            g += I.nkv;
-            const int rr = I.r0 + w * BM + row;        // query row within its sequence
-            if (I.jb[w] > I.je[w]) {
+            g += I.nkv();
+            const int rr = I.r0() + w * BM + row;        // query row within its sequence
+            if (I.jb(w) > I.je(w)) {
                 // past the sequence, or (paged) no key for any row of the tile: zero rows
-                if (PAGED && rr < I.L) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) + ((size_t)(I.s0 + rr) * P.H + I.h) * HD);
+                if (PAGED && rr < I.L()) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) + ((size_t)(I.s0() + rr) * P.H + I.h()) * HD);
 #pragma unroll
                     for (int c = 0; c < HD / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
                 }
+                release_item();
                 continue;
             }
-            const int pos = rr + I.qoff;               // the row's key position
-            int lo = 0, hi = I.Lk;                     // keys [lo, hi) kept for this row
+            const int pos = rr + I.qoff();               // the row's key position
+            int lo = 0, hi = I.Lk();                     // keys [lo, hi) kept for this row
             if (P.chunk > 0) { lo = pos / P.chunk * P.chunk; hi = min(hi, lo + P.chunk); }
             else if (P.window > 0) { lo = max(lo, pos - P.window + 1); hi = min(hi, pos + P.window); }
             if (P.causal) hi = min(hi, pos + 1);
@@ -577,12 +600,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             int cap = 0;
             if constexpr (BIAS) {
                 cap = P.num_buckets - 1;
-                rel = P.rel_bias + (size_t)I.h * (2 * cap + 1) + cap;
-                trel = tab + I.h * tab_span + (cap + BN - 1);
+                rel = P.rel_bias + (size_t)I.h() * (2 * cap + 1) + cap;
+                trel = tab + I.h() * tab_span + (cap + BN - 1);
             }
             float m = -INFINITY, l = 0.f;
             bool ok = true;
-            for (int j = I.jb[w]; j <= I.je[w]; ++j, ++cs) {
+            for (int j = I.jb(w); j <= I.je(w); ++j, ++cs) {
                 if (!wait_or_abort(BAR(B_SF + w), cs & 1, abort_flag, P.status)) { ok = false; break; }
                 tc::fence_after_sync();
                 float x[BN];
@@ -590,12 +613,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 tc::tmem_ld64(tS + 64, x + 64);
                 tc::fence_before_sync();
                 mbar_arrive(BAR(B_SE + w));            // S columns free: QK of the next key tile may start
-                const int c0 = I.c_lo + j * BN;
+                const int c0 = I.c_lo() + j * BN;
                 if constexpr (PAGED) {
                     // V rows at k_end and beyond hold unread blocks or cache rows
                     // past the context (any bits): zero them so that P = 0 there
                     // contributes exactly nothing to P V
-                    if (row >= I.k_end - c0) {
+                    if (row >= I.k_end() - c0) {
                         const uint32_t vrow = sb + OFF_KV + ((g_item + j) % NS) * 2 * TILE_BYTES + TILE_BYTES + row * 128;
 #pragma unroll
                         for (int c = 0; c < 8; ++c)
@@ -648,7 +671,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 const bool raise = mt > m + RESCALE_LOG2;
                 const float m_old = m;
                 if (raise) m = mt;
-                if (j > I.jb[w]) {
+                if (j > I.jb(w)) {
                     // P V of the previous key tile is done: P may be overwritten, O rescaled
                     if (!wait_or_abort(BAR(B_OF + w), (cs - 1) & 1, abort_flag, P.status)) { ok = false; break; }
                     tc::fence_after_sync();
@@ -657,7 +680,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 // P = 2^(scale * s - m) as bf16 into the swizzled buffer; row sum in f32
                 const float mneg = (m == -INFINITY ? 0.f : -m) + boff;
                 l += write_p_tmem<T>(x, P.scale_log2, mneg, tP);
-                if (j > I.jb[w] && __any_sync(kFull, raise)) {
+                if (j > I.jb(w) && __any_sync(kFull, raise)) {
                     // the running max rose: bring this row's O to the new max (in TMEM)
                     const float c = raise ? ex2(m_old - m) : 1.f;
                     float o[HD];
@@ -680,8 +703,8 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             mbar_arrive(BAR(B_OE + w));
             ++co;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int tile0 = I.r0 + w * BM;            // the tile's first row within its sequence
-            if (!BIAS && tile0 + BM <= I.L) {
+            const int tile0 = I.r0() + w * BM;            // the tile's first row within its sequence
+            if (!BIAS && tile0 + BM <= I.L()) {
                 // a whole tile: rows into the 128-byte-swizzled staging tile, then one
                 // TMA store, so the softmax threads issue no strided global stores
                 // (the bias instances keep plain stores: their per-key table loads
@@ -705,13 +728,13 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 mbar_arrive(BAR(B_ER + w));
                 if (row == 0) {
                     if (!wait_or_abort(BAR(B_ER + w), ep & 1, abort_flag, P.status)) break;
-                    tc::tma_store_3d(&tm_o, 0, I.h, I.s0 + tile0, sb + OFF_OST + w * TILE_BYTES);
+                    tc::tma_store_3d(&tm_o, 0, I.h(), I.s0() + tile0, sb + OFF_OST + w * TILE_BYTES);
                     tc::bulk_commit_group();
                 }
                 ++ep;
-            } else if (rr < I.L) {
+            } else if (rr < I.L()) {
                 // plain stores of the rows inside the sequence (its last, partial tile)
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) + ((size_t)(I.s0 + rr) * P.H + I.h) * HD);
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) + ((size_t)(I.s0() + rr) * P.H + I.h()) * HD);
 #pragma unroll
                 for (int c = 0; c < HD / 8; ++c) {
                     float v[8];
@@ -720,6 +743,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     dst[c] = Vec<T>::from_f32(v);
                 }
             }
+            release_item();
         }
         (void)co;
         if (!BIAS && row == 0) tc::bulk_wait_all();   // the staging tiles stay valid until the stores are done
