@@ -727,6 +727,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_small_kernel(const Param
 #pragma unroll
     for (int e = 0; e < R::EPC; ++e) acc[e] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
+    int consumed = 0;
     for (int k = 0; k < myn; ++k) {
         const int stage = k % NSTAGE;
         const unsigned char *stp = stages + stage * R::STAGE;
@@ -735,6 +736,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_small_kernel(const Param
             ok = false;
             break;
         }
+        consumed = k + 1;
         const int bi = b0 + warp + k * NW;
         if (append && bi == last) {
             const int r = (ctx - 1) % BS;
@@ -793,6 +795,12 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_small_kernel(const Param
         if (append && bi == last && lane < R::NC) fence_proxy_async();   // before a refill of this stage
         __syncwarp();
         if ((int)issued < myn) issue();
+    }
+    if (!ok) {
+        // a copy never landed: give the later stages in flight a bounded wait of
+        // their own before the CTA leaves (their shared memory must stay valid)
+        for (int k = consumed + 1; k < (int)issued; ++k)
+            if (!mbar_wait_bounded(smem_u32(&bars[k % NSTAGE]), (k / NSTAGE) & 1)) break;
     }
     // ---- the warp's partial state -> shared memory, merged by warp 0 --------------
     float l = l_run;

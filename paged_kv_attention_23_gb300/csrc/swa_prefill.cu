@@ -124,14 +124,14 @@ struct alignas(16) Item {
 static_assert(sizeof(Item) == 64, "an item is four 16-byte words in the ring");
 
 // An item's description read in place from its ring entry (the layout that
-// the producer writes: s0, L, Lk, qoff | seq, h, r0, c_lo | nkv, k_end, jb[2] | je[2]).
+// the producer writes: s0, L, Lk, qoff | seq, h, r0, c_lo | nkv, k_end, jb[2] | je[2];
+// the softmax warps never need seq).
 struct RingItem {
     const volatile int *p;
     __device__ __forceinline__ int s0() const { return p[0]; }
     __device__ __forceinline__ int L() const { return p[1]; }
     __device__ __forceinline__ int Lk() const { return p[2]; }
     __device__ __forceinline__ int qoff() const { return p[3]; }
-    __device__ __forceinline__ int seq() const { return p[4]; }
     __device__ __forceinline__ int h() const { return p[5]; }
     __device__ __forceinline__ int r0() const { return p[6]; }
     __device__ __forceinline__ int c_lo() const { return p[7]; }
