@@ -123,22 +123,36 @@ struct alignas(16) Item {
 };
 static_assert(sizeof(Item) == 64, "an item is four 16-byte words in the ring");
 
+// 32-bit words of shared memory by their shared-space address (a 32-bit
+// register instead of a 64-bit generic pointer), read and written volatile
+__device__ __forceinline__ int lds_volatile(uint32_t addr)
+{
+    int v;
+    asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts_volatile(uint32_t addr, int v)
+{
+    asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // An item's description read in place from its ring entry (the layout that
 // the producer writes: s0, L, Lk, qoff | seq, h, r0, c_lo | nkv, k_end, jb[2] | je[2];
 // the softmax warps never need seq).
 struct RingItem {
-    const volatile int *p;
-    __device__ __forceinline__ int s0() const { return p[0]; }
-    __device__ __forceinline__ int L() const { return p[1]; }
-    __device__ __forceinline__ int Lk() const { return p[2]; }
-    __device__ __forceinline__ int qoff() const { return p[3]; }
-    __device__ __forceinline__ int h() const { return p[5]; }
-    __device__ __forceinline__ int r0() const { return p[6]; }
-    __device__ __forceinline__ int c_lo() const { return p[7]; }
-    __device__ __forceinline__ int nkv() const { return p[8]; }
-    __device__ __forceinline__ int k_end() const { return p[9]; }
-    __device__ __forceinline__ int jb(int w) const { return p[10 + w]; }
-    __device__ __forceinline__ int je(int w) const { return p[12 + w]; }
+    uint32_t a;    // shared-space address of the entry
+    __device__ __forceinline__ int f(int i) const { return lds_volatile(a + 4u * i); }
+    __device__ __forceinline__ int s0() const { return f(0); }
+    __device__ __forceinline__ int L() const { return f(1); }
+    __device__ __forceinline__ int Lk() const { return f(2); }
+    __device__ __forceinline__ int qoff() const { return f(3); }
+    __device__ __forceinline__ int h() const { return f(5); }
+    __device__ __forceinline__ int r0() const { return f(6); }
+    __device__ __forceinline__ int c_lo() const { return f(7); }
+    __device__ __forceinline__ int nkv() const { return f(8); }
+    __device__ __forceinline__ int k_end() const { return f(9); }
+    __device__ __forceinline__ int jb(int w) const { return f(10 + w); }
+    __device__ __forceinline__ int je(int w) const { return f(12 + w); }
 };
 
 struct Sched {
@@ -248,16 +262,16 @@ __device__ __forceinline__ float write_p_tmem(const float *x, float scale_log2, 
     return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 
-// bounded wait that also gives up once another role has aborted
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                              int32_t *status)
+// bounded wait that also gives up once another role has aborted (the abort
+// flag is the shared word at abort_addr)
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint32_t abort_addr, int32_t *status)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (*abort_flag) return false;
+        if (lds_volatile(abort_addr)) return false;
         if (clock64() - t0 > (1ll << 31)) {
-            *abort_flag = 1;
+            sts_volatile(abort_addr, 1);
             flag_status(status, PKA_DEVCHK_TIMEOUT);
             return false;
         }
@@ -283,7 +297,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     const uint32_t bar0 = sb + OFF_BAR;
     auto BAR = [&](int i) { return bar0 + 8u * i; };
     uint32_t *tmem_base_sm = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+    const uint32_t abort_flag = sb + OFF_MISC + 4;    // shared word: a role gave up, all stop
     int *cum = reinterpret_cast<int *>(smem + OFF_SCHED);
     int *start = cum + MAX_SEQS + 1;
     int *len = start + MAX_SEQS;
@@ -318,7 +332,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             const bool by_item_readers = i >= B_IE && i < B_IE + 2;   // 2 MMA threads + 8 softmax warps
             mbar_init(BAR(i), by_softmax ? 128 : by_both_mma ? 2 : by_item_readers ? 10 : 1);
         }
-        *abort_flag = 0;
+        sts_volatile(abort_flag, 0);
     }
     fence_barrier_init();
     if (warp == 1) tc::tmem_alloc(sb + OFF_MISC, TMEM_COLS);
@@ -429,7 +443,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         for (;; ++wq) {
             Item I;
             if (t < total_items) I = sched.get(t);
-            if (!publish(t, I) || t >= total_items || *abort_flag) break;
+            if (!publish(t, I) || t >= total_items || lds_volatile(abort_flag)) break;
             t = dyn ? (int)gridDim.x + (int)ahead : t + (int)gridDim.x;
             if (dyn && t < total_items) ahead = atomicAdd(P.items, 1u);
             if (!wait_or_abort(BAR(B_QE), (wq & 1) ^ 1, abort_flag, P.status)) break;
@@ -496,7 +510,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             Item I;
             if (t < total_items) I = get_item(wq & 1);
             mbar_arrive(BAR(B_IE + (wq & 1)));
-            if (t >= total_items || *abort_flag) break;
+            if (t >= total_items || lds_volatile(abort_flag)) break;
             if (!wait_or_abort(BAR(B_QF), wq & 1, abort_flag, P.status)) break;
             const bool mine = I.jb[w] <= I.je[w];
             if (!mine) mbar_arrive(BAR(B_QE));
@@ -571,12 +585,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             // the item's description stays in its ring entry, read from shared
             // memory where used (fewer live registers); the entry is released
             // once the item is done
-            const RingItem I{reinterpret_cast<const volatile int *>(smem + OFF_RING + (kq & 1) * sizeof(Item))};
+            const RingItem I{sb + OFF_RING + (kq & 1) * (uint32_t)sizeof(Item)};
             auto release_item = [&]() {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(B_IE + (kq & 1)));
             };
-            if (t >= total_items || *abort_flag) { release_item(); break; }
+            if (t >= total_items || lds_volatile(abort_flag)) { release_item(); break; }
             const uint32_t g_item = g;                 // K/V stages of this item start at g_item
             g += I.nkv();
             const int rr = I.r0() + w * BM + row;        // query row within its sequence
