@@ -27,23 +27,32 @@
 // Work item = two consecutive 128-row query tiles of one (sequence, head)
 // sharing one stream of 128-key K/V tiles (for W = 64: three key tiles per
 // 256 rows, each query tile multiplying only the two it needs).  One
-// persistent CTA per SM, warp-specialised:
+// persistent CTA per SM, warp-specialised (warp numbers of the plain
+// instances; the bias and paged instances put both MMA threads in warpgroup 0
+// and the softmax in warps 4..11, with registers moved from warpgroup 0 to
+// the softmax warpgroups):
 //   warp 0      TMA producer: both query tiles, then the K/V tiles into a
 //               3-stage ring; everything lands 128-byte swizzled.
 //   warp 1      TMEM owner; with warp 10, one MMA-issuing thread per query
 //               tile (each blocks only on its own tile's barriers): per key
 //               tile, S = Q K^T (4 x 128x128x16) into that tile's S columns,
 //               then O += P V (8 x 128x64x16, P read from TMEM, V MN-major
-//               from shared memory) into its O columns.  QK of key tile j+1 is issued before PV of j, so
-//               scores are ready when the softmax finishes tile j.
+//               from shared memory) into its O columns.  QK of key tile j+1
+//               is issued before PV of j, so scores are ready when the
+//               softmax finishes tile j.
 //   warps 2..5  softmax of query tile 0, warps 6..9 of query tile 1 (the two
 //               groups ping-pong on the tensor core): one thread per row
 //               loads its S row, frees the S columns at once, masks, takes
-//               the max (two-input max chains), and writes P = 2^(scale*s - m) as bf16
-//               pairs into the tile's P columns of TMEM (tcgen05.st); the
-//               scale is folded into the exponent's FMA.  O stays in TMEM: the running max is raised
-//               only when a row's max grows by more than 2^8, and only then
-//               is that row of O rescaled in TMEM (rows never see P > 256).
+//               the max (two-input max chains), and writes P = 2^(scale*s - m)
+//               as bf16 pairs into the tile's P columns of TMEM (tcgen05.st);
+//               the scale is folded into the exponent's FMA.  O stays in
+//               TMEM: the running max is raised only when a row's max grows
+//               by more than 2^8, and only then is that row of O rescaled in
+//               TMEM (rows never see P > 256).  Each warp normalises its 32
+//               rows of O and writes them with one TMA store.
+// Sliding-window layers run an instance that sorts each 32-key chunk of a
+// tile into kept by no row of the warp (no max, no exponentials: P = 0), kept
+// whole, or kept in part (masked key by key).
 // Every wait is bounded: on a timeout the CTA records PKA_DEVCHK_TIMEOUT,
 // every role stops, TMEM is freed, and the kernel returns.
 #include <cuda.h>
@@ -66,7 +75,17 @@ constexpr int BN = 128;        // keys per K/V tile
 constexpr int HD = 64;         // head dim
 constexpr int NS = 3;          // K/V stages
 constexpr int MAX_SEQS = 1024; // sequences per launch (the host splits larger batches)
-constexpr int NTHREADS = 352;  // producer, MMA (tile 0), 2 x 4 softmax warps, MMA (tile 1)
+// Threads: the plain instances run 11 warps (producer, MMA of tile 0, 2 x 4
+// softmax warps, MMA of tile 1) at the 168 registers a thread that 3 warps on a
+// sub-partition leave.  The bias and paged instances run 12 warps: warpgroup 0
+// (producer, MMA of tile 0, MMA of tile 1, one idle warp) gives registers to the
+// two softmax warpgroups (setmaxnreg): 72 + 2 x 216 = 3 x 168, so the softmax's
+// table loads, bias adds and block bookkeeping fit without spills (T5 encoder
+// layer 0.440 -> 0.422 ms, paged self-attention 0.418 -> 0.404 ms; the plain
+// instances gained nothing from it).
+template <bool SPLIT> constexpr int nthreads() { return SPLIT ? 384 : 352; }
+constexpr uint32_t REGS_COPY = 72, REGS_SOFTMAX = 216, REGS_AT_LAUNCH = 168;
+static_assert(REGS_COPY + 2 * REGS_SOFTMAX <= 3 * REGS_AT_LAUNCH, "the split fits the registers of the launch");
 constexpr float RESCALE_LOG2 = 8.f;
 constexpr int LONG_ITEM_TILES = 8;              // key tiles per query tile that make an item long
 constexpr long long TILE1_DELAY_CLOCKS = 2000;  // second query tile's start offset on long items
@@ -235,13 +254,20 @@ __device__ __forceinline__ void add2(float &a0, float &a1, float y0, float y1)
 // P = 2^(scale * s - m) for one tile row as bf16 pairs into the row's TMEM
 // lane (64 columns, key 2c in the low half of column c), 16 columns per store
 // (fewer live registers than one wide store); returns the f32 row sum.
-template <typename T>
-__device__ __forceinline__ float write_p_tmem(const float *x, float scale_log2, float mneg, uint32_t tP)
+template <typename T, bool SKIP>
+__device__ __forceinline__ float write_p_tmem(const float *x, float scale_log2, float mneg, uint32_t tP, uint32_t dead)
 {
     float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t pk[BN / 8];
+        if (SKIP && ((dead >> q4) & 1u)) {
+            // no row of the warp keeps a key of these 32 columns: P = 0
+#pragma unroll
+            for (int c = 0; c < BN / 8; ++c) pk[c] = 0u;
+            tc::tmem_st16(tP + q4 * (BN / 8), pk);
+            continue;
+        }
 #pragma unroll
         for (int c = 0; c < BN / 8; ++c) {
             const int i = q4 * (BN / 4) + 2 * c;
@@ -261,6 +287,11 @@ __device__ __forceinline__ float write_p_tmem(const float *x, float scale_log2, 
     }
     return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
+
+// setmaxnreg: a warpgroup raises or lowers its registers a thread (all its
+// warps execute it); a raise waits until lowered registers are free
+template <uint32_t N> __device__ __forceinline__ void regs_raise() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <uint32_t N> __device__ __forceinline__ void regs_lower() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 
 // bounded wait that also gives up once another role has aborted (the abort
 // flag is the shared word at abort_addr)
@@ -283,12 +314,16 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
 // block tables (tm_k / tm_v are 4-D maps with one cache block per box);
 // otherwise from the packed [T, H, 64] keys of the same rows as the queries.
 // BIAS: the relative-position bias is added to the scores.
-template <typename T, bool PAGED, bool BIAS>
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <typename T, bool PAGED, bool BIAS, bool BAND>
+__global__ void __launch_bounds__(nthreads<PAGED || BIAS>(), 1)
 swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                       const Params P)
 {
+    constexpr bool SPLIT = PAGED || BIAS;             // registers moved to the softmax warpgroups
+    constexpr int NTHREADS = nthreads<SPLIT>();
+    constexpr int SOFTMAX_WARP0 = SPLIT ? 4 : 2;      // the 8 softmax warps follow
+    constexpr int MMA1_WARP = SPLIT ? 2 : NTHREADS / 32 - 1;   // issues the MMAs of query tile 1
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled tiles
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -421,7 +456,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     };
     const bool dyn = P.items != nullptr && total_items > (int)gridDim.x;
 
-    if (warp == 0 && lane == 0) {
+    auto producer = [&]() {
         // ======================= TMA producer =======================
         tc::prefetch_tensormap(&tm_q);
         tc::prefetch_tensormap(&tm_k);
@@ -498,7 +533,8 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             }
             if (!ok) break;
         }
-    } else if ((warp == 1 || warp == NTHREADS / 32 - 1) && lane == 0) {
+    };
+    auto mma_issuer = [&]() {
         // ============ MMA issuer of query tile w (one thread per query tile) ============
         // Each issuer blocks only on its own query tile's barriers; both read
         // every K/V stage and query tile, so those are released by two arrivals.
@@ -569,16 +605,17 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             g += I.nkv;
             if (mine) { cs += I.je[w] - I.jb[w] + 1; ++co; }
         }
-    } else if (warp >= 2 && warp < 10) {
+    };
+    auto softmax = [&]() {
         // ======================= softmax (query tile w) =======================
-        const int w = (warp - 2) >> 2;
+        const int w = (warp - SOFTMAX_WARP0) >> 2;
         const int quarter = warp & 3;                  // TMEM lanes this warp may touch
         const int row = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_addr + COL_S + w * BN;
         const uint32_t tO = tmem + lane_addr + COL_O + w * HD;
         const uint32_t tP = tmem + lane_addr + COL_P + w * (BN / 2);
-        uint32_t cs = 0, co = 0, g = 0, ep = 0;
+        uint32_t cs = 0, co = 0, g = 0;
         for (uint32_t kq = 0;; ++kq) {
             if (!wait_or_abort(BAR(B_IF + (kq & 1)), (kq >> 1) & 1, abort_flag, P.status)) break;
             const int t = item_ring[kq & 1];
@@ -658,27 +695,56 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     boff *= P.scale_log2;
                 }
                 // mask to the kept key range; tile max of the raw scores
-                const int ilo = lo - c0, ihi = hi - c0;
-                const bool masked = ilo > 0 || ihi < BN;
-                if (masked) {
-                    uint32_t mw[4];
+                float mx[4];
+                uint32_t dead = 0;                     // 32-key chunks no row of the warp keeps
+                if constexpr (BAND) {
+                    // banded masks (window, chunk, causal): per 32-key chunk, the
+                    // warp's rows keep none of it, all of it, or part of it; only a
+                    // part-kept chunk is masked key by key, a chunk kept by no row
+                    // skips its max and (in write_p_tmem) its exponentials
+                    const int ilo = lo - c0, ihi = hi - c0;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const int a = min(max(ilo - 32 * k, 0), 32), b = min(max(ihi - 32 * k, 0), 32);
-                        const uint32_t hiw = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
-                        const uint32_t low = a >= 32 ? 0xffffffffu : ((1u << a) - 1u);
-                        mw[k] = hiw & ~low;
+                        const int a = 32 * k;
+                        if (__all_sync(kFull, ihi <= a || ilo >= a + 32)) {
+                            dead |= 1u << k;
+                            mx[k] = -INFINITY;
+                            continue;
+                        }
+                        if (!__all_sync(kFull, ilo <= a && ihi >= a + 32)) {
+                            const int lk = min(max(ilo - a, 0), 32), hk = min(max(ihi - a, 0), 32);
+                            const uint32_t mw = (hk >= 32 ? 0xffffffffu : ((1u << hk) - 1u)) &
+                                                ~(lk >= 32 ? 0xffffffffu : ((1u << lk) - 1u));
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) x[a + i] = (mw & (1u << i)) ? x[a + i] : -INFINITY;
+                        }
+                        float a0 = x[a], a1 = x[a + 1];
+#pragma unroll
+                        for (int i = 2; i < 32; i += 2) { a0 = fmaxf(a0, x[a + i]); a1 = fmaxf(a1, x[a + i + 1]); }
+                        mx[k] = fmaxf(a0, a1);
+                    }
+                } else {
+                    const int ilo = lo - c0, ihi = hi - c0;
+                    const bool masked = ilo > 0 || ihi < BN;
+                    if (masked) {
+                        uint32_t mw[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int a = min(max(ilo - 32 * k, 0), 32), b = min(max(ihi - 32 * k, 0), 32);
+                            const uint32_t hiw = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+                            const uint32_t low = a >= 32 ? 0xffffffffu : ((1u << a) - 1u);
+                            mw[k] = hiw & ~low;
+                        }
+#pragma unroll
+                        for (int i = 0; i < BN; ++i) x[i] = (mw[i >> 5] & (1u << (i & 31))) ? x[i] : -INFINITY;
                     }
 #pragma unroll
-                    for (int i = 0; i < BN; ++i) x[i] = (mw[i >> 5] & (1u << (i & 31))) ? x[i] : -INFINITY;
-                }
-                float mx[4];
+                    for (int k = 0; k < 4; ++k) {
+                        float a0 = x[k * 32], a1 = x[k * 32 + 1];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float a0 = x[k * 32], a1 = x[k * 32 + 1];
-#pragma unroll
-                    for (int i = 2; i < 32; i += 2) { a0 = fmaxf(a0, x[k * 32 + i]); a1 = fmaxf(a1, x[k * 32 + i + 1]); }
-                    mx[k] = fmaxf(a0, a1);
+                        for (int i = 2; i < 32; i += 2) { a0 = fmaxf(a0, x[k * 32 + i]); a1 = fmaxf(a1, x[k * 32 + i + 1]); }
+                        mx[k] = fmaxf(a0, a1);
+                    }
                 }
                 const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * P.scale_log2 + boff;
                 // raise the running max only when it grows by more than 2^8
@@ -693,7 +759,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 if (raise) l *= ex2(m_old - m);
                 // P = 2^(scale * s - m) as bf16 into the swizzled buffer; row sum in f32
                 const float mneg = (m == -INFINITY ? 0.f : -m) + boff;
-                l += write_p_tmem<T>(x, P.scale_log2, mneg, tP);
+                l += write_p_tmem<T, BAND>(x, P.scale_log2, mneg, tP, dead);
                 if (j > I.jb(w) && __any_sync(kFull, raise)) {
                     // the running max rose: bring this row's O to the new max (in TMEM)
                     const float c = raise ? ex2(m_old - m) : 1.f;
@@ -718,15 +784,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             ++co;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int tile0 = I.r0() + w * BM;            // the tile's first row within its sequence
-            if (!BIAS && tile0 + BM <= I.L()) {
-                // a whole tile: rows into the 128-byte-swizzled staging tile, then one
-                // TMA store, so the softmax threads issue no strided global stores
-                // (the bias instances keep plain stores: their per-key table loads
-                // and the extra live registers of this path cost more than it saves).
-                // The group's previous store has finished reading the staging tile:
-                if (row == 0) tc::bulk_wait_read_all();
-                mbar_arrive(BAR(B_EW + w));
-                if (!wait_or_abort(BAR(B_EW + w), ep & 1, abort_flag, P.status)) break;
+            const int wrow0 = tile0 + quarter * 32;     // the warp's first row within its sequence
+            if (!BIAS && wrow0 + 32 <= I.L()) {
+                // the warp's 32 rows, all inside the sequence: into its quarter of the
+                // 128-byte-swizzled staging tile, then one TMA store by its lane 0
+                if (lane == 0) tc::bulk_wait_read_all();
+                __syncwarp();
                 const uint32_t srow = sb + OFF_OST + w * TILE_BYTES + row * 128;
 #pragma unroll
                 for (int c = 0; c < HD / 8; ++c) {
@@ -739,13 +802,11 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                                  : "memory");
                 }
                 fence_proxy_async();                   // the rows are read by the TMA engine
-                mbar_arrive(BAR(B_ER + w));
-                if (row == 0) {
-                    if (!wait_or_abort(BAR(B_ER + w), ep & 1, abort_flag, P.status)) break;
-                    tc::tma_store_3d(&tm_o, 0, I.h(), I.s0() + tile0, sb + OFF_OST + w * TILE_BYTES);
+                __syncwarp();
+                if (lane == 0) {
+                    tc::tma_store_3d(&tm_o, 0, I.h(), I.s0() + wrow0, sb + OFF_OST + w * TILE_BYTES + quarter * 32 * 128);
                     tc::bulk_commit_group();
                 }
-                ++ep;
             } else if (rr < I.L()) {
                 // plain stores of the rows inside the sequence (its last, partial tile)
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) + ((size_t)(I.s0() + rr) * P.H + I.h()) * HD);
@@ -760,7 +821,26 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             release_item();
         }
         (void)co;
-        if (!BIAS && row == 0) tc::bulk_wait_all();   // the staging tiles stay valid until the stores are done
+        if (!BIAS && lane == 0) tc::bulk_wait_all();  // the staging tiles stay valid until the stores are done
+    };
+    if constexpr (SPLIT) {
+        // a warpgroup changes its register count with all of its warps, before
+        // its roles' code, so each role's code is compiled to its own count
+        if (warp < 4) {
+            regs_lower<REGS_COPY>();
+            if (warp == 0 && lane == 0) producer();
+            else if ((warp == 1 || warp == MMA1_WARP) && lane == 0) mma_issuer();
+            __syncwarp();
+        } else {
+            regs_raise<REGS_SOFTMAX>();
+            softmax();
+            __syncwarp();
+            regs_lower<REGS_COPY>();                   // the teardown runs at warpgroup 0's count
+        }
+    } else {
+        if (warp == 0 && lane == 0) producer();
+        else if ((warp == 1 || warp == MMA1_WARP) && lane == 0) mma_issuer();
+        else if (warp >= SOFTMAX_WARP0 && warp < SOFTMAX_WARP0 + 8) softmax();
     }
 
     // ---- teardown: every role is done with TMEM --------------------------------
@@ -864,13 +944,13 @@ EncodeTiledFn encode_fn()
 }
 
 // [T, H, 64] bf16 rows -> boxes of 128 tokens x 64 dims of one head, 128-byte swizzle
-bool make_map(CUtensorMap *m, const void *base, int T, int H, CUtensorMapDataType dt)
+bool make_map(CUtensorMap *m, const void *base, int T, int H, CUtensorMapDataType dt, int rows = BM)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)H, (cuuint64_t)T};
     const cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)H * HD * 2};
-    const cuuint32_t box[3] = {HD, 1, BM};
+    const cuuint32_t box[3] = {HD, 1, (cuuint32_t)rows};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -892,15 +972,25 @@ bool make_paged_map(CUtensorMap *m, const void *base, int num_blocks, int H, CUt
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, bool PAGED, bool BIAS>
+template <typename T, bool PAGED, bool BIAS, bool BAND>
 cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
                        Params P, const PrefillArgs &a, int sms, cudaStream_t stream)
 {
-    auto kern = swa_prefill_tc_kernel<T, PAGED, BIAS>;
+    auto kern = swa_prefill_tc_kernel<T, PAGED, BIAS, BAND>;
+    constexpr bool SPLIT = PAGED || BIAS;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [&] {
         attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (attr == cudaSuccess && SPLIT) {
+            // the softmax warpgroups' raise is granted from what warpgroup 0 lowers;
+            // a build that launched with fewer registers a thread than the split
+            // assumes would leave the raise waiting forever: refuse to launch it
+            cudaFuncAttributes fa;
+            attr = cudaFuncGetAttributes(&fa, kern);
+            if (attr == cudaSuccess && REGS_COPY + 2 * REGS_SOFTMAX > 3u * (unsigned)fa.numRegs)
+                attr = cudaErrorLaunchOutOfResources;
+        }
     });
     if (attr != cudaSuccess) return attr;
     for (int base = 0; base < a.num_seqs; base += MAX_SEQS) {
@@ -913,7 +1003,7 @@ cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
         const long long tiles_upper = (long long)P.num_seqs * ((a.max_seqlen + 2 * BM - 1) / (2 * BM)) * a.num_heads;
         const int grid = (int)std::max<long long>(1, std::min<long long>(sms, tiles_upper));
         if (!next_item_counters(stream, &P.items)) return cudaErrorInvalidDevice;
-        kern<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mo, P);
+        kern<<<grid, nthreads<SPLIT>(), SMEM_BYTES, stream>>>(mq, mk, mv, mo, P);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -924,10 +1014,15 @@ template <typename T>
 cudaError_t dispatch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
                      const Params &P, const PrefillArgs &a, int sms, bool paged, bool bias, cudaStream_t stream)
 {
-    if (paged) return bias ? launch_cfg<T, true, true>(mq, mk, mv, mo, P, a, sms, stream)
-                           : launch_cfg<T, true, false>(mq, mk, mv, mo, P, a, sms, stream);
-    return bias ? launch_cfg<T, false, true>(mq, mk, mv, mo, P, a, sms, stream)
-                : launch_cfg<T, false, false>(mq, mk, mv, mo, P, a, sms, stream);
+    if (paged) return bias ? launch_cfg<T, true, true, false>(mq, mk, mv, mo, P, a, sms, stream)
+                           : launch_cfg<T, true, false, false>(mq, mk, mv, mo, P, a, sms, stream);
+    if (bias) return launch_cfg<T, false, true, false>(mq, mk, mv, mo, P, a, sms, stream);
+    // packed keys without bias: a sliding window takes the instance that
+    // classifies 32-key chunks (a third of a window item's chunks are kept by no
+    // row of the warp); full, chunked and causal attention keep the plain one,
+    // where few tiles are masked and the extra code costs more than it saves
+    if (a.window > 0) return launch_cfg<T, false, false, true>(mq, mk, mv, mo, P, a, sms, stream);
+    return launch_cfg<T, false, false, false>(mq, mk, mv, mo, P, a, sms, stream);
 }
 
 }  // namespace
@@ -939,7 +1034,7 @@ cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream)
     const CUtensorMapDataType dt =
         a.dtype == PKA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, a.q, a.num_tokens, a.num_heads, dt) || !make_map(&mo, a.out, a.num_tokens, a.num_heads, dt))
+    if (!make_map(&mq, a.q, a.num_tokens, a.num_heads, dt) || !make_map(&mo, a.out, a.num_tokens, a.num_heads, dt, 32))
         return cudaErrorInvalidValue;
     if (paged) {
         if (!make_paged_map(&mk, a.k, a.num_blocks, a.num_heads, dt) ||
