@@ -57,6 +57,12 @@
 //  * Batches of at most one (sequence, head) pair per SM run a second kernel
 //    of the same per-block math: one CTA per pair, its blocks dealt to the
 //    CTA's warps, the warps' partial states merged in shared memory.
+//  * Both kernels are launched with programmatic stream serialization: each
+//    CTA lets the next launch in the stream start at once and waits
+//    (griddepcontrol.wait) before its first global read, so a launch's CTAs
+//    take the SMs the previous grid's CTAs leave during its split-K tail
+//    while every input written by an earlier kernel is read only after that
+//    kernel has completed (T5-small-shaped step 11.2 -> 11.0 us).
 
 #include <algorithm>
 #include <cmath>
@@ -259,6 +265,10 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const Params P
     int *cum = reinterpret_cast<int *>(smem + (size_t)NW * NSTAGE * R::STAGE + NW * NSTAGE * 8);
     int *ctxs = cum + P.num_seqs + 1;
     float *table_sm = reinterpret_cast<float *>(ctxs + P.num_seqs);
+    // the next launch may start its CTAs as this grid's CTAs leave the SMs;
+    // nothing an earlier kernel wrote is read before that kernel has finished
+    griddep_launch_dependents();
+    griddep_wait();
 
     // ---- per-sequence partition counts -> prefix sums (whole CTA) ----------
     for (int s = threadIdx.x; s < P.num_seqs; s += blockDim.x) {
@@ -640,6 +650,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_small_kernel(const Param
     float2 *mrg_ml = reinterpret_cast<float2 *>(smem + (size_t)NW * NSTAGE * R::STAGE + NW * NSTAGE * 8);
     float *mrg_acc = reinterpret_cast<float *>(mrg_ml + NW);          // [NW][D]
     float *table_sm = mrg_acc + NW * D;                               // this head's T5 table row
+    griddep_launch_dependents();
+    griddep_wait();
 
     // ---- the pair: launch sequence sl (problem 0's first), head h ----------------
     const int sl = (int)P.by_H.div((uint32_t)blockIdx.x);
@@ -849,6 +861,28 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_small_kernel(const Param
 }
 
 // ---- host side --------------------------------------------------------------------
+
+// Kernels launched with programmatic stream serialization: a launch may begin
+// while the previous kernel in the stream finishes (its CTAs take the SMs the
+// previous grid's CTAs leave); the kernels wait (griddepcontrol.wait) before
+// reading anything, so every input and workspace write of earlier kernels is
+// complete and visible when read.
+template <typename K>
+cudaError_t launch_programmatic(K kern, unsigned grid, unsigned threads, size_t smem, cudaStream_t stream, const Params &P)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
 template <typename T, int D, int NSTAGE, int NW> struct Config {
     using R = Tr<T, D>;
     static size_t smem_bytes(int nseq)
@@ -875,8 +909,7 @@ template <typename T, int D, int NSTAGE, int NW> struct Config {
         for (int i = 0; i < P.nprob; ++i) units_upper += (long long)P.pr[i].num_seqs * P.H * P.pr[i].max_parts;
         long long grid = std::min<long long>((long long)sms * occ, (units_upper + NW - 1) / NW);
         if (grid < 1) grid = 1;
-        kern<<<(unsigned)grid, NW * 32, smem, stream>>>(P);
-        return cudaGetLastError();
+        return launch_programmatic(kern, (unsigned)grid, NW * 32, smem, stream, P);
     }
 };
 
@@ -912,9 +945,8 @@ template <typename T, int D, int NSTAGE> struct SmallConfig {
         int occ = 1;
         const cudaError_t e = prepare(&occ);
         if (e != cudaSuccess) return e;
-        paged_decode_small_kernel<T, D, NSTAGE, SMALL_NW>
-            <<<(unsigned)(P.num_seqs * P.H), SMALL_NW * 32, smem_bytes(table_floats), stream>>>(P);
-        return cudaGetLastError();
+        return launch_programmatic(paged_decode_small_kernel<T, D, NSTAGE, SMALL_NW>, (unsigned)(P.num_seqs * P.H),
+                                   SMALL_NW * 32, smem_bytes(table_floats), stream, P);
     }
 };
 

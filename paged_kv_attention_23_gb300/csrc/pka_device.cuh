@@ -73,6 +73,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     return true;
 }
 
+// ---- programmatic dependent launch (sm_90+) ---------------------------------
+// launch_dependents: the next kernel in the stream, if launched with
+// programmatic stream serialization, may start its CTAs once every CTA of
+// this grid has executed this (or exited).  wait: block until the grids this
+// one depends on have completed and their memory writes are visible; without
+// such a dependency it returns at once.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- copies ----------------------------------------------------------------
 // Bulk global -> shared copy on the TMA engine, completion counted in bytes on
 // the mbarrier.  dst, src 16-byte aligned; bytes a multiple of 16.
