@@ -646,8 +646,9 @@ class PrefillLaunch:
     """One prefill call of a step: its device inputs, output and FLOPs.
     ``host_inputs`` are the tensors a step copies from the host for e2e."""
 
-    def __init__(self, name, case, fn, out, flops, host_inputs, pre=None):
+    def __init__(self, name, case, fn, out, flops, host_inputs, pre=None, nbytes=None):
         self.name, self.case, self.fn, self.out, self.flops = name, case, fn, out, flops
+        self.nbytes = nbytes    # algorithmic HBM bytes of one launch
         self.host_inputs = host_inputs
         self.pre = pre               # work the step does before the call (reshape_and_cache of new K/V)
 
@@ -655,6 +656,47 @@ class PrefillLaunch:
         if self.pre is not None:
             self.pre()
         self.fn()
+
+
+def packed_prefill_bytes(c) -> int:
+    """Algorithmic bytes of a packed prefill layer: q, k, v read once, out
+    written once (2-byte elements), and the bias table if any."""
+    nbytes = 4 * c.num_tokens * c.num_heads * c.head_dim * 2
+    if c.rel_bias is not None:
+        nbytes += c.rel_bias.size * 4
+    return nbytes
+
+
+def paged_prefill_bytes(pc) -> int:
+    """Algorithmic bytes of a paged prefill call: q read and out written once,
+    and for every sequence and head the K and V rows its queries can see (the
+    last query sees keys up to ctx - 1; a window starts the first query's keys
+    W - 1 before it), the block-table entries of those rows, the context
+    lengths and query offsets, and the bias table if any."""
+    c = pc.cache
+    H, D = pc.num_heads, pc.head_dim
+    ctx = c.context_lens.astype(np.int64)
+    lq = pc.query_lens.astype(np.int64)
+    lo = np.zeros_like(ctx) if pc.window <= 0 else np.maximum(0, ctx - lq - pc.window + 1)
+    keys = np.where(lq > 0, ctx - lo, 0)
+    blocks = np.where(keys > 0, (ctx + 15) // 16 - lo // 16, 0)
+    nbytes = int(keys.sum()) * H * D * 2 * 2 + 2 * int(lq.sum()) * H * D * 2
+    nbytes += int(blocks.sum()) * 4 + 4 * len(ctx) + 4 * (len(ctx) + 1)
+    if pc.rel_bias is not None:
+        nbytes += pc.rel_bias.size * 4
+    return nbytes
+
+
+def prefill_bound(flops, nbytes, ms, peaks):
+    """The roofline that binds a launch (the longer of its FLOPs at the bf16
+    peak and its bytes at the HBM peak), the fraction of it reached, and both
+    single-resource fractions."""
+    t_f = flops / (peaks["bf16_tflops"] * 1e12)
+    t_b = nbytes / (peaks["hbm_gbs"] * 1e9) if nbytes else 0.0
+    t = ms * 1e-3
+    return {"bound": "tensor" if t_f >= t_b else "hbm", "frac_roofline": round(max(t_f, t_b) / t, 4),
+            "frac_bf16": round(t_f / t, 4), "frac_hbm": round(t_b / t, 4) if nbytes else None,
+            "intensity_flop_per_byte": round(flops / nbytes, 1) if nbytes else None}
 
 
 def build_prefill_launches(args, pka, device):
@@ -682,7 +724,8 @@ def build_prefill_launches(args, pka, device):
             else:
                 fn = (lambda c=c, q=q, k=k, v=v, out=out:
                       pka.swa_prefill(out, q, k, v, cu, c.max_seqlen, c.window, c.causal, c.scale))
-            launches.append(PrefillLaunch(c.name, c, fn, out, prefill_flops(c), [q, k, v, cu]))
+            launches.append(PrefillLaunch(c.name, c, fn, out, prefill_flops(c), [q, k, v, cu],
+                                          nbytes=packed_prefill_bytes(c)))
         return launches
     # t5-paged-prefill: a prompt chunk of every sequence of the T5-large decode
     # batch against the self-attention cache (its K/V written first) and the
@@ -715,7 +758,8 @@ def build_prefill_launches(args, pka, device):
             ins += [new_k, new_v, slots]
         fn = (lambda pc=pc, out=out, kc=kc, vc=vc, bt=bt, cl=cl, rel=rel:
               pka.paged_prefill(out, q, kc, vc, bt, cuq, cl, pc.max_query_len, pc.window, pc.causal, rel, pc.scale))
-        launches.append(PrefillLaunch(pc.name, pc, fn, out, 4 * D * H * pc.kept_pairs(), ins, pre))
+        launches.append(PrefillLaunch(pc.name, pc, fn, out, 4 * D * H * pc.kept_pairs(), ins, pre,
+                                      nbytes=paged_prefill_bytes(pc)))
         del key, value
         c.device_kv = None
     torch.cuda.empty_cache()
@@ -766,22 +810,34 @@ def run_prefill(args, rank, world, local, peaks):
     pair_ms = per_launch_ms(lambda ev: [step(ev, k) for k in range(K)], len(launches), K)
     value = sum(flops) * world / (ms_step * 1e-3) / 1e12
     jd = int(np.argmax(flops))
-    ach = flops[jd] / (launch_ms[jd] * 1e-3) / 1e12
-    peak = peaks["bf16_tflops"]
     cases = [l.case for l in launches]
+    bounds = [prefill_bound(l.flops, l.nbytes, m, peaks) for l, m in zip(launches, launch_ms)]
     packed = args.workload != "t5-paged-prefill"
     qkv_bytes = [4 * c.num_tokens * c.num_heads * c.head_dim * 2 for c in cases]
     kname = {"t5-paged-prefill": "paged_prefill (self-attention, causal + T5 bias)",
              "t5-encoder-prefill": "prefill_biased (T5 encoder layer)"}.get(args.workload,
                                                                          "swa_prefill (full-attention layer)")
-    roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+    # the dominant launch against the roofline that binds it: the tensor peak
+    # when its FLOPs take longer there than its bytes at the HBM peak, else HBM
+    bd = bounds[jd]
+    if bd["bound"] == "tensor":
+        ach, peak, unit = flops[jd] / (launch_ms[jd] * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        peak_src = peaks["src"] + " bf16_tflops (burst)"
+    else:
+        ach, peak, unit = launches[jd].nbytes / (launch_ms[jd] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+        peak_src = peaks["src"] + " hbm_gbs"
+    roof = {"bound": bd["bound"], "achieved": round(ach, 2), "peak": peak, "unit": unit,
             "frac": round(ach / peak, 4), "traffic": recorded_traffic("swa_prefill.cu", args.workload),
-            "kernel": kname, "alg_flops_per_launch": flops[jd],
+            "kernel": kname, "alg_flops_per_launch": flops[jd], "alg_bytes_per_launch": launches[jd].nbytes,
+            "frac_bf16": bd["frac_bf16"], "frac_hbm": bd["frac_hbm"],
+            "intensity_flop_per_byte": bd["intensity_flop_per_byte"],
             "launch_ms": round(launch_ms[jd], 4), "launch_timing": "a graph of that launch alone / launches",
-            "peak_src": peaks["src"] + " bf16_tflops (burst)"}
+            "peak_src": peak_src}
     extra = {"launch_ms": [round(x, 4) for x in launch_ms],
              "launch_ms_event_pairs": [round(x, 4) for x in pair_ms],
              "launch_TFLOPs": [round(f / (m * 1e-3) / 1e12, 2) for f, m in zip(flops, launch_ms)],
+             "launch_GBps": [round(l.nbytes / (m * 1e-3) / 1e9, 1) for l, m in zip(launches, launch_ms)],
+             "launch_bounds": bounds,
              "flops_per_step": sum(flops)}
     if args.workload == "encoder-prefill":
         extra["window_layer_GBps"] = [round(b / (m * 1e-3) / 1e9, 1) for b, m in zip(qkv_bytes[1:], launch_ms[1:])]
@@ -815,8 +871,9 @@ def run_prefill(args, rank, world, local, peaks):
 
 def prefill_record(launches, K, peaks, world=1, ms_step=None, launch_ms=None):
     """Graph-timed layer launches and step of the encoder prefill: TFLOP/s and
-    the fraction of the bf16 peak per layer and for the step; the window
-    layers also in GB/s of their q, k, v reads and out writes."""
+    the fraction of the bf16 peak per layer and for the step; every layer also
+    in GB/s of its algorithmic bytes (q, k, v read, out written) with the
+    roofline that binds it."""
     if launch_ms is None:
         launch_ms = [graph_ms(lambda k, l=l: l.fn(), K, world) for l in launches]
     if ms_step is None:
@@ -828,11 +885,11 @@ def prefill_record(launches, K, peaks, world=1, ms_step=None, launch_ms=None):
         tf = l.flops / (ms * 1e-3) / 1e12
         e = {"layer": c.name, "window": c.window, "ms_per_launch": round(ms, 4), "TFLOPs": round(tf, 1),
              "frac_bf16": round(tf / bf16, 4), "alg_flops": l.flops}
-        if c.window > 0:
-            nbytes = 4 * c.num_tokens * c.num_heads * c.head_dim * 2
-            e["GBps"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
-            e["frac_hbm"] = round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4)
-            e["alg_bytes"] = nbytes
+        if l.nbytes:
+            e["GBps"] = round(l.nbytes / (ms * 1e-3) / 1e9, 1)
+            e["frac_hbm"] = round(l.nbytes / (ms * 1e-3) / 1e9 / hbm, 4)
+            e["alg_bytes"] = l.nbytes
+            e["bound"] = prefill_bound(l.flops, l.nbytes, ms, peaks)["bound"]
         layers.append(e)
     flops = sum(l.flops for l in launches)
     tf = flops / (ms_step * 1e-3) / 1e12

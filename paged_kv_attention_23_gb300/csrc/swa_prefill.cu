@@ -32,7 +32,8 @@
 // and the softmax in warps 4..11, with registers moved from warpgroup 0 to
 // the softmax warpgroups):
 //   warp 0      TMA producer: both query tiles, then the K/V tiles into a
-//               3-stage ring; everything lands 128-byte swizzled.
+//               ring of 3 stages (4 for paged keys); everything lands
+//               128-byte swizzled.
 //   warp 1      TMEM owner; with warp 10, one MMA-issuing thread per query
 //               tile (each blocks only on its own tile's barriers): per key
 //               tile, S = Q K^T (4 x 128x128x16) into that tile's S columns,
@@ -73,7 +74,6 @@ namespace {
 constexpr int BM = 128;        // query rows per tile = TMEM lanes = MMA M
 constexpr int BN = 128;        // keys per K/V tile
 constexpr int HD = 64;         // head dim
-constexpr int NS = 3;          // K/V stages
 constexpr int MAX_SEQS = 1024; // sequences per launch (the host splits larger batches)
 // Threads: the plain instances run 11 warps (producer, MMA of tile 0, 2 x 4
 // softmax warps, MMA of tile 1) at the 168 registers a thread that 3 warps on a
@@ -91,19 +91,27 @@ constexpr int LONG_ITEM_TILES = 8;              // key tiles per query tile that
 constexpr long long TILE1_DELAY_CLOCKS = 2000;  // second query tile's start offset on long items
 
 constexpr uint32_t TILE_BYTES = BM * HD * 2;             // 16 KB: one Q, K or V tile
-constexpr uint32_t OFF_Q = 0;                             // 2 query tiles
-constexpr uint32_t OFF_KV = 2 * TILE_BYTES;               // NS x (K, V)
-constexpr uint32_t OFF_OST = OFF_KV + NS * 2 * TILE_BYTES;  // 2 output staging tiles (one per query tile)
-constexpr uint32_t OFF_BAR = OFF_OST + 2 * TILE_BYTES;
-// barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], s_empty[2], p_full[2], o_full[2], o_empty[2]
-constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NS, B_SF = 2 + 2 * NS, B_SE = B_SF + 2, B_PF = B_SE + 2,
-              B_OF = B_PF + 2, B_OE = B_OF + 2, B_EW = B_OE + 2, B_ER = B_EW + 2, B_IF = B_ER + 2, B_IE = B_IF + 2,
-              NBAR = B_IE + 2;
-constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, abort flag, item ring [2]
-constexpr uint32_t OFF_RING = (OFF_MISC + 16 + 127) / 128 * 128;   // the two ring entries' items (64 B each)
-constexpr uint32_t OFF_SCHED = OFF_RING + 128;
-constexpr uint32_t SMEM_BYTES = OFF_SCHED + (6 * MAX_SEQS + 1) * 4 + 1024;   // + alignment slack
-static_assert(SMEM_BYTES <= 227u * 1024u, "dynamic shared memory per CTA");
+// Shared memory and barriers of an instance with NS K/V stages.  The paged
+// instances stream one 2 KB box per cache block and keep a fourth tile in
+// flight (paged self- and cross-attention 4-5 % faster); the packed
+// instances keep three (a fourth slowed the window and T5 encoder layers).
+template <bool PAGED> constexpr int nstages() { return PAGED ? 4 : 3; }
+template <int NS> struct Layout {
+    static constexpr uint32_t OFF_Q = 0;                             // 2 query tiles
+    static constexpr uint32_t OFF_KV = 2 * TILE_BYTES;               // NS x (K, V)
+    static constexpr uint32_t OFF_OST = OFF_KV + NS * 2 * TILE_BYTES;  // 2 output staging tiles (one per query tile)
+    static constexpr uint32_t OFF_BAR = OFF_OST + 2 * TILE_BYTES;
+    // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], s_empty[2], p_full[2], o_full[2],
+    // o_empty[2], item ring full[2] / empty[2]
+    static constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NS, B_SF = 2 + 2 * NS, B_SE = B_SF + 2,
+                         B_PF = B_SE + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_IF = B_OE + 2, B_IE = B_IF + 2,
+                         NBAR = B_IE + 2;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, abort flag, item ring [2]
+    static constexpr uint32_t OFF_RING = (OFF_MISC + 16 + 127) / 128 * 128;   // the two ring entries' items (64 B each)
+    static constexpr uint32_t OFF_SCHED = OFF_RING + 128;
+    static constexpr uint32_t SMEM_BYTES = OFF_SCHED + (6 * MAX_SEQS + 1) * 4 + 1024;   // + alignment slack
+    static_assert(SMEM_BYTES <= 227u * 1024u, "dynamic shared memory per CTA");
+};
 constexpr int CBS = 16;                   // paged cache block: 16 key rows of one head
 constexpr uint32_t CBLK_BYTES = CBS * HD * 2;                                  // 2 KB per block and head
 
@@ -321,6 +329,13 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                       const Params P)
 {
     constexpr bool SPLIT = PAGED || BIAS;             // registers moved to the softmax warpgroups
+    constexpr int NS = nstages<PAGED>();
+    using LY = Layout<NS>;
+    constexpr uint32_t OFF_Q = LY::OFF_Q, OFF_KV = LY::OFF_KV, OFF_OST = LY::OFF_OST, OFF_BAR = LY::OFF_BAR,
+                       OFF_MISC = LY::OFF_MISC, OFF_RING = LY::OFF_RING, OFF_SCHED = LY::OFF_SCHED;
+    constexpr int B_QF = LY::B_QF, B_QE = LY::B_QE, B_KVF = LY::B_KVF, B_KVE = LY::B_KVE, B_SF = LY::B_SF,
+                  B_SE = LY::B_SE, B_PF = LY::B_PF, B_OF = LY::B_OF, B_OE = LY::B_OE, B_IF = LY::B_IF, B_IE = LY::B_IE,
+                  NBAR = LY::NBAR;
     constexpr int NTHREADS = nthreads<SPLIT>();
     constexpr int SOFTMAX_WARP0 = SPLIT ? 4 : 2;      // the 8 softmax warps follow
     constexpr int MMA1_WARP = SPLIT ? 2 : NTHREADS / 32 - 1;   // issues the MMAs of query tile 1
@@ -361,8 +376,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     if (threadIdx.x == 0) {
         for (int i = 0; i < NBAR; ++i) {
             const bool by_softmax = (i >= B_SE && i < B_SE + 2) || (i >= B_PF && i < B_PF + 2) ||
-                                    (i >= B_OE && i < B_OE + 2) || (i >= B_EW && i < B_EW + 2) ||
-                                    (i >= B_ER && i < B_ER + 2);
+                                    (i >= B_OE && i < B_OE + 2);
             const bool by_both_mma = i == B_QE || (i >= B_KVE && i < B_KVE + NS);
             const bool by_item_readers = i >= B_IE && i < B_IE + 2;   // 2 MMA threads + 8 softmax warps
             mbar_init(BAR(i), by_softmax ? 128 : by_both_mma ? 2 : by_item_readers ? 10 : 1);
@@ -978,6 +992,7 @@ cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
 {
     auto kern = swa_prefill_tc_kernel<T, PAGED, BIAS, BAND>;
     constexpr bool SPLIT = PAGED || BIAS;
+    constexpr uint32_t SMEM_BYTES = Layout<nstages<PAGED>()>::SMEM_BYTES;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [&] {
