@@ -701,7 +701,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     else if (tab_sm) {
                         const float *tr = trel + dhi;      // |dhi - i| < cap + BN in the band
 #pragma unroll
-                        for (int i = 0; i < BN; ++i) x[i] += tr[-i];
+                        for (int i = 0; i < BN; i += 2) add2(x[i], x[i + 1], tr[-i], tr[-i - 1]);
                     } else {
 #pragma unroll
                         for (int i = 0; i < BN; ++i) x[i] += __ldg(rel + min(max(dhi - i, -cap), cap));
