@@ -96,7 +96,10 @@ constexpr uint32_t TILE_BYTES = BM * HD * 2;             // 16 KB: one Q, K or V
 // flight (paged self- and cross-attention 4-5 % faster); the packed
 // instances keep three (a fourth slowed the window and T5 encoder layers).
 template <bool PAGED> constexpr int nstages() { return PAGED ? 4 : 3; }
-template <int NS> struct Layout {
+constexpr uint32_t TAB_FLOATS = 2 * TILE_BYTES / 4;   // widened bias tables held in shared memory, at most
+// Layout<NS, TAB>: TAB gives the bias table a region of its own (else it
+// takes the output staging tiles' place and the outputs go out by plain stores)
+template <int NS, bool TAB> struct Layout {
     static constexpr uint32_t OFF_Q = 0;                             // 2 query tiles
     static constexpr uint32_t OFF_KV = 2 * TILE_BYTES;               // NS x (K, V)
     static constexpr uint32_t OFF_OST = OFF_KV + NS * 2 * TILE_BYTES;  // 2 output staging tiles (one per query tile)
@@ -109,9 +112,16 @@ template <int NS> struct Layout {
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, abort flag, item ring [2]
     static constexpr uint32_t OFF_RING = (OFF_MISC + 16 + 127) / 128 * 128;   // the two ring entries' items (64 B each)
     static constexpr uint32_t OFF_SCHED = OFF_RING + 128;
-    static constexpr uint32_t SMEM_BYTES = OFF_SCHED + (6 * MAX_SEQS + 1) * 4 + 1024;   // + alignment slack
+    static constexpr uint32_t OFF_TAB = (OFF_SCHED + (6 * MAX_SEQS + 1) * 4 + 15) / 16 * 16;
+    static constexpr uint32_t SMEM_BYTES = OFF_TAB + (TAB ? TAB_FLOATS * 4 : 0) + 1024;   // + alignment slack
     static_assert(SMEM_BYTES <= 227u * 1024u, "dynamic shared memory per CTA");
 };
+// the packed bias instances give the table its own region, and their outputs
+// leave by TMA stores instead of strided plain stores (T5 encoder layer 0.417
+// -> 0.373 ms); the paged bias instance, with its fourth K/V stage, has no
+// room left and keeps plain stores (most of its rows end in partial warps,
+// and trading the fourth stage for the table measured 7 % slower)
+template <bool PAGED, bool BIAS> constexpr bool own_table() { return BIAS && !PAGED; }
 constexpr int CBS = 16;                   // paged cache block: 16 key rows of one head
 constexpr uint32_t CBLK_BYTES = CBS * HD * 2;                                  // 2 KB per block and head
 
@@ -330,7 +340,9 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 {
     constexpr bool SPLIT = PAGED || BIAS;             // registers moved to the softmax warpgroups
     constexpr int NS = nstages<PAGED>();
-    using LY = Layout<NS>;
+    constexpr bool TAB = own_table<PAGED, BIAS>();
+    constexpr bool TMA_OUT = !BIAS || TAB;           // outputs through the staging tiles
+    using LY = Layout<NS, TAB>;
     constexpr uint32_t OFF_Q = LY::OFF_Q, OFF_KV = LY::OFF_KV, OFF_OST = LY::OFF_OST, OFF_BAR = LY::OFF_BAR,
                        OFF_MISC = LY::OFF_MISC, OFF_RING = LY::OFF_RING, OFF_SCHED = LY::OFF_SCHED;
     constexpr int B_QF = LY::B_QF, B_QE = LY::B_QE, B_KVF = LY::B_KVF, B_KVE = LY::B_KVE, B_SF = LY::B_SF,
@@ -403,16 +415,16 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         seqid[rk] = s;
         if (PAGED) lenk[rk] = min(max(P.context_lens[s], 0), P.mbps * CBS);
     }
-    // The bias instances store outputs without the staging tiles; that space
-    // holds every head's relative-position table instead, widened to the
+    // The bias instances hold every head's relative-position table in shared
+    // memory (a region of its own, or the staging tiles' space), widened to the
     // distances a key tile in the band can present (|d| < cap + BN) with the
     // clamped values, so a score's bias is one shared load at a constant
     // offset: no clamp, no global load.  Tables too large for it stay in
     // global memory (read through the clamp, as before).
     const int bias_cap = BIAS ? P.num_buckets - 1 : 0;
     const int tab_span = 2 * (bias_cap + BN) - 1;
-    const bool tab_sm = BIAS && (long long)P.H * tab_span <= (long long)(2 * TILE_BYTES / 4);
-    float *tab = reinterpret_cast<float *>(smem + OFF_OST);
+    const bool tab_sm = BIAS && (long long)P.H * tab_span <= (long long)TAB_FLOATS;
+    float *tab = reinterpret_cast<float *>(smem + (TAB ? LY::OFF_TAB : OFF_OST));
     if (tab_sm) {
         for (int i = threadIdx.x; i < P.H * tab_span; i += NTHREADS) {
             const int h = i / tab_span, d = i - h * tab_span - (bias_cap + BN - 1);
@@ -799,7 +811,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int tile0 = I.r0() + w * BM;            // the tile's first row within its sequence
             const int wrow0 = tile0 + quarter * 32;     // the warp's first row within its sequence
-            if (!BIAS && wrow0 + 32 <= I.L()) {
+            if (TMA_OUT && wrow0 + 32 <= I.L()) {
                 // the warp's 32 rows, all inside the sequence: into its quarter of the
                 // 128-byte-swizzled staging tile, then one TMA store by its lane 0
                 if (lane == 0) tc::bulk_wait_read_all();
@@ -835,7 +847,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             release_item();
         }
         (void)co;
-        if (!BIAS && lane == 0) tc::bulk_wait_all();  // the staging tiles stay valid until the stores are done
+        if (TMA_OUT && lane == 0) tc::bulk_wait_all();   // the staging tiles stay valid until the stores are done
     };
     if constexpr (SPLIT) {
         // a warpgroup changes its register count with all of its warps, before
@@ -992,7 +1004,7 @@ cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
 {
     auto kern = swa_prefill_tc_kernel<T, PAGED, BIAS, BAND>;
     constexpr bool SPLIT = PAGED || BIAS;
-    constexpr uint32_t SMEM_BYTES = Layout<nstages<PAGED>()>::SMEM_BYTES;
+    constexpr uint32_t SMEM_BYTES = Layout<nstages<PAGED>(), own_table<PAGED, BIAS>()>::SMEM_BYTES;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [&] {
