@@ -103,25 +103,41 @@ def _torch():
     return torch
 
 
+_DTYPES = None
+
+
 def _dtype_code(t) -> int:
-    torch = _torch()
-    return {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[t.dtype]
+    global _DTYPES
+    if _DTYPES is None:
+        torch = _torch()
+        _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+    return _DTYPES[t.dtype]
 
 
 DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
 
 
 def _ptr(t):
-    if t is None:
-        return None
-    return ctypes.c_void_p(t.data_ptr())
+    """Device address of a tensor (an int, which ctypes passes as void *), or None."""
+    return None if t is None else t.data_ptr()
+
+
+_raw_stream = None
 
 
 def _stream(stream):
+    """The cudaStream_t to launch on: the given torch stream, else torch's
+    current stream on the current device."""
+    global _raw_stream
     torch = _torch()
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is None:
+        # the raw handle of the current stream without building a Stream object
+        # (where the installed torch has the call), else through current_stream
+        _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None) or \
+            (lambda idx: torch.cuda.current_stream(idx).cuda_stream)
+    return _raw_stream(torch.cuda.current_device())
 
 
 def _check(fn: str, code: int):
