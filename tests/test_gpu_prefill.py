@@ -412,3 +412,30 @@ def test_prefill_item_counters_are_clean_after_every_launch(cuda_lib):
         got = to_f64(run_gpu_prefill(cuda_lib, case), BF16)   # 172 items, the paged launch's pair
         _check(got, ref, "packed launch after a full cycle of counter pairs")
     assert int(gp.status.item()) == 0
+
+
+def test_prefill_more_sequences_than_one_launch(cuda_lib):
+    """1300 short sequences: the host splits each call into launches of at
+    most 1024 sequences (the kernel's schedule holds 1024).  Every row of the
+    full-attention, window-64 (the chunk-classifying instance), biased and
+    paged calls against the oracle, across the split."""
+    rng = np.random.default_rng(77)
+    lens = rng.integers(1, 48, size=1300).tolist()
+    for window in (-1, 64):
+        case = synth.make_prefill_case("many", 700 + max(window, 0), lens, 2, 64, window, 0, BF16, scale=1 / 8)
+        got = to_f64(run_gpu_prefill(cuda_lib, case), BF16)
+        ref = oracle.prefill(case.q, case.k, case.v, case.cu_seqlens, window, 0, case.scale, BF16)
+        _check(got, ref, f"1300 sequences W={window}")
+    case = synth.make_prefill_case("many-biased", 702, lens, 2, 64, -1, 1, BF16, scale=1 / 8)
+    case.rel_bias = synth.rel_bias_table(33, 2, 33) * np.float32(2.0)
+    got = to_f64(run_gpu_biased(cuda_lib, case), BF16)
+    ref = oracle.prefill_biased(case.q, case.k, case.v, case.cu_seqlens, -1, 1, case.scale, BF16, case.rel_bias)
+    _check(got, ref, "1300 sequences biased")
+    ctx = rng.integers(1, 70, size=1300)
+    ql = np.minimum(ctx, rng.integers(1, 40, size=1300))
+    pc = synth.make_paged_prefill_case("many-paged", 703, BF16, ctx.tolist(), ql.tolist(), 2, 64, -1, 1, 17,
+                                       scale=1 / 8, pool_blocks=int(((ctx + 15) // 16).sum()) + 64)
+    gp = GpuPagedPrefill(pc, cuda_lib)
+    got = to_f64(gp.run(), BF16)
+    _check(got, oracle_paged(gp), "1300 sequences paged")
+    assert int(gp.status.item()) == 0
