@@ -30,3 +30,56 @@ def test_oracle_leg_line():
     d = _run("--oracle-leg", "--workload", "t5-small-decode", "--cpu-seconds", "1")
     assert d["unit"] == "GB/s" and d["value"] > 0 and d["kind"] == "oracle"
     assert "drawn on the host" in d["sample"]
+
+
+def _bench():
+    sys.path.insert(0, ROOT)
+    import bench
+    return bench
+
+
+def test_paged_prefill_bytes_count_the_keys_each_sequence_sees():
+    """bench.py's algorithmic bytes of a paged prefill call: the visible key
+    rows of every sequence and head (brute force: the union of the keys each
+    query row keeps), the cache blocks that hold them, q and out, the index
+    arrays and the bias table."""
+    import numpy as np
+    import synth
+    bench = _bench()
+    rng = np.random.default_rng(5)
+    for window in (-1, 3, 40):
+        for causal in (0, 1):
+            ctx = rng.integers(0, 90, size=9)
+            ql = np.minimum(ctx, rng.integers(0, 30, size=9))
+            pc = synth.make_paged_prefill_case("bytes", 11, synth.BF16, ctx.tolist(), ql.tolist(), 2, 64, window,
+                                               causal, 5, scale=1 / 8)
+            keys = blocks = 0
+            for c, lq in zip(ctx.tolist(), ql.tolist()):
+                seen = set()
+                for r in range(lq):
+                    pos = c - lq + r
+                    lo, hi = 0, c
+                    if window > 0:
+                        lo = max(0, pos - window + 1)
+                        if not causal:
+                            hi = min(c, pos + window)
+                    if causal:
+                        hi = min(hi, pos + 1)
+                    seen.update(range(lo, hi))
+                keys += len(seen)
+                blocks += len({k // 16 for k in seen})
+            H, D, S = 2, 64, len(ctx)
+            want = keys * H * D * 2 * 2 + 2 * int(ql.sum()) * H * D * 2 + blocks * 4 + 4 * S + 4 * (S + 1) \
+                + pc.rel_bias.size * 4
+            assert bench.paged_prefill_bytes(pc) == want, (window, causal)
+
+
+def test_prefill_bound_picks_the_longer_of_flops_and_bytes():
+    bench = _bench()
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 8000.0}          # ridge: 250 FLOP per byte
+    b = bench.prefill_bound(2.0e12, 1.0e9, 2.0, peaks)           # 2000 FLOP/B: tensor-bound
+    assert b["bound"] == "tensor" and b["frac_roofline"] == b["frac_bf16"] == 0.5
+    assert b["frac_hbm"] == 0.0625 and b["intensity_flop_per_byte"] == 2000.0
+    b = bench.prefill_bound(1.0e11, 1.0e9, 0.25, peaks)          # 100 FLOP/B: HBM-bound
+    assert b["bound"] == "hbm" and b["frac_roofline"] == b["frac_hbm"] == 0.5
+    assert b["frac_bf16"] == 0.2
