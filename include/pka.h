@@ -17,6 +17,15 @@
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  *    stream) and runs asynchronously.  Outputs are valid once that work has
  *    completed.
+ *  - The decode kernels are launched with programmatic stream serialization:
+ *    they may start while the previous kernel in the stream finishes, and
+ *    read nothing before it has completed.  They also let the NEXT kernel in
+ *    the stream start early if that kernel was itself launched with
+ *    programmatic stream serialization; such a kernel must wait for its
+ *    dependencies (cudaGridDependencySynchronize / griddepcontrol.wait)
+ *    before reading a decode's outputs, as the CUDA programming model
+ *    requires of any kernel launched that way.  Kernels launched without
+ *    that attribute see plain stream order.
  *  - Arguments are checked on the host before anything is launched; a bad
  *    argument returns PKA_ERR_INVALID_ARG (or PKA_ERR_UNSUPPORTED for a legal
  *    but unimplemented shape / dtype) and launches nothing.  A failed launch
