@@ -42,7 +42,9 @@
  *    one (block, head) is one contiguous block_size * head_dim run.
  *  - Supported now: head_dim in {64, 128}; block_size 16; num_kv_heads ==
  *    num_heads.  Decode: f32, f16, bf16 (q, caches and out share one dtype;
- *    the bias is always f32).  Prefill: bf16 or f16, head_dim 64.
+ *    the bias is always f32).  Prefill: bf16 or f16; head_dim 64, or 128 for
+ *    pka_swa_prefill and pka_chunked_prefill (the biased and paged prefills
+ *    answer PKA_ERR_UNSUPPORTED at 128).
  */
 #ifndef PKA_H
 #define PKA_H
@@ -313,7 +315,7 @@ PKA_API pka_status pka_paged_attn_decode_noalloc(void *out, const void *q, const
  * Only key tiles that intersect the mask are visited.
  *
  *   out, q, k, v  [num_tokens, num_heads, head_dim] of dtype (PKA_BF16 or
- *                 PKA_F16; head_dim 64), contiguous
+ *                 PKA_F16; head_dim 64 or 128), contiguous
  *   cu_seqlens    int32 [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0,
  *                 cu_seqlens[num_seqs] = num_tokens
  *   max_seqlen    upper bound on every sequence length (a longer sequence

@@ -326,7 +326,7 @@ def paged_attn_decode_multi(problems, status=None, stream=None):
 
 def swa_prefill(out, q, k, v, cu_seqlens, max_seqlen, window=-1, causal=0, scale=None, status=None, stream=None):
     """Packed varlen prefill with full / causal / sliding-window (|i-j| < W)
-    masks; q/k/v/out [T, H, 64] bf16 or f16 (one dtype), cu_seqlens int32 [B+1]."""
+    masks; q/k/v/out [T, H, 64 or 128] bf16 or f16 (one dtype), cu_seqlens int32 [B+1]."""
     torch = _torch()
     for n, t in (("out", out), ("q", q), ("k", k), ("v", v)):
         _need(t, n, ndim=3)

@@ -100,14 +100,15 @@ pka_status prepare_decode(const pka_decode_problem &p, int block_size, int num_h
 // launch arguments (a.num_tokens == 0: nothing to launch).
 pka_status prepare_prefill(void *out, const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
                            int num_seqs, int num_tokens, int max_seqlen, int num_heads, int head_dim, int window,
-                           int causal, float scale, pka_dtype dtype, int32_t *status, pka::PrefillArgs &a)
+                           int causal, float scale, pka_dtype dtype, int32_t *status, pka::PrefillArgs &a,
+                           bool head_dim_128 = false)
 {
     if (num_seqs < 0 || num_tokens < 0 || max_seqlen < 0 || num_heads < 1 || !std::isfinite(scale) ||
         (causal != 0 && causal != 1) || !dtype_ok(dtype))
         return PKA_ERR_INVALID_ARG;
     if (window != -1 && window < 1) return PKA_ERR_INVALID_ARG;
     if (dtype != PKA_BF16 && dtype != PKA_F16) return PKA_ERR_UNSUPPORTED;
-    if (head_dim != 64) return PKA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && !(head_dim == 128 && head_dim_128)) return PKA_ERR_UNSUPPORTED;
     a.num_tokens = 0;
     a.dtype = dtype;
     if (num_seqs == 0 || num_tokens == 0) return PKA_OK;
@@ -260,7 +261,7 @@ pka_status pka_swa_prefill(void *out, const void *q, const void *k, const void *
 {
     pka::PrefillArgs a;
     const pka_status st = prepare_prefill(out, q, k, v, cu_seqlens, num_seqs, num_tokens, max_seqlen, num_heads,
-                                          head_dim, window, causal, scale, dtype, status, a);
+                                          head_dim, window, causal, scale, dtype, status, a, true);
     if (st != PKA_OK || a.num_tokens == 0) return st;
     return from_cuda(pka::launch_swa_prefill(a, static_cast<cudaStream_t>(stream)));
 }
@@ -272,7 +273,7 @@ pka_status pka_chunked_prefill(void *out, const void *q, const void *k, const vo
     if (chunk < 1) return PKA_ERR_INVALID_ARG;
     pka::PrefillArgs a;
     const pka_status st = prepare_prefill(out, q, k, v, cu_seqlens, num_seqs, num_tokens, max_seqlen, num_heads,
-                                          head_dim, -1, causal, scale, dtype, status, a);
+                                          head_dim, -1, causal, scale, dtype, status, a, true);
     if (st != PKA_OK || a.num_tokens == 0) return st;
     a.chunk = chunk;
     return from_cuda(pka::launch_swa_prefill(a, static_cast<cudaStream_t>(stream)));

@@ -54,6 +54,11 @@
 // Sliding-window layers run an instance that sorts each 32-key chunk of a
 // tile into kept by no row of the warp (no max, no exponentials: P = 0), kept
 // whole, or kept in part (masked key by key).
+// Head dim 128 (packed keys, no bias): a work item is one query tile with one
+// softmax warpgroup, since S, O and P of a tile take 320 of the 512 TMEM
+// columns; every tile is two 64-dim boxes (the 128-byte swizzle spans 64
+// elements), QK takes 8 key-dim steps, P V two 64-column MMAs per key step,
+// with two K/V stages and plain output stores.
 // Every wait is bounded: on a timeout the CTA records PKA_DEVCHK_TIMEOUT,
 // every role stops, TMEM is freed, and the kernel returns.
 #include <cuda.h>
@@ -73,7 +78,7 @@ namespace {
 
 constexpr int BM = 128;        // query rows per tile = TMEM lanes = MMA M
 constexpr int BN = 128;        // keys per K/V tile
-constexpr int HD = 64;         // head dim
+constexpr int HD = 64;         // head dim of one 128-byte-swizzled box (a 64-dim tile, or half of a 128-dim one)
 constexpr int MAX_SEQS = 1024; // sequences per launch (the host splits larger batches)
 // Threads: the plain instances run 11 warps (producer, MMA of tile 0, 2 x 4
 // softmax warps, MMA of tile 1) at the 168 registers a thread that 3 warps on a
@@ -95,15 +100,18 @@ constexpr uint32_t TILE_BYTES = BM * HD * 2;             // 16 KB: one Q, K or V
 // instances stream one 2 KB box per cache block and keep a fourth tile in
 // flight (paged self- and cross-attention 4-5 % faster); the packed
 // instances keep three (a fourth slowed the window and T5 encoder layers).
-template <bool PAGED> constexpr int nstages() { return PAGED ? 4 : 3; }
+template <bool PAGED, int D = 64> constexpr int nstages() { return D == 128 ? 2 : PAGED ? 4 : 3; }
 constexpr uint32_t TAB_FLOATS = 2 * TILE_BYTES / 4;   // widened bias tables held in shared memory, at most
 // Layout<NS, TAB>: TAB gives the bias table a region of its own (else it
 // takes the output staging tiles' place and the outputs go out by plain stores)
-template <int NS, bool TAB> struct Layout {
+// D is the head dim: 64, or 128 with every tile two 64-dim boxes (32 KB), two
+// K/V stages and no staging tiles (outputs by plain stores).
+template <int NS, bool TAB, int D = 64> struct Layout {
+    static constexpr uint32_t TQ = BM * D * 2, TKV = BN * D * 2;    // bytes of a Q tile and of a K or V tile
     static constexpr uint32_t OFF_Q = 0;                             // 2 query tiles
-    static constexpr uint32_t OFF_KV = 2 * TILE_BYTES;               // NS x (K, V)
-    static constexpr uint32_t OFF_OST = OFF_KV + NS * 2 * TILE_BYTES;  // 2 output staging tiles (one per query tile)
-    static constexpr uint32_t OFF_BAR = OFF_OST + 2 * TILE_BYTES;
+    static constexpr uint32_t OFF_KV = 2 * TQ;                       // NS x (K, V)
+    static constexpr uint32_t OFF_OST = OFF_KV + NS * 2 * TKV;       // 2 output staging tiles (one per query tile)
+    static constexpr uint32_t OFF_BAR = OFF_OST + (D == 64 ? 2 * TILE_BYTES : 0);
     // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], s_empty[2], p_full[2], o_full[2],
     // o_empty[2], item ring full[2] / empty[2]
     static constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NS, B_SF = 2 + 2 * NS, B_SE = B_SF + 2,
@@ -196,6 +204,7 @@ struct Sched {
     const int *cum, *start, *len, *lenk, *seqid;
     int nseq, H, window, causal, chunk;
     bool paged;
+    int qt;                                            // query tiles per item: 2, or 1 at head dim 128
     __device__ __forceinline__ Item get(int t) const
     {
         int lo = 0, hi = nseq;                         // cum[lo] <= t < cum[hi]
@@ -209,16 +218,16 @@ struct Sched {
         I.Lk = paged ? lenk[lo] : I.L;
         I.seq = seqid[lo];
         I.qoff = I.Lk - I.L;
-        const int np = (I.L + 2 * BM - 1) / (2 * BM);
+        const int np = (I.L + qt * BM - 1) / (qt * BM);
         const int r = t - cum[lo];
         I.h = r / np;                                  // pairs of one head are neighbours: shared K/V in L2
-        I.r0 = (r - I.h * np) * 2 * BM;
+        I.r0 = (r - I.h * np) * qt * BM;
         int c_lo = 0x7fffffff, c_hi = -1;
         int lo_w[2], hi_w[2];
         for (int w = 0; w < 2; ++w) {
             lo_w[w] = 0; hi_w[w] = -1;
             const int a = I.r0 + w * BM;
-            if (a >= I.L) continue;
+            if (w >= qt || a >= I.L) continue;
             const int pa = a + I.qoff, pb = min(a + BM, I.L) - 1 + I.qoff;   // key positions of the tile's rows
             int kl = 0, kh = I.Lk - 1;
             if (chunk > 0) { kl = pa / chunk * chunk; kh = min(I.Lk - 1, pb / chunk * chunk + chunk - 1); }
@@ -332,17 +341,21 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
 // block tables (tm_k / tm_v are 4-D maps with one cache block per box);
 // otherwise from the packed [T, H, 64] keys of the same rows as the queries.
 // BIAS: the relative-position bias is added to the scores.
-template <typename T, bool PAGED, bool BIAS, bool BAND>
+template <typename T, bool PAGED, bool BIAS, bool BAND, int D>
 __global__ void __launch_bounds__(nthreads<PAGED || BIAS>(), 1)
 swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                       const Params P)
 {
     constexpr bool SPLIT = PAGED || BIAS;             // registers moved to the softmax warpgroups
-    constexpr int NS = nstages<PAGED>();
+    static_assert(D == 64 || (D == 128 && !PAGED && !BIAS), "head dim 128: packed keys, no bias");
+    constexpr bool WIDE = D == 128;                   // one query tile per item (TMEM: 128 S + 128 O columns)
+    constexpr int QT = WIDE ? 1 : 2;                  // query tiles per item
+    constexpr int NS = nstages<PAGED, D>();
     constexpr bool TAB = own_table<PAGED, BIAS>();
-    constexpr bool TMA_OUT = !BIAS || TAB;           // outputs through the staging tiles
-    using LY = Layout<NS, TAB>;
+    constexpr bool TMA_OUT = (!BIAS || TAB) && !WIDE;   // outputs through the staging tiles
+    using LY = Layout<NS, TAB, D>;
+    constexpr uint32_t TQ = LY::TQ, TKV = LY::TKV;
     constexpr uint32_t OFF_Q = LY::OFF_Q, OFF_KV = LY::OFF_KV, OFF_OST = LY::OFF_OST, OFF_BAR = LY::OFF_BAR,
                        OFF_MISC = LY::OFF_MISC, OFF_RING = LY::OFF_RING, OFF_SCHED = LY::OFF_SCHED;
     constexpr int B_QF = LY::B_QF, B_QE = LY::B_QE, B_KVF = LY::B_KVF, B_KVE = LY::B_KVE, B_SF = LY::B_SF,
@@ -436,7 +449,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const int per = (S + 31) / 32;
         const int a = min(lane * per, S), b = min(a + per, S);
         int local = 0;
-        for (int i = a; i < b; ++i) local += (len[i] + 2 * BM - 1) / (2 * BM) * P.H;
+        for (int i = a; i < b; ++i) local += (len[i] + QT * BM - 1) / (QT * BM) * P.H;
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -444,11 +457,11 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             if (lane >= o) incl += v;
         }
         int run = incl - local;
-        for (int i = a; i < b; ++i) { cum[i] = run; run += (len[i] + 2 * BM - 1) / (2 * BM) * P.H; }
+        for (int i = a; i < b; ++i) { cum[i] = run; run += (len[i] + QT * BM - 1) / (QT * BM) * P.H; }
         if (lane == 31) cum[S] = incl;
     }
     __syncthreads();
-    const Sched sched{cum, start, len, lenk, seqid, S, P.H, P.window, P.causal, P.chunk, PAGED};
+    const Sched sched{cum, start, len, lenk, seqid, S, P.H, P.window, P.causal, P.chunk, PAGED, QT};
     const int total_items = cum[S];
     const uint32_t tmem = *tmem_base_sm;
     // Items: CTA c takes item c, then items from a global counter one at a
@@ -508,10 +521,13 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             t = dyn ? (int)gridDim.x + (int)ahead : t + (int)gridDim.x;
             if (dyn && t < total_items) ahead = atomicAdd(P.items, 1u);
             if (!wait_or_abort(BAR(B_QE), (wq & 1) ^ 1, abort_flag, P.status)) break;
-            const bool two = I.r0 + BM < I.L;
-            mbar_arrive_expect_tx(BAR(B_QF), (two ? 2 : 1) * TILE_BYTES);
-            tc::tma_load_3d(sb + OFF_Q, &tm_q, 0, I.h, I.s0 + I.r0, BAR(B_QF));
-            if (two) tc::tma_load_3d(sb + OFF_Q + TILE_BYTES, &tm_q, 0, I.h, I.s0 + I.r0 + BM, BAR(B_QF));
+            const bool two = !WIDE && I.r0 + BM < I.L;
+            mbar_arrive_expect_tx(BAR(B_QF), (two ? 2 : 1) * TQ);
+#pragma unroll
+            for (int x = 0; x < D; x += HD) {          // a 128-dim tile is two 64-dim boxes, 16 KB apart
+                tc::tma_load_3d(sb + OFF_Q + x * 256, &tm_q, x, I.h, I.s0 + I.r0, BAR(B_QF));
+                if (two) tc::tma_load_3d(sb + OFF_Q + TQ + x * 256, &tm_q, x, I.h, I.s0 + I.r0 + BM, BAR(B_QF));
+            }
             bool ok = true;
             // paged: the block-table entries of key tile j + 1 are read while tile j
             // waits for its stage, so the table's latency leaves the copy path
@@ -533,7 +549,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 }
                 const uint32_t st = g % NS;
                 if (!wait_or_abort(BAR(B_KVE + st), ((g / NS) & 1) ^ 1, abort_flag, P.status)) { ok = false; break; }
-                const uint32_t dk = sb + OFF_KV + st * 2 * TILE_BYTES, dv = dk + TILE_BYTES;
+                const uint32_t dk = sb + OFF_KV + st * 2 * TKV, dv = dk + TKV;
                 if constexpr (PAGED) {
                     // the tile's cache blocks below k_end, one 16-row box each; a
                     // 2 KB box keeps the 1024-byte swizzle atoms of a contiguous tile
@@ -552,9 +568,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     }
                 } else {
                     const int row = I.s0 + I.c_lo + j * BN;
-                    mbar_arrive_expect_tx(BAR(B_KVF + st), 2 * TILE_BYTES);
-                    tc::tma_load_3d(dk, &tm_k, 0, I.h, row, BAR(B_KVF + st));
-                    tc::tma_load_3d(dv, &tm_v, 0, I.h, row, BAR(B_KVF + st));
+                    mbar_arrive_expect_tx(BAR(B_KVF + st), 2 * TKV);
+#pragma unroll
+                    for (int x = 0; x < D; x += HD) {
+                        tc::tma_load_3d(dk + x * 256, &tm_k, x, I.h, row, BAR(B_KVF + st));
+                        tc::tma_load_3d(dv + x * 256, &tm_v, x, I.h, row, BAR(B_KVF + st));
+                    }
                 }
             }
             if (!ok) break;
@@ -584,11 +603,13 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 const uint32_t c = cs + (j - I.jb[w]);
                 if (!wait_or_abort(BAR(B_SE + w), (c & 1) ^ 1, abort_flag, P.status)) return false;
                 tc::fence_after_sync();
-                const uint32_t qa = sb + OFF_Q + w * TILE_BYTES, ka = sb + OFF_KV + st * 2 * TILE_BYTES;
+                const uint32_t qa = sb + OFF_Q + w * TQ, ka = sb + OFF_KV + st * 2 * TKV;
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk)
-                    tc::mma_bf16(tmem + COL_S + w * BN, tc::sw128_desc(qa + kk * 32), tc::sw128_desc(ka + kk * 32),
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * TILE_BYTES + (kk & 3) * 32;   // box kk / 4, 16 dims in
+                    tc::mma_bf16(tmem + COL_S + w * BN, tc::sw128_desc(qa + off), tc::sw128_desc(ka + off),
                                  idesc_qk<T>(), kk > 0);
+                }
                 tc::commit(BAR(B_SF + w));
                 if (j == I.je[w]) tc::commit(BAR(B_QE));         // last read of Q_w in this item
                 return true;
@@ -604,11 +625,14 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 if (!wait_or_abort(BAR(B_PF + w), c & 1, abort_flag, P.status)) return false;
                 if (j == I.jb[w] && !wait_or_abort(BAR(B_OE + w), (co & 1) ^ 1, abort_flag, P.status)) return false;
                 tc::fence_after_sync();
-                const uint32_t va = sb + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES;
+                const uint32_t va = sb + OFF_KV + st * 2 * TKV + TKV;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    tc::mma_bf16_ta(tmem + COL_O + w * HD, tmem + COL_P + w * (BN / 2) + kk * 8,
-                                    tc::sw128_desc(va + kk * 2048), idesc_pv<T>(), kk > 0 || j > I.jb[w]);
+                for (int nh = 0; nh < D / HD; ++nh)          // the O columns of each 64-dim box of V
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        tc::mma_bf16_ta(tmem + COL_O + w * D + nh * HD, tmem + COL_P + w * (BN / 2) + kk * 8,
+                                        tc::sw128_desc(va + nh * TILE_BYTES + kk * 2048), idesc_pv<T>(),
+                                        kk > 0 || j > I.jb[w]);
                 tc::commit(BAR(B_OF + w));
                 tc::commit(BAR(B_KVE + st));
                 return true;
@@ -639,7 +663,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const int row = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_addr + COL_S + w * BN;
-        const uint32_t tO = tmem + lane_addr + COL_O + w * HD;
+        const uint32_t tO = tmem + lane_addr + COL_O + w * D;
         const uint32_t tP = tmem + lane_addr + COL_P + w * (BN / 2);
         uint32_t cs = 0, co = 0, g = 0;
         for (uint32_t kq = 0;; ++kq) {
@@ -696,7 +720,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     // past the context (any bits): zero them so that P = 0 there
                     // contributes exactly nothing to P V
                     if (row >= I.k_end() - c0) {
-                        const uint32_t vrow = sb + OFF_KV + ((g_item + j) % NS) * 2 * TILE_BYTES + TILE_BYTES + row * 128;
+                        const uint32_t vrow = sb + OFF_KV + ((g_item + j) % NS) * 2 * TKV + TKV + row * 128;
 #pragma unroll
                         for (int c = 0; c < 8; ++c)
                             asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + c * 16), "r"(0)
@@ -789,11 +813,14 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 if (j > I.jb(w) && __any_sync(kFull, raise)) {
                     // the running max rose: bring this row's O to the new max (in TMEM)
                     const float c = raise ? ex2(m_old - m) : 1.f;
-                    float o[HD];
-                    tc::tmem_ld64(tO, o);
 #pragma unroll
-                    for (int i = 0; i < HD; ++i) o[i] *= c;
-                    tc::tmem_st64(tO, o);
+                    for (int x = 0; x < D; x += HD) {
+                        float o[HD];
+                        tc::tmem_ld64(tO + x, o);
+#pragma unroll
+                        for (int i = 0; i < HD; ++i) o[i] *= c;
+                        tc::tmem_st64(tO + x, o);
+                    }
                 }
                 if constexpr (PAGED) fence_proxy_async();   // zeroed V rows are read by the tensor cores
                 tc::fence_before_sync();               // orders P and the O rescale before the next P V
@@ -803,8 +830,9 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             // all key tiles done: read O, free the O columns, normalise, store
             if (!wait_or_abort(BAR(B_OF + w), (cs - 1) & 1, abort_flag, P.status)) break;
             tc::fence_after_sync();
-            float o[HD];
+            float o[D];
             tc::tmem_ld64(tO, o);
+            if constexpr (D == 128) tc::tmem_ld64(tO + HD, o + HD);
             tc::fence_before_sync();
             mbar_arrive(BAR(B_OE + w));
             ++co;
@@ -835,9 +863,9 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 }
             } else if (rr < I.L()) {
                 // plain stores of the rows inside the sequence (its last, partial tile)
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) + ((size_t)(I.s0() + rr) * P.H + I.h()) * HD);
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) + ((size_t)(I.s0() + rr) * P.H + I.h()) * D);
 #pragma unroll
-                for (int c = 0; c < HD / 8; ++c) {
+                for (int c = 0; c < D / 8; ++c) {
                     float v[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) v[e] = o[c * 8 + e] * inv;
@@ -970,13 +998,13 @@ EncodeTiledFn encode_fn()
 }
 
 // [T, H, 64] bf16 rows -> boxes of 128 tokens x 64 dims of one head, 128-byte swizzle
-bool make_map(CUtensorMap *m, const void *base, int T, int H, CUtensorMapDataType dt, int rows = BM)
+bool make_map(CUtensorMap *m, const void *base, int T, int H, CUtensorMapDataType dt, int rows = BM, int d = HD)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)H, (cuuint64_t)T};
-    const cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)H * HD * 2};
-    const cuuint32_t box[3] = {HD, 1, (cuuint32_t)rows};
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+    const cuuint32_t box[3] = {HD, 1, (cuuint32_t)rows};   // 64 dims (128 bytes, the swizzle span) per box
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -998,13 +1026,14 @@ bool make_paged_map(CUtensorMap *m, const void *base, int num_blocks, int H, CUt
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, bool PAGED, bool BIAS, bool BAND>
+template <typename T, bool PAGED, bool BIAS, bool BAND, int D = 64>
 cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
                        Params P, const PrefillArgs &a, int sms, cudaStream_t stream)
 {
-    auto kern = swa_prefill_tc_kernel<T, PAGED, BIAS, BAND>;
+    auto kern = swa_prefill_tc_kernel<T, PAGED, BIAS, BAND, D>;
     constexpr bool SPLIT = PAGED || BIAS;
-    constexpr uint32_t SMEM_BYTES = Layout<nstages<PAGED>(), own_table<PAGED, BIAS>()>::SMEM_BYTES;
+    constexpr uint32_t SMEM_BYTES = Layout<nstages<PAGED, D>(), own_table<PAGED, BIAS>(), D>::SMEM_BYTES;
+    constexpr int QT = D == 128 ? 1 : 2;              // query tiles per item
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [&] {
@@ -1027,7 +1056,7 @@ cudaError_t launch_cfg(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
             P.context_lens = a.context_lens + base;
             P.block_tables = a.block_tables + (size_t)base * a.mbps;
         }
-        const long long tiles_upper = (long long)P.num_seqs * ((a.max_seqlen + 2 * BM - 1) / (2 * BM)) * a.num_heads;
+        const long long tiles_upper = (long long)P.num_seqs * ((a.max_seqlen + QT * BM - 1) / (QT * BM)) * a.num_heads;
         const int grid = (int)std::max<long long>(1, std::min<long long>(sms, tiles_upper));
         if (!next_item_counters(stream, &P.items)) return cudaErrorInvalidDevice;
         kern<<<grid, nthreads<SPLIT>(), SMEM_BYTES, stream>>>(mq, mk, mv, mo, P);
@@ -1048,6 +1077,9 @@ cudaError_t dispatch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtenso
     // classifies 32-key chunks (a third of a window item's chunks are kept by no
     // row of the warp); full, chunked and causal attention keep the plain one,
     // where few tiles are masked and the extra code costs more than it saves
+    if (a.head_dim == 128)
+        return a.window > 0 ? launch_cfg<T, false, false, true, 128>(mq, mk, mv, mo, P, a, sms, stream)
+                            : launch_cfg<T, false, false, false, 128>(mq, mk, mv, mo, P, a, sms, stream);
     if (a.window > 0) return launch_cfg<T, false, false, true>(mq, mk, mv, mo, P, a, sms, stream);
     return launch_cfg<T, false, false, false>(mq, mk, mv, mo, P, a, sms, stream);
 }
@@ -1056,18 +1088,22 @@ cudaError_t dispatch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtenso
 
 cudaError_t launch_swa_prefill(const PrefillArgs &a, cudaStream_t stream)
 {
-    if (a.head_dim != HD) return cudaErrorInvalidValue;
     const bool paged = a.block_tables != nullptr;
+    // head dim 64, or 128 for packed keys without bias
+    if (a.head_dim != HD && !(a.head_dim == 128 && !paged && a.rel_bias == nullptr)) return cudaErrorInvalidValue;
+    const int d = a.head_dim;
     const CUtensorMapDataType dt =
         a.dtype == PKA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, a.q, a.num_tokens, a.num_heads, dt) || !make_map(&mo, a.out, a.num_tokens, a.num_heads, dt, 32))
+    if (!make_map(&mq, a.q, a.num_tokens, a.num_heads, dt, BM, d) ||
+        !make_map(&mo, a.out, a.num_tokens, a.num_heads, dt, 32, d))
         return cudaErrorInvalidValue;
     if (paged) {
         if (!make_paged_map(&mk, a.k, a.num_blocks, a.num_heads, dt) ||
             !make_paged_map(&mv, a.v, a.num_blocks, a.num_heads, dt))
             return cudaErrorInvalidValue;
-    } else if (!make_map(&mk, a.k, a.num_tokens, a.num_heads, dt) || !make_map(&mv, a.v, a.num_tokens, a.num_heads, dt)) {
+    } else if (!make_map(&mk, a.k, a.num_tokens, a.num_heads, dt, BN, d) ||
+               !make_map(&mv, a.v, a.num_tokens, a.num_heads, dt, BN, d)) {
         return cudaErrorInvalidValue;
     }
     int dev = 0, sms = 148;

@@ -94,6 +94,12 @@ def test_reshape_and_prefill_argument_checks_need_no_gpu(lib):
     assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, 0.125, 0, NULL, NULL) == pka.PKA_ERR_UNSUPPORTED
     assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, 0.125, 1, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
     assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, 0.125, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
+    # head dim 128 is taken by the packed prefill (NULL buffers: an argument error), 96 is not
+    assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 128, -1, 0, 0.125, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
+    assert p(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 96, -1, 0, 0.125, 2, NULL, NULL) == pka.PKA_ERR_UNSUPPORTED
+    c = lib.pka_chunked_prefill
+    assert c(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 128, 64, 0, 0.125, 2, NULL, NULL) == pka.PKA_ERR_INVALID_ARG
+    assert c(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 96, 64, 0, 0.125, 2, NULL, NULL) == pka.PKA_ERR_UNSUPPORTED
 
 
 def test_product_path_refuses_to_run_without_the_library(monkeypatch, tmp_path):
@@ -180,6 +186,8 @@ def test_biased_and_paged_prefill_argument_checks_need_no_gpu(lib):
         pka.PKA_ERR_INVALID_ARG                                                    # f16 accepted; NULL buffers
     assert b(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 64, -1, 0, fake, 4, 0.125, 2, NULL, NULL) == \
         pka.PKA_ERR_INVALID_ARG                                                    # NULL buffers
+    assert b(NULL, NULL, NULL, NULL, NULL, 1, 5, 5, 12, 128, -1, 0, fake, 4, 0.125, 2, NULL, NULL) == \
+        pka.PKA_ERR_UNSUPPORTED                                                    # head dim 128: bias not built
     p = lib.pka_paged_prefill
 
     def paged(**kw):

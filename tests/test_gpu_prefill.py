@@ -439,3 +439,40 @@ def test_prefill_more_sequences_than_one_launch(cuda_lib):
     got = to_f64(gp.run(), BF16)
     _check(got, oracle_paged(gp), "1300 sequences paged")
     assert int(gp.status.item()) == 0
+
+
+# ---------------------------------------------------------------------------
+# head dim 128 (packed keys, no bias): one query tile per work item
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("window", [-1, 1, 63, 64, 65, 128, 300])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_prefill_head_dim_128_parity(cuda_lib, window, causal):
+    lens = [1, 2, 127, 128, 129, 255, 300, 513]
+    case = synth.make_prefill_case("d128", 800 + max(window, 0) + causal, lens, 3, 128, window, causal, BF16,
+                                   scale=128 ** -0.5)
+    got = to_f64(run_gpu_prefill(cuda_lib, case), BF16)
+    ref = oracle.prefill(case.q, case.k, case.v, case.cu_seqlens, window, causal, case.scale, BF16)
+    _check(got, ref, f"D=128 W={window} causal={causal}")
+
+
+@pytest.mark.parametrize("chunk", [1, 100, 128, 256])
+def test_chunked_prefill_head_dim_128_parity(cuda_lib, chunk):
+    lens = [1, 2, 127, 128, 129, 255, 300, 513]
+    case = synth.make_prefill_case("d128-chunk", 820 + chunk, lens, 3, 128, -1, 1, BF16, scale=128 ** -0.5)
+    case.chunk = chunk
+    got = to_f64(run_gpu_chunked(cuda_lib, case), BF16)
+    ref = oracle.prefill_chunked(case.q, case.k, case.v, case.cu_seqlens, chunk, 1, case.scale, BF16)
+    _check(got, ref, f"D=128 chunk={chunk}")
+
+
+def test_prefill_head_dim_128_f16_and_long_sequences(cuda_lib):
+    """f16 at head dim 128 on ragged lengths up to 1300 (up to 11 key tiles per
+    query tile: the running max is raised and O rescaled in TMEM), full and
+    window 64; every row against the oracle."""
+    lens = [1, 700, 1300]
+    for window in (-1, 64):
+        case = synth.make_prefill_case("d128-f16", 840 + max(window, 0), lens, 2, 128, window, 0, F16,
+                                       scale=128 ** -0.5)
+        got = to_f64(run_gpu_prefill(cuda_lib, case), F16)
+        ref = oracle.prefill(case.q, case.k, case.v, case.cu_seqlens, window, 0, case.scale, F16)
+        _check(got, ref, f"f16 D=128 W={window}", F16)
