@@ -57,8 +57,10 @@
 // Head dim 128 (packed keys, no bias): a work item is one query tile with one
 // softmax warpgroup, since S, O and P of a tile take 320 of the 512 TMEM
 // columns; every tile is two 64-dim boxes (the 128-byte swizzle spans 64
-// elements), QK takes 8 key-dim steps, P V two 64-column MMAs per key step,
-// with two K/V stages and plain output stores.
+// elements), QK takes 8 key-dim steps, P V two 64-column MMAs per key step.
+// K and V stream into separate slots (three K, two V), each freed by its own
+// MMA, so loads run two key tiles ahead; with a banded mask P alternates
+// between two TMEM buffers; outputs leave by plain stores.
 // Every wait is bounded: on a timeout the CTA records PKA_DEVCHK_TIMEOUT,
 // every role stops, TMEM is freed, and the kernel returns.
 #include <cuda.h>
@@ -100,23 +102,27 @@ constexpr uint32_t TILE_BYTES = BM * HD * 2;             // 16 KB: one Q, K or V
 // instances stream one 2 KB box per cache block and keep a fourth tile in
 // flight (paged self- and cross-attention 4-5 % faster); the packed
 // instances keep three (a fourth slowed the window and T5 encoder layers).
-template <bool PAGED, int D = 64> constexpr int nstages() { return D == 128 ? 2 : PAGED ? 4 : 3; }
+// At head dim 128 the "stages" are five 32 KB slots: three for K, two for V
+// (K and V released separately: a K slot once its QK is done, a V slot once
+// its P V is done), so each streams two key tiles ahead of its use.
+template <bool PAGED, int D = 64> constexpr int nstages() { return D == 128 ? 5 : PAGED ? 4 : 3; }
+constexpr int KSLOTS_128 = 3, VSLOTS_128 = 2;
 constexpr uint32_t TAB_FLOATS = 2 * TILE_BYTES / 4;   // widened bias tables held in shared memory, at most
 // Layout<NS, TAB>: TAB gives the bias table a region of its own (else it
 // takes the output staging tiles' place and the outputs go out by plain stores)
-// D is the head dim: 64, or 128 with every tile two 64-dim boxes (32 KB), two
-// K/V stages and no staging tiles (outputs by plain stores).
+// D is the head dim: 64, or 128 with every tile two 64-dim boxes (32 KB), one
+// query tile, 3 K + 2 V slots and no staging tiles (outputs by plain stores).
 template <int NS, bool TAB, int D = 64> struct Layout {
     static constexpr uint32_t TQ = BM * D * 2, TKV = BN * D * 2;    // bytes of a Q tile and of a K or V tile
-    static constexpr uint32_t OFF_Q = 0;                             // 2 query tiles
-    static constexpr uint32_t OFF_KV = 2 * TQ;                       // NS x (K, V)
-    static constexpr uint32_t OFF_OST = OFF_KV + NS * 2 * TKV;       // 2 output staging tiles (one per query tile)
+    static constexpr uint32_t OFF_Q = 0;                             // 2 query tiles (1 at head dim 128)
+    static constexpr uint32_t OFF_KV = (D == 128 ? 1 : 2) * TQ;      // NS x (K, V), or the K and V slots
+    static constexpr uint32_t OFF_OST = OFF_KV + (D == 128 ? NS : 2 * NS) * TKV;   // 2 output staging tiles
     static constexpr uint32_t OFF_BAR = OFF_OST + (D == 64 ? 2 * TILE_BYTES : 0);
     // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], s_empty[2], p_full[2], o_full[2],
     // o_empty[2], item ring full[2] / empty[2]
     static constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NS, B_SF = 2 + 2 * NS, B_SE = B_SF + 2,
                          B_PF = B_SE + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_IF = B_OE + 2, B_IE = B_IF + 2,
-                         NBAR = B_IE + 2;
+                         B_PE = B_IE + 2, NBAR = B_IE + 2 + (D == 128 ? 2 : 0);   // p_empty[2] at 128
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, abort flag, item ring [2]
     static constexpr uint32_t OFF_RING = (OFF_MISC + 16 + 127) / 128 * 128;   // the two ring entries' items (64 B each)
     static constexpr uint32_t OFF_SCHED = OFF_RING + 128;
@@ -134,7 +140,8 @@ constexpr int CBS = 16;                   // paged cache block: 16 key rows of o
 constexpr uint32_t CBLK_BYTES = CBS * HD * 2;                                  // 2 KB per block and head
 
 // TMEM columns of query tile w: S (f32) at 128 w, O (f32) at 256 + 64 w, P
-// (bf16 pairs) at 384 + 64 w: the 512 columns exactly
+// (bf16 pairs) at 384 + 64 w: the 512 columns exactly.  At head dim 128 (one
+// tile): S at 0, O at 256..383, P at 384 (and 448 for a second P buffer)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_O = 256, COL_P = 384;
 
@@ -351,6 +358,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     static_assert(D == 64 || (D == 128 && !PAGED && !BIAS), "head dim 128: packed keys, no bias");
     constexpr bool WIDE = D == 128;                   // one query tile per item (TMEM: 128 S + 128 O columns)
     constexpr int QT = WIDE ? 1 : 2;                  // query tiles per item
+    // P in two TMEM buffers (the second query tile's columns are free at head
+    // dim 128): the softmax writes P of key tile j while P V of tile j - 1 still
+    // reads the other one.  Kept for the banded masks only (window 64 layer
+    // 0.586 -> 0.551 ms), since full attention measured slower with it
+    // (6.74 -> 7.08 ms)
+    constexpr bool PDB = WIDE && BAND;
     constexpr int NS = nstages<PAGED, D>();
     constexpr bool TAB = own_table<PAGED, BIAS>();
     constexpr bool TMA_OUT = (!BIAS || TAB) && !WIDE;   // outputs through the staging tiles
@@ -360,7 +373,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                        OFF_MISC = LY::OFF_MISC, OFF_RING = LY::OFF_RING, OFF_SCHED = LY::OFF_SCHED;
     constexpr int B_QF = LY::B_QF, B_QE = LY::B_QE, B_KVF = LY::B_KVF, B_KVE = LY::B_KVE, B_SF = LY::B_SF,
                   B_SE = LY::B_SE, B_PF = LY::B_PF, B_OF = LY::B_OF, B_OE = LY::B_OE, B_IF = LY::B_IF, B_IE = LY::B_IE,
-                  NBAR = LY::NBAR;
+                  B_PE = LY::B_PE, NBAR = LY::NBAR;
     constexpr int NTHREADS = nthreads<SPLIT>();
     constexpr int SOFTMAX_WARP0 = SPLIT ? 4 : 2;      // the 8 softmax warps follow
     constexpr int MMA1_WARP = SPLIT ? 2 : NTHREADS / 32 - 1;   // issues the MMAs of query tile 1
@@ -540,12 +553,38 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             };
             int ids_next[BN / CBS];
             if constexpr (PAGED) read_table(ids_next, 0);
+            // head dim 128: V of key tile number gv (global count) into its V slot
+            auto load_v = [&](uint32_t gv, int row) -> bool {
+                const uint32_t vs = KSLOTS_128 + gv % VSLOTS_128;
+                if (!wait_or_abort(BAR(B_KVE + vs), ((gv / VSLOTS_128) & 1) ^ 1, abort_flag, P.status)) return false;
+                mbar_arrive_expect_tx(BAR(B_KVF + vs), TKV);
+#pragma unroll
+                for (int x = 0; x < D; x += HD)
+                    tc::tma_load_3d(sb + OFF_KV + vs * TKV + x * 256, &tm_v, x, I.h, row, BAR(B_KVF + vs));
+                return true;
+            };
             for (int j = 0; j < I.nkv; ++j, ++g) {
                 int phys[BN / CBS];
                 if constexpr (PAGED) {
 #pragma unroll
                     for (int b = 0; b < BN / CBS; ++b) phys[b] = ids_next[b];
                     if (j + 1 < I.nkv) read_table(ids_next, j + 1);
+                }
+                if constexpr (WIDE) {
+                    // K of key tile j, then V of key tile j - 1 (V one tile behind, so a
+                    // K slot never waits for a V slot to drain)
+                    const uint32_t kslot = g % KSLOTS_128;
+                    if (!wait_or_abort(BAR(B_KVE + kslot), ((g / KSLOTS_128) & 1) ^ 1, abort_flag, P.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const int row = I.s0 + I.c_lo + j * BN;
+                    mbar_arrive_expect_tx(BAR(B_KVF + kslot), TKV);
+#pragma unroll
+                    for (int x = 0; x < D; x += HD)
+                        tc::tma_load_3d(sb + OFF_KV + kslot * TKV + x * 256, &tm_k, x, I.h, row, BAR(B_KVF + kslot));
+                    if (j > 0 && !load_v(g - 1, row - BN)) { ok = false; break; }
+                    continue;
                 }
                 const uint32_t st = g % NS;
                 if (!wait_or_abort(BAR(B_KVE + st), ((g / NS) & 1) ^ 1, abort_flag, P.status)) { ok = false; break; }
@@ -576,6 +615,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     }
                 }
             }
+            if (WIDE && ok && I.nkv > 0 && !load_v(g - 1, I.s0 + I.c_lo + (I.nkv - 1) * BN)) ok = false;
             if (!ok) break;
         }
     };
@@ -597,7 +637,32 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             if (!mine) mbar_arrive(BAR(B_QE));
             // S_w = Q_w K_j^T, when query tile w needs key tile j
             auto issue_qk = [&](int j) -> bool {
-                const uint32_t gg = g + j, st = gg % NS;
+                const uint32_t gg = g + j;
+                if constexpr (WIDE) {
+                    // key tile j's K slot; released once this QK is done (or at once
+                    // by the thread whose query tile does not use it)
+                    const uint32_t ks = gg % KSLOTS_128;
+                    if (!wait_or_abort(BAR(B_KVF + ks), (gg / KSLOTS_128) & 1, abort_flag, P.status)) return false;
+                    if (j < I.jb[w] || j > I.je[w]) {
+                        mbar_arrive(BAR(B_KVE + ks));
+                        return true;
+                    }
+                    const uint32_t c = cs + (j - I.jb[w]);
+                    if (!wait_or_abort(BAR(B_SE + w), (c & 1) ^ 1, abort_flag, P.status)) return false;
+                    tc::fence_after_sync();
+                    const uint32_t qa = sb + OFF_Q + w * TQ, ka = sb + OFF_KV + ks * TKV;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * TILE_BYTES + (kk & 3) * 32;
+                        tc::mma_bf16(tmem + COL_S + w * BN, tc::sw128_desc(qa + off), tc::sw128_desc(ka + off),
+                                     idesc_qk<T>(), kk > 0);
+                    }
+                    tc::commit(BAR(B_SF + w));
+                    tc::commit(BAR(B_KVE + ks));
+                    if (j == I.je[w]) tc::commit(BAR(B_QE));
+                    return true;
+                }
+                const uint32_t st = gg % NS;
                 if (!wait_or_abort(BAR(B_KVF + st), (gg / NS) & 1, abort_flag, P.status)) return false;
                 if (j < I.jb[w] || j > I.je[w]) return true;
                 const uint32_t c = cs + (j - I.jb[w]);
@@ -616,7 +681,11 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             };
             // O_w += P_w V_j, then release the K/V stage (or just release it)
             auto issue_pv = [&](int j) -> bool {
-                const uint32_t st = (g + j) % NS;
+                // head dim 128: key tile j's V slot (filled after its K: wait for it
+                // here), released once this P V is done
+                const uint32_t st = WIDE ? KSLOTS_128 + (g + j) % VSLOTS_128 : (g + j) % NS;
+                if (WIDE && !wait_or_abort(BAR(B_KVF + st), ((g + j) / VSLOTS_128) & 1, abort_flag, P.status))
+                    return false;
                 if (j < I.jb[w] || j > I.je[w]) {
                     mbar_arrive(BAR(B_KVE + st));
                     return true;
@@ -625,15 +694,17 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 if (!wait_or_abort(BAR(B_PF + w), c & 1, abort_flag, P.status)) return false;
                 if (j == I.jb[w] && !wait_or_abort(BAR(B_OE + w), (co & 1) ^ 1, abort_flag, P.status)) return false;
                 tc::fence_after_sync();
-                const uint32_t va = sb + OFF_KV + st * 2 * TKV + TKV;
+                const uint32_t va = WIDE ? sb + OFF_KV + st * TKV : sb + OFF_KV + st * 2 * TKV + TKV;
 #pragma unroll
                 for (int nh = 0; nh < D / HD; ++nh)          // the O columns of each 64-dim box of V
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        tc::mma_bf16_ta(tmem + COL_O + w * D + nh * HD, tmem + COL_P + w * (BN / 2) + kk * 8,
+                        tc::mma_bf16_ta(tmem + COL_O + w * D + nh * HD,
+                                        tmem + COL_P + (PDB ? (c & 1) : w) * (BN / 2) + kk * 8,
                                         tc::sw128_desc(va + nh * TILE_BYTES + kk * 2048), idesc_pv<T>(),
                                         kk > 0 || j > I.jb[w]);
                 tc::commit(BAR(B_OF + w));
+                if constexpr (PDB) tc::commit(BAR(B_PE + (c & 1)));   // the P buffer is free again
                 tc::commit(BAR(B_KVE + st));
                 return true;
             };
@@ -801,7 +872,15 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 const bool raise = mt > m + RESCALE_LOG2;
                 const float m_old = m;
                 if (raise) m = mt;
-                if (j > I.jb(w)) {
+                if constexpr (PDB) {
+                    // P alternates between two buffers; the one written now is free
+                    // once the P V two key tiles back has read it
+                    if (!wait_or_abort(BAR(B_PE + (cs & 1)), ((cs >> 1) & 1) ^ 1, abort_flag, P.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                } else if (j > I.jb(w)) {
                     // P V of the previous key tile is done: P may be overwritten, O rescaled
                     if (!wait_or_abort(BAR(B_OF + w), (cs - 1) & 1, abort_flag, P.status)) { ok = false; break; }
                     tc::fence_after_sync();
@@ -809,9 +888,14 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 if (raise) l *= ex2(m_old - m);
                 // P = 2^(scale * s - m) as bf16 into the swizzled buffer; row sum in f32
                 const float mneg = (m == -INFINITY ? 0.f : -m) + boff;
-                l += write_p_tmem<T, BAND>(x, P.scale_log2, mneg, tP, dead);
+                l += write_p_tmem<T, BAND>(x, P.scale_log2, mneg, PDB ? tP + (cs & 1) * (BN / 2) : tP, dead);
                 if (j > I.jb(w) && __any_sync(kFull, raise)) {
                     // the running max rose: bring this row's O to the new max (in TMEM)
+                    if (PDB) {
+                        // (P double-buffered) once the previous key tile's P V is done
+                        if (!wait_or_abort(BAR(B_OF + w), (cs - 1) & 1, abort_flag, P.status)) { ok = false; break; }
+                        tc::fence_after_sync();
+                    }
                     const float c = raise ? ex2(m_old - m) : 1.f;
 #pragma unroll
                     for (int x = 0; x < D; x += HD) {
@@ -827,8 +911,15 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 mbar_arrive(BAR(B_PF + w));
             }
             if (!ok) break;
-            // all key tiles done: read O, free the O columns, normalise, store
-            if (!wait_or_abort(BAR(B_OF + w), (cs - 1) & 1, abort_flag, P.status)) break;
+            // all key tiles done: read O, free the O columns, normalise, store.  With
+            // P double-buffered the softmax skips the o_full waits of tiles without
+            // a rescale, so o_full may still be two phases short here and its parity
+            // would alias: the last tile's p_empty phase, committed after its P V,
+            // is exact (the P V two tiles back is known done)
+            const uint32_t lt = cs - 1;
+            if (!(PDB ? wait_or_abort(BAR(B_PE + (lt & 1)), (lt >> 1) & 1, abort_flag, P.status)
+                       : wait_or_abort(BAR(B_OF + w), lt & 1, abort_flag, P.status)))
+                break;
             tc::fence_after_sync();
             float o[D];
             tc::tmem_ld64(tO, o);
