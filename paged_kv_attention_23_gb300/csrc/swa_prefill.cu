@@ -324,22 +324,31 @@ __device__ __forceinline__ float write_p_tmem(const float *x, float scale_log2, 
 
 // The same P for one tile row into registers (pk[c] = keys 2c, 2c + 1), the
 // TMEM stores left to the caller; returns the f32 row sum
-template <typename T>
-__device__ __forceinline__ float exp_pack(const float *x, float scale_log2, float mneg, uint32_t *pk)
+template <typename T, bool SKIP>
+__device__ __forceinline__ float exp_pack(const float *x, float scale_log2, float mneg, uint32_t *pk, uint32_t dead)
 {
     float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int c = 0; c < BN / 2; ++c) {
-        float a0, a1;
-        fma2(x[2 * c], x[2 * c + 1], scale_log2, mneg, a0, a1);
-        const float p0 = ex2(a0), p1 = ex2(a1);
-        add2(ls[(c & 1) * 2], ls[(c & 1) * 2 + 1], p0, p1);
-        if constexpr (is_bf16<T>()) {
-            __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
-            pk[c] = *reinterpret_cast<uint32_t *>(&hb);
-        } else {
-            __half2 hh = __floats2half2_rn(p0, p1);
-            pk[c] = *reinterpret_cast<uint32_t *>(&hh);
+    for (int q4 = 0; q4 < 4; ++q4) {
+        if (SKIP && ((dead >> q4) & 1u)) {
+#pragma unroll
+            for (int c = 0; c < BN / 8; ++c) pk[q4 * (BN / 8) + c] = 0u;
+            continue;
+        }
+#pragma unroll
+        for (int c = 0; c < BN / 8; ++c) {
+            const int i = q4 * (BN / 4) + 2 * c;
+            float a0, a1;
+            fma2(x[i], x[i + 1], scale_log2, mneg, a0, a1);
+            const float p0 = ex2(a0), p1 = ex2(a1);
+            add2(ls[(c & 1) * 2], ls[(c & 1) * 2 + 1], p0, p1);
+            if constexpr (is_bf16<T>()) {
+                __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
+                pk[q4 * (BN / 8) + c] = *reinterpret_cast<uint32_t *>(&hb);
+            } else {
+                __half2 hh = __floats2half2_rn(p0, p1);
+                pk[q4 * (BN / 8) + c] = *reinterpret_cast<uint32_t *>(&hh);
+            }
         }
     }
     return (ls[0] + ls[1]) + (ls[2] + ls[3]);
@@ -387,12 +396,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     // 0.586 -> 0.551 ms), since full attention measured slower with it
     // (6.74 -> 7.08 ms)
     constexpr bool PDB = WIDE && BAND;
-    // full, chunked and causal attention at head dim 64 (packed keys, no bias):
-    // a key tile's exponentials run before the wait for the previous tile's
-    // P V, P held in registers until then (full-attention layer 1.737 ->
-    // 1.638 ms; chunked unchanged; 1 % slower at head dim 128, which keeps
-    // the stores inside the exponential loop)
-    constexpr bool EARLYP = !PAGED && !BIAS && !BAND && !WIDE;
+    // no bias, head dim 64: a key tile's exponentials run before the wait for
+    // the previous tile's P V, P held in registers until then (full-attention
+    // layer 1.737 -> 1.638 ms, window-64 layer 0.161 -> 0.157 ms, paged
+    // cross-attention 0.181 -> 0.178 ms; chunked unchanged).  The bias
+    // instances measured slightly slower with it, and head dim 128 1 % slower
+    constexpr bool EARLYP = !BIAS && !WIDE;
     constexpr int NS = nstages<PAGED, D>();
     constexpr bool TAB = own_table<PAGED, BIAS>();
     constexpr bool TMA_OUT = (!BIAS || TAB) && !WIDE;   // outputs through the staging tiles
@@ -919,7 +928,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 const float mneg = (m == -INFINITY ? 0.f : -m) + boff;
                 if constexpr (EARLYP) {
                     uint32_t pk[BN / 2];
-                    l += exp_pack<T>(x, P.scale_log2, mneg, pk);
+                    l += exp_pack<T, BAND>(x, P.scale_log2, mneg, pk, dead);
                     if (j > I.jb(w)) {
                         if (!wait_or_abort(BAR(B_OF + w), (cs - 1) & 1, abort_flag, P.status)) { ok = false; break; }
                         tc::fence_after_sync();
