@@ -402,6 +402,11 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     // cross-attention 0.181 -> 0.178 ms; chunked unchanged).  The bias
     // instances measured slightly slower with it, and head dim 128 1 % slower
     constexpr bool EARLYP = !BIAS && !WIDE;
+    // a row of S (and at head dim 128 of O) read from TMEM by one 128-column
+    // load and one wait on the bias instances and the full-attention instance at
+    // head dim 128 (T5 encoder 0.373 -> 0.369 ms); the other instances spill
+    // more with it and measured 1-5 % slower, and keep two 64-column loads
+    constexpr bool LD128 = BIAS || (WIDE && !BAND);
     constexpr int NS = nstages<PAGED, D>();
     constexpr bool TAB = own_table<PAGED, BIAS>();
     constexpr bool TMA_OUT = (!BIAS || TAB) && !WIDE;   // outputs through the staging tiles
@@ -819,8 +824,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 if (!wait_or_abort(BAR(B_SF + w), cs & 1, abort_flag, P.status)) { ok = false; break; }
                 tc::fence_after_sync();
                 float x[BN];
-                tc::tmem_ld64(tS, x);
-                tc::tmem_ld64(tS + 64, x + 64);
+                if constexpr (LD128) {
+                    tc::tmem_ld128(tS, x);
+                } else {
+                    tc::tmem_ld64(tS, x);
+                    tc::tmem_ld64(tS + 64, x + 64);
+                }
                 tc::fence_before_sync();
                 mbar_arrive(BAR(B_SE + w));            // S columns free: QK of the next key tile may start
                 const int c0 = I.c_lo() + j * BN;
@@ -971,8 +980,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 break;
             tc::fence_after_sync();
             float o[D];
-            tc::tmem_ld64(tO, o);
-            if constexpr (D == 128) tc::tmem_ld64(tO + HD, o + HD);
+            if constexpr (D == 128 && LD128) {
+                tc::tmem_ld128(tO, o);
+            } else {
+                tc::tmem_ld64(tO, o);
+                if constexpr (D == 128) tc::tmem_ld64(tO + HD, o + HD);
+            }
             tc::fence_before_sync();
             mbar_arrive(BAR(B_OE + w));
             ++co;
