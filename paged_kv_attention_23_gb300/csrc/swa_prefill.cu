@@ -553,53 +553,85 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 
     auto producer = [&]() {
         // ======================= TMA producer =======================
-        tc::prefetch_tensormap(&tm_q);
-        tc::prefetch_tensormap(&tm_k);
-        tc::prefetch_tensormap(&tm_v);
-        tc::prefetch_tensormap(&tm_o);
+        // Paged keys: the whole warp runs the producer, lane 0 doing every wait,
+        // arrival and item hand-out and each of lanes 0-15 issuing one cache
+        // block's K or V box of a key tile (16 boxes a tile, issued at once
+        // instead of one after another by one thread).  Otherwise one thread.
+        constexpr bool WP = PAGED;
+        const bool lead = !WP || lane == 0;
+        auto wwait = [&](uint32_t bar, uint32_t parity) -> bool {
+            if constexpr (WP) {
+                int r = 1;
+                if (lane == 0) r = wait_or_abort(bar, parity, abort_flag, P.status) ? 1 : 0;
+                return __shfl_sync(kFull, r, 0) != 0;
+            } else {
+                return wait_or_abort(bar, parity, abort_flag, P.status);
+            }
+        };
+        auto aborted = [&]() -> bool {
+            int v = lds_volatile(abort_flag);
+            if constexpr (WP) v = __shfl_sync(kFull, v, 0);
+            return v != 0;
+        };
+        if (lead) {
+            tc::prefetch_tensormap(&tm_q);
+            tc::prefetch_tensormap(&tm_k);
+            tc::prefetch_tensormap(&tm_v);
+            tc::prefetch_tensormap(&tm_o);
+        }
         uint32_t g = 0, wq = 0, ik = 0;
         auto publish = [&](int id, const Item &it) -> bool {
             const uint32_t slot = ik & 1;
-            if (!wait_or_abort(BAR(B_IE + slot), ((ik >> 1) & 1) ^ 1, abort_flag, P.status)) return false;
-            item_ring[slot] = id;
-            if (id < total_items) put_item(slot, it);
-            mbar_arrive(BAR(B_IF + slot));
+            if (!wwait(BAR(B_IE + slot), ((ik >> 1) & 1) ^ 1)) return false;
+            if (lead) {
+                item_ring[slot] = id;
+                if (id < total_items) put_item(slot, it);
+                mbar_arrive(BAR(B_IF + slot));
+            }
             ++ik;
             return true;
         };
+        auto next_ahead = [&]() -> unsigned {
+            unsigned a = 0;
+            if (lead) a = atomicAdd(P.items, 1u);
+            if constexpr (WP) a = __shfl_sync(kFull, a, 0);
+            return a;
+        };
         int t = (int)blockIdx.x < total_items ? (int)blockIdx.x : total_items;
         unsigned ahead = 0;                                // the counter's answer for the item after t
-        if (dyn && t < total_items) ahead = atomicAdd(P.items, 1u);
+        if (dyn && t < total_items) ahead = next_ahead();
         for (;; ++wq) {
             Item I;
             if (t < total_items) I = sched.get(t);
-            if (!publish(t, I) || t >= total_items || lds_volatile(abort_flag)) break;
+            if (!publish(t, I) || t >= total_items || aborted()) break;
             t = dyn ? (int)gridDim.x + (int)ahead : t + (int)gridDim.x;
-            if (dyn && t < total_items) ahead = atomicAdd(P.items, 1u);
-            if (!wait_or_abort(BAR(B_QE), (wq & 1) ^ 1, abort_flag, P.status)) break;
+            if (dyn && t < total_items) ahead = next_ahead();
+            if (!wwait(BAR(B_QE), (wq & 1) ^ 1)) break;
             const bool two = !WIDE && I.r0 + BM < I.L;
-            mbar_arrive_expect_tx(BAR(B_QF), (two ? 2 : 1) * TQ);
+            if (lead) {
+                mbar_arrive_expect_tx(BAR(B_QF), (two ? 2 : 1) * TQ);
 #pragma unroll
-            for (int x = 0; x < D; x += HD) {          // a 128-dim tile is two 64-dim boxes, 16 KB apart
-                tc::tma_load_3d(sb + OFF_Q + x * 256, &tm_q, x, I.h, I.s0 + I.r0, BAR(B_QF));
-                if (two) tc::tma_load_3d(sb + OFF_Q + TQ + x * 256, &tm_q, x, I.h, I.s0 + I.r0 + BM, BAR(B_QF));
+                for (int x = 0; x < D; x += HD) {      // a 128-dim tile is two 64-dim boxes, 16 KB apart
+                    tc::tma_load_3d(sb + OFF_Q + x * 256, &tm_q, x, I.h, I.s0 + I.r0, BAR(B_QF));
+                    if (two) tc::tma_load_3d(sb + OFF_Q + TQ + x * 256, &tm_q, x, I.h, I.s0 + I.r0 + BM, BAR(B_QF));
+                }
             }
             bool ok = true;
-            // paged: the block-table entries of key tile j + 1 are read while tile j
-            // waits for its stage, so the table's latency leaves the copy path
+            // paged: the block-table entry of this lane's block of key tile j + 1 is
+            // read while tile j waits for its stage, so the table's latency leaves
+            // the copy path
             auto tile_blocks = [&](int j) { return min(BN / CBS, (I.k_end - (I.c_lo + j * BN) + CBS - 1) / CBS); };
-            auto read_table = [&](int *ids, int j) {
-                const int nblk = tile_blocks(j);
+            const int lb = lane & (BN / CBS - 1);        // the lane's block within a key tile
+            auto read_table = [&](int j) -> int {
                 const int32_t *bt = P.block_tables + (size_t)I.seq * P.mbps + (I.c_lo + j * BN) / CBS;
-#pragma unroll
-                for (int b = 0; b < BN / CBS; ++b) ids[b] = b < nblk ? __ldg(bt + b) : 0;
+                return lb < tile_blocks(j) ? __ldg(bt + lb) : 0;
             };
-            int ids_next[BN / CBS];
-            if constexpr (PAGED) read_table(ids_next, 0);
+            int id_next = 0;
+            if constexpr (PAGED) id_next = read_table(0);
             // head dim 128: V of key tile number gv (global count) into its V slot
             auto load_v = [&](uint32_t gv, int row) -> bool {
                 const uint32_t vs = KSLOTS_128 + gv % VSLOTS_128;
-                if (!wait_or_abort(BAR(B_KVE + vs), ((gv / VSLOTS_128) & 1) ^ 1, abort_flag, P.status)) return false;
+                if (!wwait(BAR(B_KVE + vs), ((gv / VSLOTS_128) & 1) ^ 1)) return false;
                 mbar_arrive_expect_tx(BAR(B_KVF + vs), TKV);
 #pragma unroll
                 for (int x = 0; x < D; x += HD)
@@ -607,17 +639,16 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 return true;
             };
             for (int j = 0; j < I.nkv; ++j, ++g) {
-                int phys[BN / CBS];
+                int phys = 0;
                 if constexpr (PAGED) {
-#pragma unroll
-                    for (int b = 0; b < BN / CBS; ++b) phys[b] = ids_next[b];
-                    if (j + 1 < I.nkv) read_table(ids_next, j + 1);
+                    phys = id_next;
+                    if (j + 1 < I.nkv) id_next = read_table(j + 1);
                 }
                 if constexpr (WIDE) {
                     // K of key tile j, then V of key tile j - 1 (V one tile behind, so a
                     // K slot never waits for a V slot to drain)
                     const uint32_t kslot = g % KSLOTS_128;
-                    if (!wait_or_abort(BAR(B_KVE + kslot), ((g / KSLOTS_128) & 1) ^ 1, abort_flag, P.status)) {
+                    if (!wwait(BAR(B_KVE + kslot), ((g / KSLOTS_128) & 1) ^ 1)) {
                         ok = false;
                         break;
                     }
@@ -630,23 +661,23 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     continue;
                 }
                 const uint32_t st = g % NS;
-                if (!wait_or_abort(BAR(B_KVE + st), ((g / NS) & 1) ^ 1, abort_flag, P.status)) { ok = false; break; }
+                if (!wwait(BAR(B_KVE + st), ((g / NS) & 1) ^ 1)) { ok = false; break; }
                 const uint32_t dk = sb + OFF_KV + st * 2 * TKV, dv = dk + TKV;
                 if constexpr (PAGED) {
                     // the tile's cache blocks below k_end, one 16-row box each; a
                     // 2 KB box keeps the 1024-byte swizzle atoms of a contiguous tile
+                    // (lanes 0-7 the K boxes, lanes 8-15 the V boxes, of block lane % 8)
                     const int nblk = tile_blocks(j);
-                    mbar_arrive_expect_tx(BAR(B_KVF + st), 2u * nblk * CBLK_BYTES);
-#pragma unroll
-                    for (int b = 0; b < BN / CBS; ++b) {
-                        if (b >= nblk) break;
-                        int pb = phys[b];
+                    if (lead) mbar_arrive_expect_tx(BAR(B_KVF + st), 2u * nblk * CBLK_BYTES);
+                    __syncwarp();                      // the byte count is set before any copy lands
+                    if (lane < 2 * (BN / CBS) && lb < nblk) {
+                        int pb = phys;
                         if ((unsigned)pb >= (unsigned)P.num_blocks) {
                             flag_status(P.status, PKA_DEVCHK_BLOCK_ID);
                             pb = 0;
                         }
-                        tc::tma_load_4d(dk + b * CBLK_BYTES, &tm_k, 0, 0, I.h, pb, BAR(B_KVF + st));
-                        tc::tma_load_4d(dv + b * CBLK_BYTES, &tm_v, 0, 0, I.h, pb, BAR(B_KVF + st));
+                        if (lane < BN / CBS) tc::tma_load_4d(dk + lb * CBLK_BYTES, &tm_k, 0, 0, I.h, pb, BAR(B_KVF + st));
+                        else tc::tma_load_4d(dv + lb * CBLK_BYTES, &tm_v, 0, 0, I.h, pb, BAR(B_KVF + st));
                     }
                 } else {
                     const int row = I.s0 + I.c_lo + j * BN;
@@ -1035,7 +1066,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         // its roles' code, so each role's code is compiled to its own count
         if (warp < 4) {
             regs_lower<REGS_COPY>();
-            if (warp == 0 && lane == 0) producer();
+            if (warp == 0 && (PAGED || lane == 0)) producer();
             else if ((warp == 1 || warp == MMA1_WARP) && lane == 0) mma_issuer();
             __syncwarp();
         } else {
