@@ -54,13 +54,16 @@
 // Sliding-window layers run an instance that sorts each 32-key chunk of a
 // tile into kept by no row of the warp (no max, no exponentials: P = 0), kept
 // whole, or kept in part (masked key by key).
-// Head dim 128 (packed keys, no bias): a work item is one query tile with one
-// softmax warpgroup, since S, O and P of a tile take 320 of the 512 TMEM
-// columns; every tile is two 64-dim boxes (the 128-byte swizzle spans 64
-// elements), QK takes 8 key-dim steps, P V two 64-column MMAs per key step.
-// K and V stream into separate slots (three K, two V), each freed by its own
-// MMA, so loads run two key tiles ahead; with a banded mask P alternates
-// between two TMEM buffers; outputs leave by plain stores.
+// Head dim 128 (packed keys, no bias): a work item is one query tile (two
+// tiles' S and O do not fit the 512 TMEM columns), and the two softmax
+// warpgroups split its S tile by columns: warpgroup h takes keys 64 h .. 64 h
+// + 63 of every key tile, with its own running max and sum, P and O
+// accumulator (P V of a half: the half's 64 keys of V into its own O), and the
+// two halves of a row are merged at the end of the item, each warpgroup
+// writing 64 of the row's 128 output dims.  Every tile is two 64-dim boxes
+// (the 128-byte swizzle spans 64 elements), QK takes 8 key-dim steps.  K and V
+// stream into separate slots (three K, two V), each freed by its own MMAs, so
+// loads run two key tiles ahead; outputs leave by plain stores.
 // Every wait is bounded: on a timeout the CTA records PKA_DEVCHK_TIMEOUT,
 // every role stops, TMEM is freed, and the kernel returns.
 #include <cuda.h>
@@ -111,18 +114,20 @@ constexpr uint32_t TAB_FLOATS = 2 * TILE_BYTES / 4;   // widened bias tables hel
 // Layout<NS, TAB>: TAB gives the bias table a region of its own (else it
 // takes the output staging tiles' place and the outputs go out by plain stores)
 // D is the head dim: 64, or 128 with every tile two 64-dim boxes (32 KB), one
-// query tile, 3 K + 2 V slots and no staging tiles (outputs by plain stores).
+// query tile, 3 K + 2 V slots and no staging tiles (outputs by plain stores;
+// their space holds the column halves' (m, l) exchange instead).
 template <int NS, bool TAB, int D = 64> struct Layout {
     static constexpr uint32_t TQ = BM * D * 2, TKV = BN * D * 2;    // bytes of a Q tile and of a K or V tile
     static constexpr uint32_t OFF_Q = 0;                             // 2 query tiles (1 at head dim 128)
     static constexpr uint32_t OFF_KV = (D == 128 ? 1 : 2) * TQ;      // NS x (K, V), or the K and V slots
     static constexpr uint32_t OFF_OST = OFF_KV + (D == 128 ? NS : 2 * NS) * TKV;   // 2 output staging tiles
-    static constexpr uint32_t OFF_BAR = OFF_OST + (D == 64 ? 2 * TILE_BYTES : 0);
+    // (head dim 128: no staging tiles; the two column halves' (m, l) per row, 2 KB)
+    static constexpr uint32_t OFF_BAR = OFF_OST + (D == 64 ? 2 * TILE_BYTES : 2 * BM * 8);
     // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], s_empty[2], p_full[2], o_full[2],
     // o_empty[2], item ring full[2] / empty[2]
     static constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NS, B_SF = 2 + 2 * NS, B_SE = B_SF + 2,
                          B_PF = B_SE + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_IF = B_OE + 2, B_IE = B_IF + 2,
-                         B_PE = B_IE + 2, NBAR = B_IE + 2 + (D == 128 ? 2 : 0);   // p_empty[2] at 128
+                         B_MX = B_IE + 2, NBAR = B_IE + 2 + (D == 128 ? 2 : 0);   // ml_full[2] at 128
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, abort flag, item ring [2]
     static constexpr uint32_t OFF_RING = (OFF_MISC + 16 + 127) / 128 * 128;   // the two ring entries' items (64 B each)
     static constexpr uint32_t OFF_SCHED = OFF_RING + 128;
@@ -141,9 +146,11 @@ constexpr uint32_t CBLK_BYTES = CBS * HD * 2;                                  /
 
 // TMEM columns of query tile w: S (f32) at 128 w, O (f32) at 256 + 64 w, P
 // (bf16 pairs) at 384 + 64 w: the 512 columns exactly.  At head dim 128 (one
-// tile): S at 0, O at 256..383, P at 384 (and 448 for a second P buffer)
+// tile, two column halves h): S at 0, P of half h at 128 + 32 h, O of half h
+// at 256 + 128 h
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_O = 256, COL_P = 384;
+constexpr uint32_t COL_P_128 = 128;                 // head dim 128: P of the two column halves
 
 // S = Q K^T (both K-major) and O += P V (V MN-major), for bf16 or f16 operands
 template <typename T> __host__ __device__ constexpr bool is_bf16() { return std::is_same<T, __nv_bfloat16>::value; }
@@ -260,6 +267,10 @@ struct Sched {
             I.jb[w] = (lo_w[w] - c_lo) / BN;
             I.je[w] = (hi_w[w] - c_lo) / BN;
         }
+        if (qt == 1) {                                 // the two column halves of the one tile
+            I.jb[1] = I.jb[0];
+            I.je[1] = I.je[0];
+        }
         return I;
     }
 };
@@ -324,12 +335,12 @@ __device__ __forceinline__ float write_p_tmem(const float *x, float scale_log2, 
 
 // The same P for one tile row into registers (pk[c] = keys 2c, 2c + 1), the
 // TMEM stores left to the caller; returns the f32 row sum
-template <typename T, bool SKIP>
+template <typename T, bool SKIP, int NC = BN>
 __device__ __forceinline__ float exp_pack(const float *x, float scale_log2, float mneg, uint32_t *pk, uint32_t dead)
 {
     float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < NC / 32; ++q4) {
         if (SKIP && ((dead >> q4) & 1u)) {
 #pragma unroll
             for (int c = 0; c < BN / 8; ++c) pk[q4 * (BN / 8) + c] = 0u;
@@ -388,25 +399,24 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 {
     constexpr bool SPLIT = PAGED || BIAS;             // registers moved to the softmax warpgroups
     static_assert(D == 64 || (D == 128 && !PAGED && !BIAS), "head dim 128: packed keys, no bias");
-    constexpr bool WIDE = D == 128;                   // one query tile per item (TMEM: 128 S + 128 O columns)
+    // Head dim 128: one query tile per item, its S tile split by columns
+    // between the two softmax warpgroups (warpgroup h takes keys 64 h .. 64 h
+    // + 63 of every key tile), each with its own running max and sum, P and O
+    // accumulator; the two halves are merged per row at the end of the item.
+    // TMEM: S at 0, P of half h at 128 + 32 h, O of half h at 256 + 128 h.
+    constexpr bool WIDE = D == 128;
     constexpr int QT = WIDE ? 1 : 2;                  // query tiles per item
-    // P in two TMEM buffers (the second query tile's columns are free at head
-    // dim 128): the softmax writes P of key tile j while P V of tile j - 1 still
-    // reads the other one.  Kept for the banded masks only (window 64 layer
-    // 0.586 -> 0.551 ms), since full attention measured slower with it
-    // (6.74 -> 7.08 ms)
-    constexpr bool PDB = WIDE && BAND;
-    // no bias, head dim 64: a key tile's exponentials run before the wait for
-    // the previous tile's P V, P held in registers until then (full-attention
-    // layer 1.737 -> 1.638 ms, window-64 layer 0.161 -> 0.157 ms, paged
-    // cross-attention 0.181 -> 0.178 ms; chunked unchanged).  The bias
-    // instances measured slightly slower with it, and head dim 128 1 % slower
-    constexpr bool EARLYP = !BIAS && !WIDE;
-    // a row of S (and at head dim 128 of O) read from TMEM by one 128-column
-    // load and one wait on the bias instances and the full-attention instance at
-    // head dim 128 (T5 encoder 0.373 -> 0.369 ms); the other instances spill
-    // more with it and measured 1-5 % slower, and keep two 64-column loads
-    constexpr bool LD128 = BIAS || (WIDE && !BAND);
+    constexpr int NCOL = WIDE ? BN / 2 : BN;          // score columns of a softmax warp's row
+    // no bias: a key tile's exponentials run before the wait for the previous
+    // tile's P V, P held in registers until then (full-attention layer 1.737 ->
+    // 1.638 ms, window-64 layer 0.161 -> 0.157 ms, paged cross-attention 0.181
+    // -> 0.178 ms; chunked unchanged).  The bias instances measured slightly
+    // slower with it
+    constexpr bool EARLYP = !BIAS;
+    // a row of S read from TMEM by one 128-column load and one wait on the bias
+    // instances (T5 encoder 0.373 -> 0.369 ms); the others spill more with it
+    // and measured 1-5 % slower, and keep two 64-column loads
+    constexpr bool LD128 = BIAS;
     constexpr int NS = nstages<PAGED, D>();
     constexpr bool TAB = own_table<PAGED, BIAS>();
     constexpr bool TMA_OUT = (!BIAS || TAB) && !WIDE;   // outputs through the staging tiles
@@ -416,7 +426,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                        OFF_MISC = LY::OFF_MISC, OFF_RING = LY::OFF_RING, OFF_SCHED = LY::OFF_SCHED;
     constexpr int B_QF = LY::B_QF, B_QE = LY::B_QE, B_KVF = LY::B_KVF, B_KVE = LY::B_KVE, B_SF = LY::B_SF,
                   B_SE = LY::B_SE, B_PF = LY::B_PF, B_OF = LY::B_OF, B_OE = LY::B_OE, B_IF = LY::B_IF, B_IE = LY::B_IE,
-                  B_PE = LY::B_PE, NBAR = LY::NBAR;
+                  B_MX = LY::B_MX, NBAR = LY::NBAR;
     constexpr int NTHREADS = nthreads<SPLIT>();
     constexpr int SOFTMAX_WARP0 = SPLIT ? 4 : 2;      // the 8 softmax warps follow
     constexpr int MMA1_WARP = SPLIT ? 2 : NTHREADS / 32 - 1;   // issues the MMAs of query tile 1
@@ -456,11 +466,14 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NBAR; ++i) {
+            // (head dim 128: both warpgroups read both O accumulators, so o_empty
+            // takes the 256 threads of both, and ml_full the 128 of one)
+            const bool by_both_softmax = WIDE && i >= B_OE && i < B_OE + 2;
             const bool by_softmax = (i >= B_SE && i < B_SE + 2) || (i >= B_PF && i < B_PF + 2) ||
-                                    (i >= B_OE && i < B_OE + 2);
+                                    (i >= B_OE && i < B_OE + 2) || (WIDE && i >= B_MX && i < B_MX + 2);
             const bool by_both_mma = i == B_QE || (i >= B_KVE && i < B_KVE + NS);
             const bool by_item_readers = i >= B_IE && i < B_IE + 2;   // 2 MMA threads + 8 softmax warps
-            mbar_init(BAR(i), by_softmax ? 128 : by_both_mma ? 2 : by_item_readers ? 10 : 1);
+            mbar_init(BAR(i), by_both_softmax ? 256 : by_softmax ? 128 : by_both_mma ? 2 : by_item_readers ? 10 : 1);
         }
         sts_volatile(abort_flag, 0);
     }
@@ -708,30 +721,34 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             if (t >= total_items || lds_volatile(abort_flag)) break;
             if (!wait_or_abort(BAR(B_QF), wq & 1, abort_flag, P.status)) break;
             const bool mine = I.jb[w] <= I.je[w];
-            if (!mine) mbar_arrive(BAR(B_QE));
+            // (head dim 128: thread 0 issues every QK, thread 1 only its half's P V)
+            if (!mine || (WIDE && w == 1)) mbar_arrive(BAR(B_QE));
             // S_w = Q_w K_j^T, when query tile w needs key tile j
             auto issue_qk = [&](int j) -> bool {
                 const uint32_t gg = g + j;
                 if constexpr (WIDE) {
-                    // key tile j's K slot; released once this QK is done (or at once
-                    // by the thread whose query tile does not use it)
+                    // key tile j's K slot; released once this QK is done (and at once
+                    // by thread 1).  The QK waits until both halves have read S.
                     const uint32_t ks = gg % KSLOTS_128;
                     if (!wait_or_abort(BAR(B_KVF + ks), (gg / KSLOTS_128) & 1, abort_flag, P.status)) return false;
-                    if (j < I.jb[w] || j > I.je[w]) {
+                    if (w == 1 || j < I.jb[w] || j > I.je[w]) {
                         mbar_arrive(BAR(B_KVE + ks));
                         return true;
                     }
                     const uint32_t c = cs + (j - I.jb[w]);
-                    if (!wait_or_abort(BAR(B_SE + w), (c & 1) ^ 1, abort_flag, P.status)) return false;
+                    if (!wait_or_abort(BAR(B_SE), (c & 1) ^ 1, abort_flag, P.status) ||
+                        !wait_or_abort(BAR(B_SE + 1), (c & 1) ^ 1, abort_flag, P.status))
+                        return false;
                     tc::fence_after_sync();
-                    const uint32_t qa = sb + OFF_Q + w * TQ, ka = sb + OFF_KV + ks * TKV;
+                    const uint32_t qa = sb + OFF_Q, ka = sb + OFF_KV + ks * TKV;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * TILE_BYTES + (kk & 3) * 32;
-                        tc::mma_bf16(tmem + COL_S + w * BN, tc::sw128_desc(qa + off), tc::sw128_desc(ka + off),
-                                     idesc_qk<T>(), kk > 0);
+                        tc::mma_bf16(tmem + COL_S, tc::sw128_desc(qa + off), tc::sw128_desc(ka + off), idesc_qk<T>(),
+                                     kk > 0);
                     }
-                    tc::commit(BAR(B_SF + w));
+                    tc::commit(BAR(B_SF));
+                    tc::commit(BAR(B_SF + 1));
                     tc::commit(BAR(B_KVE + ks));
                     if (j == I.je[w]) tc::commit(BAR(B_QE));
                     return true;
@@ -769,20 +786,22 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 if (j == I.jb[w] && !wait_or_abort(BAR(B_OE + w), (co & 1) ^ 1, abort_flag, P.status)) return false;
                 tc::fence_after_sync();
                 const uint32_t va = WIDE ? sb + OFF_KV + st * TKV : sb + OFF_KV + st * 2 * TKV + TKV;
+                // (head dim 128: half w's 64 keys, 16-key groups 4 w .. 4 w + 3 of V,
+                // into half w's O; P of the half at column 128 + 32 w)
+                const uint32_t pcol = WIDE ? COL_P_128 + w * (NCOL / 2) : COL_P + w * (BN / 2);
+                const int kk0 = WIDE ? w * (NCOL / 16) : 0;
 #pragma unroll
                 for (int nh = 0; nh < D / HD; ++nh)          // the O columns of each 64-dim box of V
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        tc::mma_bf16_ta(tmem + COL_O + w * D + nh * HD,
-                                        tmem + COL_P + (PDB ? (c & 1) : w) * (BN / 2) + kk * 8,
-                                        tc::sw128_desc(va + nh * TILE_BYTES + kk * 2048), idesc_pv<T>(),
+                    for (int kk = 0; kk < NCOL / 16; ++kk)
+                        tc::mma_bf16_ta(tmem + COL_O + w * D + nh * HD, tmem + pcol + kk * 8,
+                                        tc::sw128_desc(va + nh * TILE_BYTES + (kk0 + kk) * 2048), idesc_pv<T>(),
                                         kk > 0 || j > I.jb[w]);
                 tc::commit(BAR(B_OF + w));
-                if constexpr (PDB) tc::commit(BAR(B_PE + (c & 1)));   // the P buffer is free again
                 tc::commit(BAR(B_KVE + st));
                 return true;
             };
-            if (w == 1 && I.je[0] - I.jb[0] >= LONG_ITEM_TILES - 1 && I.je[1] - I.jb[1] >= LONG_ITEM_TILES - 1) {
+            if (!WIDE && w == 1 && I.je[0] - I.jb[0] >= LONG_ITEM_TILES - 1 && I.je[1] - I.jb[1] >= LONG_ITEM_TILES - 1) {
                 // On a long item the second query tile starts about half a key tile
                 // after the first: both softmax warpgroups share each sub-partition's
                 // exponential unit, and offset their exponentials interleave instead
@@ -802,14 +821,14 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         }
     };
     auto softmax = [&]() {
-        // ======================= softmax (query tile w) =======================
+        // ============ softmax (query tile w; at head dim 128 column half w) ============
         const int w = (warp - SOFTMAX_WARP0) >> 2;
         const int quarter = warp & 3;                  // TMEM lanes this warp may touch
         const int row = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_addr + COL_S + w * BN;
+        const uint32_t tS = tmem + lane_addr + COL_S + w * (WIDE ? NCOL : BN);
         const uint32_t tO = tmem + lane_addr + COL_O + w * D;
-        const uint32_t tP = tmem + lane_addr + COL_P + w * (BN / 2);
+        const uint32_t tP = tmem + lane_addr + (WIDE ? COL_P_128 + w * (NCOL / 2) : COL_P + w * (BN / 2));
         uint32_t cs = 0, co = 0, g = 0;
         for (uint32_t kq = 0;; ++kq) {
             if (!wait_or_abort(BAR(B_IF + (kq & 1)), (kq >> 1) & 1, abort_flag, P.status)) break;
@@ -825,7 +844,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             if (t >= total_items || lds_volatile(abort_flag)) { release_item(); break; }
             const uint32_t g_item = g;                 // K/V stages of this item start at g_item
             g += I.nkv();
-            const int rr = I.r0() + w * BM + row;        // query row within its sequence
+            const int rr = I.r0() + (WIDE ? 0 : w) * BM + row;   // query row within its sequence
             if (I.jb(w) > I.je(w)) {
                 // past the sequence, or (paged) no key for any row of the tile: zero rows
                 if (PAGED && rr < I.L()) {
@@ -854,16 +873,16 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             for (int j = I.jb(w); j <= I.je(w); ++j, ++cs) {
                 if (!wait_or_abort(BAR(B_SF + w), cs & 1, abort_flag, P.status)) { ok = false; break; }
                 tc::fence_after_sync();
-                float x[BN];
+                float x[NCOL];
                 if constexpr (LD128) {
                     tc::tmem_ld128(tS, x);
                 } else {
                     tc::tmem_ld64(tS, x);
-                    tc::tmem_ld64(tS + 64, x + 64);
+                    if constexpr (NCOL == 128) tc::tmem_ld64(tS + 64, x + 64);
                 }
                 tc::fence_before_sync();
                 mbar_arrive(BAR(B_SE + w));            // S columns free: QK of the next key tile may start
-                const int c0 = I.c_lo() + j * BN;
+                const int c0 = I.c_lo() + j * BN + (WIDE ? w * NCOL : 0);   // the key of column 0
                 if constexpr (PAGED) {
                     // V rows at k_end and beyond hold unread blocks or cache rows
                     // past the context (any bits): zero them so that P = 0 there
@@ -894,7 +913,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     boff *= P.scale_log2;
                 }
                 // mask to the kept key range; tile max of the raw scores
-                float mx[4];
+                float mx[NCOL / 32];
                 uint32_t dead = 0;                     // 32-key chunks no row of the warp keeps
                 if constexpr (BAND) {
                     // banded masks (window, chunk, causal): per 32-key chunk, the
@@ -903,7 +922,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     // skips its max and (in write_p_tmem) its exponentials
                     const int ilo = lo - c0, ihi = hi - c0;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
+                    for (int k = 0; k < NCOL / 32; ++k) {
                         const int a = 32 * k;
                         if (__all_sync(kFull, ihi <= a || ilo >= a + 32)) {
                             dead |= 1u << k;
@@ -924,41 +943,36 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     }
                 } else {
                     const int ilo = lo - c0, ihi = hi - c0;
-                    const bool masked = ilo > 0 || ihi < BN;
+                    const bool masked = ilo > 0 || ihi < NCOL;
                     if (masked) {
-                        uint32_t mw[4];
+                        uint32_t mw[NCOL / 32];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
+                        for (int k = 0; k < NCOL / 32; ++k) {
                             const int a = min(max(ilo - 32 * k, 0), 32), b = min(max(ihi - 32 * k, 0), 32);
                             const uint32_t hiw = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
                             const uint32_t low = a >= 32 ? 0xffffffffu : ((1u << a) - 1u);
                             mw[k] = hiw & ~low;
                         }
 #pragma unroll
-                        for (int i = 0; i < BN; ++i) x[i] = (mw[i >> 5] & (1u << (i & 31))) ? x[i] : -INFINITY;
+                        for (int i = 0; i < NCOL; ++i) x[i] = (mw[i >> 5] & (1u << (i & 31))) ? x[i] : -INFINITY;
                     }
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
+                    for (int k = 0; k < NCOL / 32; ++k) {
                         float a0 = x[k * 32], a1 = x[k * 32 + 1];
 #pragma unroll
                         for (int i = 2; i < 32; i += 2) { a0 = fmaxf(a0, x[k * 32 + i]); a1 = fmaxf(a1, x[k * 32 + i + 1]); }
                         mx[k] = fmaxf(a0, a1);
                     }
                 }
-                const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * P.scale_log2 + boff;
+                float mxt;
+                if constexpr (NCOL == 128) mxt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                else mxt = fmaxf(mx[0], mx[1]);
+                const float mt = mxt * P.scale_log2 + boff;
                 // raise the running max only when it grows by more than 2^8
                 const bool raise = mt > m + RESCALE_LOG2;
                 const float m_old = m;
                 if (raise) m = mt;
-                if constexpr (PDB) {
-                    // P alternates between two buffers; the one written now is free
-                    // once the P V two key tiles back has read it
-                    if (!wait_or_abort(BAR(B_PE + (cs & 1)), ((cs >> 1) & 1) ^ 1, abort_flag, P.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after_sync();
-                } else if (!EARLYP && j > I.jb(w)) {
+                if (!EARLYP && j > I.jb(w)) {
                     // P V of the previous key tile is done: P may be overwritten, O rescaled
                     if (!wait_or_abort(BAR(B_OF + w), (cs - 1) & 1, abort_flag, P.status)) { ok = false; break; }
                     tc::fence_after_sync();
@@ -967,24 +981,19 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 // P = 2^(scale * s - m) as bf16 into the swizzled buffer; row sum in f32
                 const float mneg = (m == -INFINITY ? 0.f : -m) + boff;
                 if constexpr (EARLYP) {
-                    uint32_t pk[BN / 2];
-                    l += exp_pack<T, BAND>(x, P.scale_log2, mneg, pk, dead);
+                    uint32_t pk[NCOL / 2];
+                    l += exp_pack<T, BAND, NCOL>(x, P.scale_log2, mneg, pk, dead);
                     if (j > I.jb(w)) {
                         if (!wait_or_abort(BAR(B_OF + w), (cs - 1) & 1, abort_flag, P.status)) { ok = false; break; }
                         tc::fence_after_sync();
                     }
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) tc::tmem_st16(tP + q4 * (BN / 8), pk + q4 * (BN / 8));
+                    for (int q4 = 0; q4 < NCOL / 32; ++q4) tc::tmem_st16(tP + q4 * (BN / 8), pk + q4 * (BN / 8));
                 } else {
-                    l += write_p_tmem<T, BAND>(x, P.scale_log2, mneg, PDB ? tP + (cs & 1) * (BN / 2) : tP, dead);
+                    l += write_p_tmem<T, BAND>(x, P.scale_log2, mneg, tP, dead);
                 }
                 if (j > I.jb(w) && __any_sync(kFull, raise)) {
                     // the running max rose: bring this row's O to the new max (in TMEM)
-                    if (PDB) {
-                        // (P double-buffered) once the previous key tile's P V is done
-                        if (!wait_or_abort(BAR(B_OF + w), (cs - 1) & 1, abort_flag, P.status)) { ok = false; break; }
-                        tc::fence_after_sync();
-                    }
                     const float c = raise ? ex2(m_old - m) : 1.f;
 #pragma unroll
                     for (int x = 0; x < D; x += HD) {
@@ -1000,23 +1009,45 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 mbar_arrive(BAR(B_PF + w));
             }
             if (!ok) break;
-            // all key tiles done: read O, free the O columns, normalise, store.  With
-            // P double-buffered the softmax skips the o_full waits of tiles without
-            // a rescale, so o_full may still be two phases short here and its parity
-            // would alias: the last tile's p_empty phase, committed after its P V,
-            // is exact (the P V two tiles back is known done)
-            const uint32_t lt = cs - 1;
-            if (!(PDB ? wait_or_abort(BAR(B_PE + (lt & 1)), (lt >> 1) & 1, abort_flag, P.status)
-                       : wait_or_abort(BAR(B_OF + w), lt & 1, abort_flag, P.status)))
-                break;
+            // all key tiles done: read O, free the O columns, normalise, store
+            if (!wait_or_abort(BAR(B_OF + w), (cs - 1) & 1, abort_flag, P.status)) break;
             tc::fence_after_sync();
-            float o[D];
-            if constexpr (D == 128 && LD128) {
-                tc::tmem_ld128(tO, o);
-            } else {
-                tc::tmem_ld64(tO, o);
-                if constexpr (D == 128) tc::tmem_ld64(tO + HD, o + HD);
+            if constexpr (WIDE) {
+                // the two column halves of each row: trade (m, l) through shared
+                // memory, then half w writes output dims 64 w .. 64 w + 63 from both
+                // O accumulators, rescaled to the larger max
+                float2 *mlx = reinterpret_cast<float2 *>(smem + OFF_OST);
+                mlx[w * BM + row] = make_float2(m, l);
+                mbar_arrive(BAR(B_MX + w));
+                if (!wait_or_abort(BAR(B_MX + (1 - w)), co & 1, abort_flag, P.status)) break;
+                const float2 oth = mlx[(1 - w) * BM + row];
+                const float M = fmaxf(m, oth.x);
+                const float as = M == -INFINITY ? 0.f : ex2(m - M), ao = M == -INFINITY ? 0.f : ex2(oth.x - M);
+                const float L = l * as + oth.y * ao;
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                float o[HD], q[HD];
+                tc::tmem_ld64(tmem + lane_addr + COL_O + w * D + w * HD, o);         // this half's O
+                tc::tmem_ld64(tmem + lane_addr + COL_O + (1 - w) * D + w * HD, q);   // the other half's
+                tc::fence_before_sync();
+                mbar_arrive(BAR(B_OE));                // both O accumulators read by this warpgroup
+                mbar_arrive(BAR(B_OE + 1));
+                ++co;
+                if (rr < I.L()) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) +
+                                                           ((size_t)(I.s0() + rr) * P.H + I.h()) * D + w * HD);
+#pragma unroll
+                    for (int c = 0; c < HD / 8; ++c) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = (o[c * 8 + e] * as + q[c * 8 + e] * ao) * inv;
+                        dst[c] = Vec<T>::from_f32(v);
+                    }
+                }
+                release_item();
+                continue;
             }
+            float o[HD];
+            tc::tmem_ld64(tO, o);
             tc::fence_before_sync();
             mbar_arrive(BAR(B_OE + w));
             ++co;
@@ -1047,9 +1078,9 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 }
             } else if (rr < I.L()) {
                 // plain stores of the rows inside the sequence (its last, partial tile)
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) + ((size_t)(I.s0() + rr) * P.H + I.h()) * D);
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(P.out) + ((size_t)(I.s0() + rr) * P.H + I.h()) * HD);
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c) {
+                for (int c = 0; c < HD / 8; ++c) {
                     float v[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) v[e] = o[c * 8 + e] * inv;
