@@ -916,6 +916,7 @@ template <typename T, int D, int NSTAGE, int NW> struct Config {
 // The small-batch kernel: NW warps per CTA, one CTA per (sequence, head).
 constexpr int SMALL_NW = 4;
 constexpr int SMALL_MAX_BLOCKS = 32 * SMALL_NW;   // visible blocks one CTA's warps cover (one table entry per lane)
+constexpr int SMALL_SHORT_BLOCKS = 32;           // a pair this short stays cheap on one CTA of 4 warps
 
 template <typename T, int D, int NSTAGE> struct SmallConfig {
     using R = Tr<T, D>;
@@ -1059,9 +1060,10 @@ cudaError_t launch_paged_decode_multi(const DecodeArgs *a, const DecodePlan *siz
     // Batches of at most one (sequence, head) pair per SM, each pair's visible
     // blocks within one CTA's warps, go to the small-batch kernel: no prefix
     // scan and no global split-K merge (tiny f32 workload 6.7 -> 2.7 us a
-    // launch).  Larger batches stay on the persistent kernel, which measured
-    // as fast or faster from about 500 pairs on (T5-small: 11.4 against
-    // 11.6 us).
+    // launch).  So do batches of short contexts (at most SMALL_SHORT_BLOCKS
+    // visible blocks a pair) whose pairs fit the GPU's resident small-kernel
+    // CTAs at once, several to an SM (T5-small-shaped step 11.0 -> 10.9 us).
+    // Other batches stay on the persistent kernel.
     bool small = false;
     {
         long long pairs = 0, vb_max = 0;
@@ -1073,7 +1075,7 @@ cudaError_t launch_paged_decode_multi(const DecodeArgs *a, const DecodePlan *siz
         if (vb_max <= SMALL_MAX_BLOCKS && pairs <= MAX_SEQS_PER_LAUNCH * (long long)H) {
             const cudaError_t e = small_kernel_slots(a[0].dtype, a[0].head_dim, sms, &slots);
             if (e != cudaSuccess) return e;
-            small = pairs <= std::min<long long>(slots, sms);
+            small = pairs <= std::min<long long>(slots, sms) || (vb_max <= SMALL_SHORT_BLOCKS && pairs <= slots);
         }
     }
     const long long target = 3ll * sms * streaming_warps(a[0].dtype, a[0].head_dim);
