@@ -98,7 +98,7 @@ constexpr uint32_t REGS_COPY = 72, REGS_SOFTMAX = 216, REGS_AT_LAUNCH = 168;
 static_assert(REGS_COPY + 2 * REGS_SOFTMAX <= 3 * REGS_AT_LAUNCH, "the split fits the registers of the launch");
 constexpr float RESCALE_LOG2 = 8.f;
 constexpr int LONG_ITEM_TILES = 8;              // key tiles per query tile that make an item long
-constexpr long long TILE1_DELAY_CLOCKS = 2000;  // second query tile's start offset on long items
+constexpr long long TILE1_DELAY_CLOCKS = 1000;  // second query tile's start offset on long items
 
 constexpr uint32_t TILE_BYTES = BM * HD * 2;             // 16 KB: one Q, K or V tile
 // Shared memory and barriers of an instance with NS K/V stages.  The paged
@@ -802,11 +802,14 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 return true;
             };
             if (!WIDE && w == 1 && I.je[0] - I.jb[0] >= LONG_ITEM_TILES - 1 && I.je[1] - I.jb[1] >= LONG_ITEM_TILES - 1) {
-                // On a long item the second query tile starts about half a key tile
-                // after the first: both softmax warpgroups share each sub-partition's
-                // exponential unit, and offset their exponentials interleave instead
-                // of colliding (the offset carries through the item; full-attention
-                // layer 1.88 -> 1.78 ms).  A bounded wait on the clock.
+                // On a long item the second query tile starts a fraction of a key
+                // tile after the first: both softmax warpgroups share each
+                // sub-partition's exponential unit, and offset their exponentials
+                // interleave instead of colliding (the offset carries through the
+                // item; full-attention layer 1.88 -> 1.78 ms at 2000 cycles; with the
+                // exponentials ahead of the P V wait 0 / 500 / 1000 / 2000 / 3200
+                // cycles gave 1.775 / 1.743 / 1.629 / 1.640 / 1.657 ms).  A bounded
+                // wait on the clock.
                 const long long t0 = clock64();
                 while (clock64() - t0 < TILE1_DELAY_CLOCKS) {}
             }
