@@ -32,8 +32,9 @@
 // and the softmax in warps 4..11, with registers moved from warpgroup 0 to
 // the softmax warpgroups):
 //   warp 0      TMA producer: both query tiles, then the K/V tiles into a
-//               ring of 3 stages (4 for paged keys); everything lands
-//               128-byte swizzled.
+//               ring of 3 stages (4 for paged keys; there the whole warp
+//               issues a key tile's 16 cache-block boxes at once); everything
+//               lands 128-byte swizzled.
 //   warp 1      TMEM owner; with warp 10, one MMA-issuing thread per query
 //               tile (each blocks only on its own tile's barriers): per key
 //               tile, S = Q K^T (4 x 128x128x16) into that tile's S columns,
@@ -46,7 +47,9 @@
 //               loads its S row, frees the S columns at once, masks, takes
 //               the max (two-input max chains), and writes P = 2^(scale*s - m)
 //               as bf16 pairs into the tile's P columns of TMEM (tcgen05.st);
-//               the scale is folded into the exponent's FMA.  O stays in
+//               the scale is folded into the exponent's FMA.  Without bias the
+//               exponentials run before the wait for the previous key tile's
+//               P V, P held in registers until the store.  O stays in
 //               TMEM: the running max is raised only when a row's max grows
 //               by more than 2^8, and only then is that row of O rescaled in
 //               TMEM (rows never see P > 256).  Each warp normalises its 32
