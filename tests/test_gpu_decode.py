@@ -74,6 +74,19 @@ def test_decode_workload_parity(cuda_lib, n, bias):
     assert int(g.status.item()) == 0
 
 
+def test_short_context_batch_above_the_small_kernel_slots(cuda_lib):
+    """T5-small-shaped contexts (at most 32 cache blocks a pair) run on the
+    one-CTA-per-pair kernel while the batch's pairs fit its resident CTAs; 160
+    sequences x 8 heads (1280 pairs) exceed them and take the persistent
+    kernel with its split-K merge.  Both against the oracle, bias on."""
+    case = synth.decode_workload(2, num_seqs=160)
+    g = GpuDecode(case, cuda_lib)
+    got = to_f64(g.run(bias=True), case.dtype)
+    ref = oracle_decode(case, bias=True)
+    _check(got, ref, case.dtype, "short contexts, 1280 pairs")
+    assert int(g.status.item()) == 0
+
+
 def test_cross_attention_decode_parity(cuda_lib):
     """Cross-attention decode: its own block table and pool, encoder length
     512, no bias, no window."""
