@@ -20,7 +20,8 @@ batch of seeded synthetic input, already resident in HBM:
   long-ctx-decode    512 x 16 x 128 fp16, contexts log-U[16,8192], causal
         window 4096, bias [512,16,8192] N(0,0.25) NaN-padded.
   encoder-prefill    32 packed sequences U[128,8192], 12 heads x 64 bf16,
-        three layers: full, window 64, window 64 (bidirectional).
+        three layers: full, window 64, window 64 (bidirectional); with
+        --head-dim 128 the same shapes at head dim 128.
   chunked-prefill    the same sequences, one chunked-local layer (chunks of
         1024 positions, causal within the chunk).
   t5-encoder-prefill T5-large-shaped encoder self-attention: 256 x 512 tokens,
@@ -742,7 +743,7 @@ def build_prefill_launches(args, pka, device):
         elif w == "t5-encoder-prefill":
             layers = [synth.t5_encoder_prefill_workload(device=device)]
         else:
-            layers = [synth.prefill_workload(l, device=device) for l in range(3)]
+            layers = [synth.prefill_workload(l, device=device, head_dim=args.head_dim) for l in range(3)]
         cu = torch.from_numpy(layers[0].cu_seqlens).to(device)
         for c in layers:
             q, k, v = c.device_qkv
@@ -859,8 +860,9 @@ def run_prefill(args, rank, world, local, peaks):
     else:
         ach, peak, unit = launches[jd].nbytes / (launch_ms[jd] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
         peak_src = peaks["src"] + " hbm_gbs"
+    traffic_key = args.workload + ("" if args.head_dim == 64 else f"-d{args.head_dim}")
     roof = {"bound": bd["bound"], "achieved": round(ach, 2), "peak": peak, "unit": unit,
-            "frac": round(ach / peak, 4), "traffic": recorded_traffic("swa_prefill.cu", args.workload),
+            "frac": round(ach / peak, 4), "traffic": recorded_traffic("swa_prefill.cu", traffic_key),
             "kernel": kname, "alg_flops_per_launch": flops[jd], "alg_bytes_per_launch": launches[jd].nbytes,
             "frac_bf16": bd["frac_bf16"], "frac_hbm": bd["frac_hbm"],
             "intensity_flop_per_byte": bd["intensity_flop_per_byte"],
@@ -1179,7 +1181,7 @@ def _kept_keys(c, rows):
     return tot
 
 
-def host_prefill_cases(workload, small=False):
+def host_prefill_cases(workload, small=False, head_dim=64):
     """Host-drawn cases of a prefill workload for the oracle (small: fewer
     sequences of the same shape for the large T5 workloads)."""
     if workload == "chunked-prefill":
@@ -1188,7 +1190,7 @@ def host_prefill_cases(workload, small=False):
         return [synth.t5_encoder_prefill_workload(num_seqs=32 if small else 256)]
     if workload == "t5-paged-prefill":
         return list(synth.t5_paged_prefill_workload(num_seqs=32))
-    return [synth.prefill_workload(l) for l in range(3)]
+    return [synth.prefill_workload(l, head_dim=head_dim) for l in range(3)]
 
 
 def host_decode_cases(workload):
@@ -1202,11 +1204,11 @@ def host_decode_cases(workload):
     return [synth.decode_workload(n)], "the whole batch, drawn on the host"
 
 
-def oracle_leg(workload, budget_s):
+def oracle_leg(workload, budget_s, head_dim=64):
     """The fp64 oracle timed on the host cores on a bounded sample of the
     workload: (value, unit, threads, sample description, seconds)."""
     if workload in PREFILL_WORKLOADS:
-        cases = host_prefill_cases(workload, small=True)
+        cases = host_prefill_cases(workload, small=True, head_dim=head_dim)
         oracle_prefill_sample(cases, 0.5)             # warm-up: pages the arrays in
         f, s, th, desc = oracle_prefill_sample(cases, budget_s)
         if workload == "t5-paged-prefill" or workload == "t5-encoder-prefill":
@@ -1225,7 +1227,7 @@ def cpu_baseline(args):
     load = os.getloadavg()
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="1")
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-leg", "--workload", args.workload,
-           "--cpu-seconds", str(args.cpu_seconds)]
+           "--cpu-seconds", str(args.cpu_seconds), "--head-dim", str(args.head_dim)]
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600 + 4 * args.cpu_seconds)
     if r.returncode != 0:
         raise RuntimeError(f"oracle leg failed: {r.stderr[-2000:]}")
@@ -1236,7 +1238,7 @@ def cpu_baseline(args):
 
 
 def oracle_leg_main(args):
-    val, unit, th, desc, _ = oracle_leg(args.workload, args.cpu_seconds)
+    val, unit, th, desc, _ = oracle_leg(args.workload, args.cpu_seconds, args.head_dim)
     print(json.dumps({"value": round(val, 6), "unit": unit, "cores": th, "kind": "oracle", "sample": desc}),
           flush=True)
 
@@ -1248,11 +1250,12 @@ def run_reference(args, rank, world):
         return None
     per = max(0.25, args.ref_seconds / max(1, args.steps + args.warmup))
     load = os.getloadavg()
-    val, unit, th, desc, s = oracle_leg(args.workload, per * args.steps)
+    val, unit, th, desc, s = oracle_leg(args.workload, per * args.steps, args.head_dim)
     line = {"metric": METRIC, "value": round(val, 6), "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(s * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload}, "impl": "reference",
+            "config": ({"workload": args.workload} if args.head_dim == 64
+                       else {"workload": args.workload, "head_dim": args.head_dim}), "impl": "reference",
             "cpu_baseline": {"value": round(val, 6), "unit": unit, "cores": th, "kind": "oracle", "sample": desc,
                              "conditions": f"{th} oracle threads; host load average {load[0]:.2f} (1 min) before"},
             "e2e": {"value": round(val, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -1283,8 +1286,12 @@ def main():
     ap.add_argument("--per-config", dest="per_config", action="store_true", default=None,
                     help="also measure every target workload (default with one GPU and the default step)")
     ap.add_argument("--no-per-config", dest="per_config", action="store_false")
+    ap.add_argument("--head-dim", type=int, default=64, choices=[64, 128],
+                    help="encoder-prefill only: the head dim of its three layers")
     ap.add_argument("--oracle-leg", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.head_dim != 64 and args.workload != "encoder-prefill":
+        ap.error("--head-dim applies to --workload encoder-prefill only")
     args.warmup = max(3, args.warmup)
     if args.oracle_leg:
         oracle_leg_main(args)
@@ -1292,7 +1299,7 @@ def main():
     rank, world, local = dist_setup()
     if args.per_config is None:
         args.per_config = (world == 1 and not args.separate_launches and not args.t5_table
-                           and args.num_seqs is None)
+                           and args.num_seqs is None and args.head_dim == 64)
     if args.impl == "reference":
         line = run_reference(args, rank, world)
         if line is not None:

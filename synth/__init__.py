@@ -386,16 +386,18 @@ def prefill_seqlens(seed: int = 1004, num_seqs: int = 32, lo: int = 128, hi: int
     return rng.integers(lo, hi + 1, size=num_seqs).astype(np.int64)
 
 
-def prefill_workload(layer: int, device: Optional[str] = None, seqlens=None) -> PrefillCase:
+def prefill_workload(layer: int, device: Optional[str] = None, seqlens=None, head_dim: int = 64) -> PrefillCase:
     """Encoder-only bidirectional prefill, bf16, 12 heads x 64, 32 sequences
     with lengths U[128,8192] packed by cu_seqlens.  ``layer`` 0, 1, 2 selects
     the window of the alternating pattern (full, 64, 64) and its own seeded
-    q/k/v."""
+    q/k/v.  ``head_dim`` 128 gives the same shapes at head dim 128 (scale
+    1/sqrt(128))."""
     if seqlens is None:
         seqlens = prefill_seqlens()
     W = ENCODER_LAYER_WINDOWS[layer % 3]
-    return make_prefill_case(f"encoder-prefill-layer{layer}-w{W}", 1004 * 10 + layer, seqlens, 12, 64,
-                             W, 0, BF16, 1 / 8, device)
+    name = f"encoder-prefill-layer{layer}-w{W}" + ("" if head_dim == 64 else f"-d{head_dim}")
+    return make_prefill_case(name, 1004 * 10 + layer, seqlens, 12, head_dim, W, 0, BF16, 1 / math.sqrt(head_dim),
+                             device)
 
 
 CHUNKED_PREFILL_CHUNK = 1024

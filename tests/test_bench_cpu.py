@@ -83,3 +83,21 @@ def test_prefill_bound_picks_the_longer_of_flops_and_bytes():
     b = bench.prefill_bound(1.0e11, 1.0e9, 0.25, peaks)          # 100 FLOP/B: HBM-bound
     assert b["bound"] == "hbm" and b["frac_roofline"] == b["frac_hbm"] == 0.5
     assert b["frac_bf16"] == 0.2
+
+
+def test_head_dim_128_encoder_workload():
+    """--head-dim 128 gives the encoder workload's shapes at head dim 128 (its
+    oracle leg runs on them), and is refused for any other workload."""
+    sys.path.insert(0, ROOT)
+    import synth
+    c64, c128 = synth.prefill_workload(0), synth.prefill_workload(0, head_dim=128)
+    assert (c64.head_dim, c128.head_dim) == (64, 128)
+    assert c64.scale == 1 / 8 and abs(c128.scale - 128 ** -0.5) < 1e-12
+    assert (c64.cu_seqlens == c128.cu_seqlens).all() and c64.num_heads == c128.num_heads
+    assert c128.q.shape[-1] == 128
+    d = _run("--oracle-leg", "--workload", "encoder-prefill", "--head-dim", "128", "--cpu-seconds", "1")
+    assert d["unit"] == "TFLOP/s" and d["value"] > 0
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "tiny-decode",
+                        "--head-dim", "128"], capture_output=True, text=True, timeout=120,
+                       env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
+    assert r.returncode != 0 and "--head-dim" in r.stderr
