@@ -41,6 +41,15 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
            (1ull << 46) | (2ull << 61);
 }
 
+// The same for an MN-major operand wider than one 128-byte swizzle atom along
+// M or N: `lbo` is the byte distance between consecutive 64-element atoms along
+// that dimension (for example two 64-dim boxes of a 128-dim V tile).
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t lbo)
+{
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
 // Instruction descriptor, kind::f16 with 16-bit A and B of one type, f32
 // accumulator: D format f32 (1) at bits [4,6), A format at [7,10) and B format
 // at [10,13) (f16 = 0, bf16 = 1), A major at bit 15, B major at bit 16 (0 =

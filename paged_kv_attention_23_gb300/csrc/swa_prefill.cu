@@ -160,6 +160,7 @@ constexpr uint32_t COL_P_128 = 128;                 // head dim 128: P of the tw
 template <typename T> __host__ __device__ constexpr bool is_bf16() { return std::is_same<T, __nv_bfloat16>::value; }
 template <typename T> __host__ __device__ constexpr uint32_t idesc_qk() { return tc::idesc_16_f32(BM, BN, false, false, is_bf16<T>()); }
 template <typename T> __host__ __device__ constexpr uint32_t idesc_pv() { return tc::idesc_16_f32(BM, HD, false, true, is_bf16<T>()); }
+template <typename T> __host__ __device__ constexpr uint32_t idesc_pv128() { return tc::idesc_16_f32(BM, 2 * HD, false, true, is_bf16<T>()); }
 
 struct Params {
     void *out;                       // [T, H, 64] of the operand type
@@ -411,6 +412,12 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     constexpr bool WIDE = D == 128;
     constexpr int QT = WIDE ? 1 : 2;                  // query tiles per item
     constexpr int NCOL = WIDE ? BN / 2 : BN;          // score columns of a softmax warp's row
+    // head dim 128, full attention: MMA thread 0 issues only the QKs and thread
+    // 1 the P V of both halves (the issuing threads, not the tensor pipe, had
+    // set the pace: 5.42 -> 4.54 ms); the banded instance, whose items are a
+    // few key tiles long, keeps one half's P V per thread (0.456 -> 0.506 ms
+    // the other way)
+    constexpr bool PV_BY_1 = WIDE && !BAND;
     // no bias: a key tile's exponentials run before the wait for the previous
     // tile's P V, P held in registers until then (full-attention layer 1.737 ->
     // 1.638 ms, window-64 layer 0.161 -> 0.157 ms, paged cross-attention 0.181
@@ -475,7 +482,9 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             const bool by_both_softmax = WIDE && i >= B_OE && i < B_OE + 2;
             const bool by_softmax = (i >= B_SE && i < B_SE + 2) || (i >= B_PF && i < B_PF + 2) ||
                                     (i >= B_OE && i < B_OE + 2) || (WIDE && i >= B_MX && i < B_MX + 2);
-            const bool by_both_mma = i == B_QE || (i >= B_KVE && i < B_KVE + NS);
+            // (head dim 128, thread 1 issuing both halves' P V: a K slot is released
+            // by thread 0's QK alone)
+            const bool by_both_mma = i == B_QE || (i >= B_KVE + (PV_BY_1 ? KSLOTS_128 : 0) && i < B_KVE + NS);
             const bool by_item_readers = i >= B_IE && i < B_IE + 2;   // 2 MMA threads + 8 softmax warps
             mbar_init(BAR(i), by_both_softmax ? 256 : by_softmax ? 128 : by_both_mma ? 2 : by_item_readers ? 10 : 1);
         }
@@ -731,8 +740,11 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             auto issue_qk = [&](int j) -> bool {
                 const uint32_t gg = g + j;
                 if constexpr (WIDE) {
-                    // key tile j's K slot; released once this QK is done (and at once
-                    // by thread 1).  The QK waits until both halves have read S.
+                    // key tile j's K slot, released once this QK is done (and, when
+                    // thread 1 issues half 1's P V, at once by thread 1; when it issues
+                    // both halves' P V it leaves the K slots alone).  The QK waits until
+                    // both halves have read S.
+                    if (PV_BY_1 && w == 1) return true;
                     const uint32_t ks = gg % KSLOTS_128;
                     if (!wait_or_abort(BAR(B_KVF + ks), (gg / KSLOTS_128) & 1, abort_flag, P.status)) return false;
                     if (w == 1 || j < I.jb[w] || j > I.je[w]) {
@@ -776,8 +788,35 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             };
             // O_w += P_w V_j, then release the K/V stage (or just release it)
             auto issue_pv = [&](int j) -> bool {
-                // head dim 128: key tile j's V slot (filled after its K: wait for it
-                // here), released once this P V is done
+                if constexpr (PV_BY_1) {
+                    // head dim 128, full attention: thread 1 issues the P V of both
+                    // column halves, thread 0 only the QKs.  Key tile j's V slot (filled
+                    // after its K: waited for here) is released by one commit after each
+                    // half.  Half h: its 64 keys (16-key groups 4 h .. 4 h + 3 of V) into
+                    // its O, P of the half at column 128 + 32 h.
+                    if (w == 0) return true;
+                    const uint32_t st = KSLOTS_128 + (g + j) % VSLOTS_128;
+                    if (!wait_or_abort(BAR(B_KVF + st), ((g + j) / VSLOTS_128) & 1, abort_flag, P.status)) return false;
+                    const uint32_t c = cs + (j - I.jb[w]);
+                    const uint32_t va = sb + OFF_KV + st * TKV;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (!wait_or_abort(BAR(B_PF + h), c & 1, abort_flag, P.status)) return false;
+                        if (j == I.jb[w] && !wait_or_abort(BAR(B_OE + h), (co & 1) ^ 1, abort_flag, P.status))
+                            return false;
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int kk = 0; kk < NCOL / 16; ++kk)
+                            tc::mma_bf16_ta(tmem + COL_O + h * D, tmem + COL_P_128 + h * (NCOL / 2) + kk * 8,
+                                            tc::sw128_desc_mn(va + (h * (NCOL / 16) + kk) * 2048, TILE_BYTES),
+                                            idesc_pv128<T>(), kk > 0 || j > I.jb[w]);
+                        tc::commit(BAR(B_OF + h));
+                        tc::commit(BAR(B_KVE + st));
+                    }
+                    return true;
+                }
+                // head dim 128 (banded): key tile j's V slot (filled after its K: wait
+                // for it here), released once this P V is done
                 const uint32_t st = WIDE ? KSLOTS_128 + (g + j) % VSLOTS_128 : (g + j) % NS;
                 if (WIDE && !wait_or_abort(BAR(B_KVF + st), ((g + j) / VSLOTS_128) & 1, abort_flag, P.status))
                     return false;
@@ -794,13 +833,20 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 // into half w's O; P of the half at column 128 + 32 w)
                 const uint32_t pcol = WIDE ? COL_P_128 + w * (NCOL / 2) : COL_P + w * (BN / 2);
                 const int kk0 = WIDE ? w * (NCOL / 16) : 0;
-#pragma unroll
-                for (int nh = 0; nh < D / HD; ++nh)          // the O columns of each 64-dim box of V
+                if constexpr (WIDE) {
+                    // one N = 128 MMA per 16 keys over both 64-dim boxes of V (the
+                    // descriptor's leading byte offset steps from one box to the next)
 #pragma unroll
                     for (int kk = 0; kk < NCOL / 16; ++kk)
-                        tc::mma_bf16_ta(tmem + COL_O + w * D + nh * HD, tmem + pcol + kk * 8,
-                                        tc::sw128_desc(va + nh * TILE_BYTES + (kk0 + kk) * 2048), idesc_pv<T>(),
+                        tc::mma_bf16_ta(tmem + COL_O + w * D, tmem + pcol + kk * 8,
+                                        tc::sw128_desc_mn(va + (kk0 + kk) * 2048, TILE_BYTES), idesc_pv128<T>(),
                                         kk > 0 || j > I.jb[w]);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < NCOL / 16; ++kk)
+                        tc::mma_bf16_ta(tmem + COL_O + w * D, tmem + pcol + kk * 8,
+                                        tc::sw128_desc(va + (kk0 + kk) * 2048), idesc_pv<T>(), kk > 0 || j > I.jb[w]);
+                }
                 tc::commit(BAR(B_OF + w));
                 tc::commit(BAR(B_KVE + st));
                 return true;
