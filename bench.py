@@ -743,7 +743,8 @@ def build_prefill_launches(args, pka, device):
         elif w == "t5-encoder-prefill":
             layers = [synth.t5_encoder_prefill_workload(device=device)]
         else:
-            layers = [synth.prefill_workload(l, device=device, head_dim=args.head_dim) for l in range(3)]
+            layers = [synth.prefill_workload(l, device=device, head_dim=getattr(args, "head_dim", 64))
+                      for l in range(3)]
         cu = torch.from_numpy(layers[0].cu_seqlens).to(device)
         for c in layers:
             q, k, v = c.device_qkv
@@ -951,7 +952,7 @@ def per_config_records(args, world, local, peaks, headline):
             out[key] = headline
             continue
         if name == "encoder-prefill":
-            launches = build_prefill_launches(argparse.Namespace(workload=name), pka, device)
+            launches = build_prefill_launches(argparse.Namespace(workload=name, head_dim=64), pka, device)
             for _ in range(args.warmup):
                 for l in launches:
                     l()
