@@ -418,6 +418,10 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     // few key tiles long, keeps one half's P V per thread (0.456 -> 0.506 ms
     // the other way)
     constexpr bool PV_BY_1 = WIDE && !BAND;
+    // MMA descriptors built once per tile and stepped by offset adds (window
+    // 64 layer -1 %, paged -2 to -3 %, head dim 128 -2.5 to -3.6 %), except on
+    // the plain 64-dim instance, where that measured 1-2 % slower
+    constexpr bool DSTEP = PAGED || BIAS || BAND || WIDE;
     // no bias: a key tile's exponentials run before the wait for the previous
     // tile's P V, P held in registers until then (full-attention layer 1.737 ->
     // 1.638 ms, window-64 layer 0.161 -> 0.157 ms, paged cross-attention 0.181
@@ -756,12 +760,13 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                         !wait_or_abort(BAR(B_SE + 1), (c & 1) ^ 1, abort_flag, P.status))
                         return false;
                     tc::fence_after_sync();
-                    const uint32_t qa = sb + OFF_Q, ka = sb + OFF_KV + ks * TKV;
+                    // the tile's descriptors once, then stepped by the operands' byte
+                    // offsets (>> 4, added to the start-address field)
+                    const uint64_t dq = tc::sw128_desc(sb + OFF_Q), dk = tc::sw128_desc(sb + OFF_KV + ks * TKV);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * TILE_BYTES + (kk & 3) * 32;
-                        tc::mma_bf16(tmem + COL_S, tc::sw128_desc(qa + off), tc::sw128_desc(ka + off), idesc_qk<T>(),
-                                     kk > 0);
+                        const uint32_t off = ((kk >> 2) * TILE_BYTES + (kk & 3) * 32) >> 4;
+                        tc::mma_bf16(tmem + COL_S, dq + off, dk + off, idesc_qk<T>(), kk > 0);
                     }
                     tc::commit(BAR(B_SF));
                     tc::commit(BAR(B_SF + 1));
@@ -775,12 +780,19 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 const uint32_t c = cs + (j - I.jb[w]);
                 if (!wait_or_abort(BAR(B_SE + w), (c & 1) ^ 1, abort_flag, P.status)) return false;
                 tc::fence_after_sync();
+                // the tile's descriptors once, then stepped by the operands' byte offsets
+                // (>> 4, added to the start-address field); the plain instance builds
+                // each descriptor from its address (1-2 % faster there)
                 const uint32_t qa = sb + OFF_Q + w * TQ, ka = sb + OFF_KV + st * 2 * TKV;
+                const uint64_t dq = tc::sw128_desc(qa), dk = tc::sw128_desc(ka);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * TILE_BYTES + (kk & 3) * 32;   // box kk / 4, 16 dims in
-                    tc::mma_bf16(tmem + COL_S + w * BN, tc::sw128_desc(qa + off), tc::sw128_desc(ka + off),
-                                 idesc_qk<T>(), kk > 0);
+                    if constexpr (DSTEP)
+                        tc::mma_bf16(tmem + COL_S + w * BN, dq + (off >> 4), dk + (off >> 4), idesc_qk<T>(), kk > 0);
+                    else
+                        tc::mma_bf16(tmem + COL_S + w * BN, tc::sw128_desc(qa + off), tc::sw128_desc(ka + off),
+                                     idesc_qk<T>(), kk > 0);
                 }
                 tc::commit(BAR(B_SF + w));
                 if (j == I.je[w]) tc::commit(BAR(B_QE));         // last read of Q_w in this item
@@ -798,7 +810,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                     const uint32_t st = KSLOTS_128 + (g + j) % VSLOTS_128;
                     if (!wait_or_abort(BAR(B_KVF + st), ((g + j) / VSLOTS_128) & 1, abort_flag, P.status)) return false;
                     const uint32_t c = cs + (j - I.jb[w]);
-                    const uint32_t va = sb + OFF_KV + st * TKV;
+                    const uint64_t dv = tc::sw128_desc_mn(sb + OFF_KV + st * TKV, TILE_BYTES);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         if (!wait_or_abort(BAR(B_PF + h), c & 1, abort_flag, P.status)) return false;
@@ -808,8 +820,8 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 #pragma unroll
                         for (int kk = 0; kk < NCOL / 16; ++kk)
                             tc::mma_bf16_ta(tmem + COL_O + h * D, tmem + COL_P_128 + h * (NCOL / 2) + kk * 8,
-                                            tc::sw128_desc_mn(va + (h * (NCOL / 16) + kk) * 2048, TILE_BYTES),
-                                            idesc_pv128<T>(), kk > 0 || j > I.jb[w]);
+                                            dv + (((h * (NCOL / 16) + kk) * 2048) >> 4), idesc_pv128<T>(),
+                                            kk > 0 || j > I.jb[w]);
                         tc::commit(BAR(B_OF + h));
                         tc::commit(BAR(B_KVE + st));
                     }
@@ -829,6 +841,7 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                 if (j == I.jb[w] && !wait_or_abort(BAR(B_OE + w), (co & 1) ^ 1, abort_flag, P.status)) return false;
                 tc::fence_after_sync();
                 const uint32_t va = WIDE ? sb + OFF_KV + st * TKV : sb + OFF_KV + st * 2 * TKV + TKV;
+                const uint64_t dv = WIDE ? tc::sw128_desc_mn(va, TILE_BYTES) : tc::sw128_desc(va);
                 // (head dim 128: half w's 64 keys, 16-key groups 4 w .. 4 w + 3 of V,
                 // into half w's O; P of the half at column 128 + 32 w)
                 const uint32_t pcol = WIDE ? COL_P_128 + w * (NCOL / 2) : COL_P + w * (BN / 2);
@@ -839,13 +852,13 @@ swa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 #pragma unroll
                     for (int kk = 0; kk < NCOL / 16; ++kk)
                         tc::mma_bf16_ta(tmem + COL_O + w * D, tmem + pcol + kk * 8,
-                                        tc::sw128_desc_mn(va + (kk0 + kk) * 2048, TILE_BYTES), idesc_pv128<T>(),
-                                        kk > 0 || j > I.jb[w]);
+                                        dv + (((kk0 + kk) * 2048) >> 4), idesc_pv128<T>(), kk > 0 || j > I.jb[w]);
                 } else {
 #pragma unroll
                     for (int kk = 0; kk < NCOL / 16; ++kk)
                         tc::mma_bf16_ta(tmem + COL_O + w * D, tmem + pcol + kk * 8,
-                                        tc::sw128_desc(va + (kk0 + kk) * 2048), idesc_pv<T>(), kk > 0 || j > I.jb[w]);
+                                        DSTEP ? dv + (((kk0 + kk) * 2048) >> 4) : tc::sw128_desc(va + (kk0 + kk) * 2048),
+                                        idesc_pv<T>(), kk > 0 || j > I.jb[w]);
                 }
                 tc::commit(BAR(B_OF + w));
                 tc::commit(BAR(B_KVE + st));
