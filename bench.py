@@ -49,6 +49,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -110,8 +111,14 @@ def measured_peaks():
 
 
 def kernel_source_hash(name: str) -> str:
+    """sha1[:12] of a kernel source with its comments, blank lines and each
+    line's leading and trailing blanks removed (a comment edit leaves the
+    recorded counters valid; a code edit does not)."""
     path = os.path.join(ROOT, "paged_kv_attention_23_gb300", "csrc", name)
-    return hashlib.sha1(open(path, "rb").read()).hexdigest()[:12]
+    src = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+    lines = [re.sub(r"//.*$", "", ln).strip() for ln in src.splitlines()]
+    code = "\n".join(ln for ln in lines if ln)
+    return hashlib.sha1(code.encode()).hexdigest()[:12]
 
 
 def recorded_traffic(kernel_file: str, workload: str):

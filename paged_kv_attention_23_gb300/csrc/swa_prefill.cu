@@ -64,9 +64,12 @@
 // accumulator (P V of a half: the half's 64 keys of V into its own O), and the
 // two halves of a row are merged at the end of the item, each warpgroup
 // writing 64 of the row's 128 output dims.  Every tile is two 64-dim boxes
-// (the 128-byte swizzle spans 64 elements), QK takes 8 key-dim steps.  K and V
-// stream into separate slots (two K, three V), each freed by its own MMAs, so
-// loads run ahead of their use; outputs leave by plain stores.
+// (the 128-byte swizzle spans 64 elements), QK takes 8 key-dim steps, and P V
+// one N = 128 MMA per 16 keys across both boxes of V.  MMA thread 0 issues
+// every QK; on full attention thread 1 issues both halves' P V, on banded
+// masks each thread its own half's (issuing, not the tensor pipe, set the
+// pace).  K and V stream into separate slots (two K, three V), each freed by
+// its own MMAs; outputs leave by plain stores.
 // Every wait is bounded: on a timeout the CTA records PKA_DEVCHK_TIMEOUT,
 // every role stops, TMEM is freed, and the kernel returns.
 #include <cuda.h>

@@ -101,3 +101,19 @@ def test_head_dim_128_encoder_workload():
                         "--head-dim", "128"], capture_output=True, text=True, timeout=120,
                        env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
     assert r.returncode != 0 and "--head-dim" in r.stderr
+
+
+def test_kernel_source_hash_ignores_comments_only(tmp_path, monkeypatch):
+    """The recorded DRAM traffic is keyed by a hash of the kernel's code: a
+    comment or blank-line edit keeps the key, a code edit changes it."""
+    bench = _bench()
+    csrc = tmp_path / "paged_kv_attention_23_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    f = csrc / "k.cu"
+    f.write_text("// header\nint a = 1;  // trailing\n/* block\n comment */\nint b = 2;\n")
+    h0 = bench.kernel_source_hash("k.cu")
+    f.write_text("// another header\n\nint a = 1;\n/* other */ int b = 2;\n")
+    assert bench.kernel_source_hash("k.cu") == h0
+    f.write_text("int a = 1;\nint b = 3;\n")
+    assert bench.kernel_source_hash("k.cu") != h0
